@@ -1,0 +1,430 @@
+"""Plain, slow, double-precision CPU oracle for the int4g path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this module:
+only the tests, the smoke check and the benchmark's CPU-baseline leg do.  It
+shares no code with the CUDA library (no kernels, headers, tables or helpers);
+the two meet only through arrays produced by the seeded input generators.
+
+What it computes, and where it comes from:
+
+* int4g group quantization -- "FastLLM：零依赖CPU推理框架" (pgsm.cn), section
+  3.1 "4-bit 量化与权重重排": weights are quantized to 4 bits in groups, commonly
+  128 weights per group, each group sharing one scale and one zero point, and
+  dequantized to float inside the matmul.  The page gives no formula; the plain
+  asymmetric min/max rule is used:
+      s = (max - min) / 15,  s16 = fp16(s)  (round to nearest even)
+      z = clamp(round(-min / s16), 0, 15)
+      q = clamp(round(w / s16) + z, 0, 15)
+      w' = s16 * (q - z)
+  with round = half away from zero, computed in double.
+* the dequantized linear y = x . deq(W)^T  (same section: "read 4-bit weight ->
+  dequantize -> matmul" pipeline), and its elementwise error bound
+  |y - y_ref| <= 2e-3 * sum_k |x||w'| + 1e-5.
+* the tile-interleaved weight layout ("按组重排 ... 连续内存", same section):
+  an invertible byte/nibble permutation, restated here from its definition.
+* the routed MoE expert FFN with int4g experts -- fastllm README (gittoolsai
+  mirror), "2. 如何设定推理精度" (--moe_dtype int4g) and "5. 其它参数"
+  (--moe_experts = top-k, --cuda_se = shared expert): top-k routing,
+  permutation by expert, SwiGLU gate/up, down projection, gate-weighted
+  combine, plus an always-on shared expert with weight 1.
+
+Readings where the pages are silent (tie-breaks, constant groups, storage
+order, ...) are stated beside the code that takes them.
+
+Parity pins: every function here is checked by tests/test_oracle_pins.py
+against hand-worked cases (tests/golden/), closed forms, invariants and
+brute force.  None is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+GROUP = 128          # weights per group along K (FastLLM page, section 3.1)
+QMAX = 15            # 4-bit codes 0..15
+ROW_TILE = 128       # rows per super-block of the interleaved layout
+SB_NIB = 8192        # nibble bytes per super-block: 128 rows x 64 B
+SB_SCALE = 256       # 128 fp16 scales
+SB_ZERO = 64         # 128 4-bit zeros
+SB_BYTES = SB_NIB + SB_SCALE + SB_ZERO   # 8512
+
+
+# --------------------------------------------------------------------------
+# scalar helpers (exact definitions)
+# --------------------------------------------------------------------------
+
+def round_half_away(v):
+    """Round to the nearest integer, ties away from zero (C `round`).
+
+    Written as trunc + exact fractional part so that no addition of 0.5 can
+    round the argument itself (0.49999999999999994 stays 0).
+    """
+    v = np.asarray(v, dtype=np.float64)
+    t = np.trunc(v)
+    frac = v - t                      # exact in binary floating point
+    return t + np.where(np.abs(frac) >= 0.5, np.sign(v), 0.0)
+
+
+def fp16_bits(v):
+    """Correctly rounded (nearest even) double -> IEEE half, as uint16 bits."""
+    return np.asarray(v, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def fp16_value(bits):
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def bf16_value(bits):
+    """bf16 bit patterns (uint16) -> exact float64 values."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# a1: quantizer
+# --------------------------------------------------------------------------
+
+def quantize_group(w):
+    """Quantize one group (1-D array of fp32 values) -> (q[uint8], s16 bits, z).
+
+    Readings where the pages are silent:
+      * the scale used for z and q is the stored fp16 s16, so that the
+        dequantized weight is exactly what the stored triple encodes;
+      * a constant group c: c == 0 -> s16 = 0, z = 0, q = 0; c != 0 -> the
+        range [min(c, 0), max(c, 0)] is used, which reconstructs c;
+      * s16 == 0 after rounding (range below half the smallest fp16
+        subnormal times 15) -> treated as the zero group;
+      * s16 overflowing fp16 is an error (ValueError).
+    """
+    w = np.asarray(w, dtype=np.float32).astype(np.float64)
+    n = w.shape[0]
+    mn = w.min()
+    mx = w.max()
+    if mn == mx:
+        if mn == 0.0:
+            return np.zeros(n, np.uint8), np.uint16(0), 0
+        mn, mx = min(mn, 0.0), max(mx, 0.0)
+    s = (mx - mn) / QMAX
+    sbits = fp16_bits(s)
+    s16 = float(fp16_value(sbits))
+    if np.isinf(s16) or np.isnan(s16):
+        raise ValueError("group scale overflows fp16")
+    if s16 == 0.0:
+        return np.zeros(n, np.uint8), np.uint16(0), 0
+    z = int(np.clip(round_half_away(-mn / s16), 0, QMAX))
+    q = np.clip(round_half_away(w / s16) + z, 0, QMAX).astype(np.uint8)
+    return q, np.uint16(sbits), z
+
+
+def quantize(W, group=GROUP):
+    """W fp32 [N, K] -> canonical triple (Q, S, Z).
+
+    Q uint8 [N, K/2]       two codes per byte, low nibble = even k
+    S uint16 [N, G]        fp16 scale bits, G = K / group
+    Z uint8 [N, ceil(G/2)] two zero points per byte, low nibble = even g
+    """
+    W = np.asarray(W, dtype=np.float32)
+    N, K = W.shape
+    if K % group != 0 or K % 2 != 0:
+        raise ValueError("K must be a multiple of the group size")
+    G = K // group
+    q = np.zeros((N, K), np.uint8)
+    S = np.zeros((N, G), np.uint16)
+    z = np.zeros((N, G), np.uint8)
+    for n in range(N):
+        for g in range(G):
+            qq, sb, zz = quantize_group(W[n, g * group:(g + 1) * group])
+            q[n, g * group:(g + 1) * group] = qq
+            S[n, g] = sb
+            z[n, g] = zz
+    return pack_codes(q), S, pack_zeros(z)
+
+
+def pack_codes(q):
+    """codes uint8 [N, K] (0..15) -> bytes [N, K/2], low nibble = even k."""
+    q = np.asarray(q, np.uint8)
+    return (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_codes(Q):
+    Q = np.asarray(Q, np.uint8)
+    N, Kh = Q.shape
+    q = np.empty((N, 2 * Kh), np.uint8)
+    q[:, 0::2] = Q & 0xF
+    q[:, 1::2] = Q >> 4
+    return q
+
+
+def pack_zeros(z):
+    """zero points uint8 [N, G] -> bytes [N, ceil(G/2)], low nibble = even g."""
+    z = np.asarray(z, np.uint8)
+    N, G = z.shape
+    if G % 2:
+        z = np.concatenate([z, np.zeros((N, 1), np.uint8)], axis=1)
+    return (z[:, 0::2] | (z[:, 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_zeros(Z, G):
+    Z = np.asarray(Z, np.uint8)
+    z = np.empty((Z.shape[0], 2 * Z.shape[1]), np.uint8)
+    z[:, 0::2] = Z & 0xF
+    z[:, 1::2] = Z >> 4
+    return z[:, :G]
+
+
+def dequantize(Q, S, Z, group=GROUP):
+    """Canonical triple -> W' float64 [N, K], w' = s16 * (q - z) exactly."""
+    q = unpack_codes(Q).astype(np.float64)
+    N, K = q.shape
+    G = K // group
+    s = fp16_value(S).reshape(N, G)
+    z = unpack_zeros(Z, G).astype(np.float64)
+    qg = q.reshape(N, G, group)
+    return (s[:, :, None] * (qg - z[:, :, None])).reshape(N, K)
+
+
+# --------------------------------------------------------------------------
+# a3/a4: dequantized linear and its error bound
+# --------------------------------------------------------------------------
+
+def linear(x, Q, S, Z, group=GROUP):
+    """y[m, n] = sum_k x[m, k] * w'[n, k] in double.  x: float64 [M, K]."""
+    Wd = dequantize(Q, S, Z, group)
+    return np.asarray(x, np.float64) @ Wd.T
+
+
+def linear_tolerance(x, Q, S, Z, group=GROUP, rel=2e-3, abs_=1e-5):
+    """Elementwise bound rel * sum_k |x[m,k]| |w'[n,k]| + abs_."""
+    Wd = dequantize(Q, S, Z, group)
+    return rel * (np.abs(np.asarray(x, np.float64)) @ np.abs(Wd).T) + abs_
+
+
+def linear_columns(x, Q, S, Z, cols, group=GROUP):
+    """Only the output columns `cols` of linear() (for sampled checks at full
+    size): dequantizes just those weight rows.  Returns (y, tol)."""
+    cols = np.asarray(cols)
+    Wd = dequantize(Q[cols], S[cols], Z[cols], group)
+    x = np.asarray(x, np.float64)
+    return x @ Wd.T, 2e-3 * (np.abs(x) @ np.abs(Wd).T) + 1e-5
+
+
+# --------------------------------------------------------------------------
+# a2: tile-interleaved layout ("int4g-tiled")
+# --------------------------------------------------------------------------
+
+def tiled_bytes(N, K, group=GROUP):
+    Np = -(-N // ROW_TILE) * ROW_TILE
+    return (Np // ROW_TILE) * (K // group) * SB_BYTES
+
+
+def _nibble_address(kk):
+    """Position of logical column kk (0..127 inside a group) in a 64-byte
+    row of a super-block: returns (byte offset, nibble half).
+
+    The 16 32-bit words of a row hold 8 columns each; word slot p holds
+    logical word 4*(p%4) + p//4, and inside a word, nibble e holds column
+    offset 2*(e%4) + e//4.  Inverted: logical word wl -> p = 4*(wl%4) +
+    wl//4, offset o -> e = 4*(o%2) + o//2.
+    """
+    kk = np.asarray(kk)
+    wl, o = kk // 8, kk % 8
+    p = 4 * (wl % 4) + wl // 4
+    e = 4 * (o % 2) + o // 2
+    return 4 * p + e // 2, e % 2
+
+
+def repack(Q, S, Z, N, K, group=GROUP):
+    """Canonical triple -> interleaved byte array (uint8, tiled_bytes long).
+
+    Super-block (T, g) -- rows 128T..128T+127, group g -- starts at byte
+    (T * G + g) * 8512 and holds: 128 rows x 64 B of codes (row r at r*64,
+    columns placed by _nibble_address), then 128 fp16 scales (row r at
+    8192 + 2r, little endian), then 128 zero points (row r in byte
+    8448 + r//2, low nibble = even r).  Rows past N are zero.
+    """
+    if group != GROUP:
+        raise ValueError("the interleaved layout is defined for group 128")
+    G = K // group
+    Np = -(-N // ROW_TILE) * ROW_TILE
+    q = np.zeros((Np, K), np.uint8)
+    q[:N] = unpack_codes(Q)
+    s = np.zeros((Np, G), np.uint16)
+    s[:N] = S
+    z = np.zeros((Np, G), np.uint8)
+    z[:N] = unpack_zeros(Z, G)
+    out = np.zeros(tiled_bytes(N, K, group), np.uint8)
+    boff, half = _nibble_address(np.arange(GROUP))
+    rows = np.arange(ROW_TILE)
+    for T in range(Np // ROW_TILE):
+        for g in range(G):
+            base = (T * G + g) * SB_BYTES
+            blk = q[T * ROW_TILE:(T + 1) * ROW_TILE, g * group:(g + 1) * group]
+            nib = np.zeros((ROW_TILE, 64), np.uint8)
+            for kk in range(GROUP):
+                nib[:, boff[kk]] |= (blk[:, kk] << (4 * half[kk])).astype(np.uint8)
+            out[base:base + SB_NIB] = nib.reshape(-1)
+            sc = s[T * ROW_TILE:(T + 1) * ROW_TILE, g]
+            out[base + SB_NIB:base + SB_NIB + SB_SCALE] = sc.astype('<u2').view(np.uint8)
+            zz = z[T * ROW_TILE:(T + 1) * ROW_TILE, g]
+            zb = np.zeros(SB_ZERO, np.uint8)
+            for r in rows:
+                zb[r // 2] |= (zz[r] << (4 * (r % 2))).astype(np.uint8)
+            out[base + SB_NIB + SB_SCALE:base + SB_BYTES] = zb
+    return out
+
+
+def unrepack(buf, N, K, group=GROUP):
+    """Inverse of repack(): interleaved bytes -> canonical (Q, S, Z)."""
+    G = K // group
+    Np = -(-N // ROW_TILE) * ROW_TILE
+    buf = np.asarray(buf, np.uint8)
+    q = np.zeros((Np, K), np.uint8)
+    s = np.zeros((Np, G), np.uint16)
+    z = np.zeros((Np, G), np.uint8)
+    boff, half = _nibble_address(np.arange(GROUP))
+    rows = np.arange(ROW_TILE)
+    for T in range(Np // ROW_TILE):
+        for g in range(G):
+            base = (T * G + g) * SB_BYTES
+            nib = buf[base:base + SB_NIB].reshape(ROW_TILE, 64)
+            for kk in range(GROUP):
+                q[T * ROW_TILE:(T + 1) * ROW_TILE, g * group + kk] = (nib[:, boff[kk]] >> (4 * half[kk])) & 0xF
+            s[T * ROW_TILE:(T + 1) * ROW_TILE, g] = buf[base + SB_NIB:base + SB_NIB + SB_SCALE].view('<u2')
+            zb = buf[base + SB_NIB + SB_SCALE:base + SB_BYTES]
+            z[T * ROW_TILE:(T + 1) * ROW_TILE, g] = (zb[rows // 2] >> (4 * (rows % 2))) & 0xF
+    return pack_codes(q[:N]), s[:N].copy(), pack_zeros(z[:N])
+
+
+# --------------------------------------------------------------------------
+# a5: routing and permutation
+# --------------------------------------------------------------------------
+
+SOFTMAX = 0
+SIGMOID = 1
+
+
+def route(logits, k, scoring=SOFTMAX, renorm=True):
+    """Top-k routing of fp32 router logits [M, E].
+
+    Selection uses the raw fp32 logits: the k largest; equal logits go to
+    the lower expert index; slots are ordered by descending logit, then
+    ascending index.  Weights, in double:
+      softmax: w_j = exp(l_j - l_max) / sum_sel exp(l - l_max) when renorm,
+               else divided by the sum over all E (plain softmax);
+      sigmoid: w_j = sigma(l_j) / sum_sel sigma(l) when renorm, else sigma(l_j).
+    Returns ids int32 [M, k], weights float64 [M, k].
+    """
+    logits = np.asarray(logits, np.float32)
+    M, E = logits.shape
+    if not (1 <= k <= E):
+        raise ValueError("need 1 <= k <= E")
+    if np.isnan(logits).any():
+        raise ValueError("NaN router logit")
+    ids = np.zeros((M, k), np.int32)
+    wts = np.zeros((M, k), np.float64)
+    for t in range(M):
+        l = logits[t].astype(np.float64)
+        order = sorted(range(E), key=lambda e: (-l[e], e))
+        sel = np.array(order[:k])
+        ids[t] = sel
+        if scoring == SOFTMAX:
+            lmax = l[sel[0]]
+            ex = np.exp(l[sel] - lmax)
+            den = ex.sum() if renorm else np.exp(l - lmax).sum()
+            wts[t] = ex / den
+        elif scoring == SIGMOID:
+            sg = 1.0 / (1.0 + np.exp(-l[sel]))
+            wts[t] = sg / sg.sum() if renorm else sg
+        else:
+            raise ValueError("unknown scoring")
+    return ids, wts
+
+
+def permute(ids, E):
+    """Stable counting sort of the flattened assignments t*k + j by expert.
+
+    Returns (expert_offsets int32 [E+1] -- exclusive scan of per-expert
+    counts, perm int32 [M*k] -- perm[pos] = t*k + j, experts ascending and,
+    within an expert, flattened index ascending).
+    """
+    flat = np.asarray(ids, np.int64).reshape(-1)
+    counts = np.array([(flat == e).sum() for e in range(E)], np.int64)
+    offsets = np.zeros(E + 1, np.int64)
+    offsets[1:] = np.cumsum(counts)
+    perm = np.zeros(flat.size, np.int64)
+    fill = offsets[:-1].copy()
+    for i in range(flat.size):          # visiting i in order keeps it stable
+        e = flat[i]
+        perm[fill[e]] = i
+        fill[e] += 1
+    return offsets.astype(np.int32), perm.astype(np.int32)
+
+
+# --------------------------------------------------------------------------
+# a6/a7: expert FFN, combine, error bound
+# --------------------------------------------------------------------------
+
+def silu(a):
+    with np.errstate(over='ignore'):
+        return a / (1.0 + np.exp(-a))
+
+
+def silu_grad(a):
+    with np.errstate(over='ignore'):
+        sg = 1.0 / (1.0 + np.exp(-a))
+    return sg * (1.0 + a * (1.0 - sg))
+
+
+def expert_ffn(x, w13, w2, group=GROUP):
+    """One expert on tokens x float64 [T, H].
+
+    w13 = (Q, S, Z) of [2I, H]: rows 0..I-1 gate, rows I..2I-1 up.
+    w2  = (Q, S, Z) of [H, I].
+    h = silu(G x) * (U x);  out = W2 h.
+    Returns (out [T, H], tol_out [T, H]) where tol_out bounds the error of a
+    path that rounds h to bf16 and computes both projections to the linear
+    bound (2e-3 relative to sum |a||w'|):
+      tol_h = 2e-3 (|silu'(g)| A_g |u| + |silu(g)| A_u) + 2e-3 |h|
+      tol_out = 2e-3 |h| |W2'|^T + tol_h |W2'|^T
+    """
+    W13 = dequantize(*w13, group=group)
+    W2 = dequantize(*w2, group=group)
+    I = W13.shape[0] // 2
+    x = np.asarray(x, np.float64)
+    gu = x @ W13.T
+    A = np.abs(x) @ np.abs(W13).T
+    g, u = gu[:, :I], gu[:, I:]
+    Ag, Au = A[:, :I], A[:, I:]
+    h = silu(g) * u
+    tol_h = 2e-3 * (np.abs(silu_grad(g)) * Ag * np.abs(u) + np.abs(silu(g)) * Au) + 2e-3 * np.abs(h)
+    out = h @ W2.T
+    tol = 2e-3 * (np.abs(h) @ np.abs(W2).T) + tol_h @ np.abs(W2).T
+    return out, tol
+
+
+def moe(x, logits, k, w13, w2, scoring=SOFTMAX, renorm=True,
+        shared_w13=None, shared_w2=None, group=GROUP):
+    """Routed MoE layer with int4g experts, in double.
+
+    x float64 [M, H]; logits fp32 [M, E]; w13[e], w2[e] canonical triples
+    (any indexable, fetched only for experts that receive tokens).
+    y[t] = sum_j w_{t,j} * expert_{ids[t,j]}(x[t])  (+ shared(x[t]) * 1).
+    Returns (y, tol, ids, weights) with tol the propagated elementwise bound
+    (the per-expert bound above, weighted by the gate weights, + 1e-5).
+    """
+    x = np.asarray(x, np.float64)
+    M, H = x.shape
+    ids, wts = route(logits, k, scoring, renorm)
+    y = np.zeros((M, H))
+    tol = np.zeros((M, H))
+    for e in np.unique(ids):
+        tok, slot = np.nonzero(ids == e)
+        out, t_out = expert_ffn(x[tok], w13[e], w2[e], group)
+        wv = wts[tok, slot][:, None]
+        for i in range(tok.size):      # a token meets an expert at most once
+            y[tok[i]] += wv[i] * out[i]
+            tol[tok[i]] += wv[i] * t_out[i]
+    if shared_w13 is not None:
+        out, t_out = expert_ffn(x, shared_w13, shared_w2, group)
+        y += out
+        tol += t_out
+    return y, tol + 1e-5, ids, wts

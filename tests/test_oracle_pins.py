@@ -1,0 +1,371 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself:
+hand-worked cases (tests/golden/), closed forms, invariants and brute force.
+CPU only."""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import int4g_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- scalars
+
+def test_round_half_away_cases():
+    v = np.array([0.5, -0.5, 1.5, 2.5, -2.5, 0.49999999999999994, -2.4, 7.0, -0.0])
+    want = np.array([1, -1, 2, 3, -3, 0, -2, 7, 0], dtype=np.float64)
+    assert np.array_equal(O.round_half_away(v), want)
+
+
+def _fp16_by_fractions(x):
+    """Nearest-even fp16 of a double, by exact rational arithmetic over a
+    window of candidate bit patterns around a first guess."""
+    fx = Fraction(x)
+    a = abs(fx)
+    guess = int(np.float16(abs(x)).view(np.uint16))
+    best = None
+    for bits in range(max(0, guess - 3), min(0x7BFF, guess + 3) + 1):
+        e, m = bits >> 10, bits & 0x3FF
+        val = Fraction(m, 1 << 24) if e == 0 else Fraction(1024 + m, 1024) * Fraction(2) ** (e - 15)
+        key = (abs(val - a), m & 1)
+        if best is None or key < best[0]:
+            best = (key, bits)
+    bits = best[1]
+    return bits | (0x8000 if fx < 0 else 0)
+
+
+def test_fp16_rounding_is_correct_from_double():
+    rng = np.random.default_rng([0, 99])
+    vals = list(rng.uniform(-3, 3, 12)) + list(rng.uniform(1e-7, 1e-5, 6))
+    # exact ties and near-ties that a float32 detour would round wrongly
+    vals += [1.0 + 2 ** -11, 1.0 + 2 ** -11 + 2 ** -40, 1.0 + 3 * 2 ** -11, 2 ** -25, 2 ** -25 + 2 ** -45]
+    for v in vals:
+        assert int(O.fp16_bits(v)) == _fp16_by_fractions(v), v
+
+
+# ---------------------------------------------------------- hand cases
+
+@pytest.mark.parametrize("name", ["quant_hand_g8.json", "quant_hand_g4.json"])
+def test_quantizer_hand_cases(name):
+    g = _load(name)
+    W = np.array(g["W"], np.float32)
+    group = g["group"]
+    Q, S, Z = O.quantize(W, group)
+    assert np.array_equal(S, np.array(g["s16_bits"], np.uint16))
+    G = W.shape[1] // group
+    assert np.array_equal(O.unpack_zeros(Z, G), np.array(g["z"], np.uint8))
+    assert np.array_equal(O.unpack_codes(Q), np.array(g["q"], np.uint8))
+    assert np.array_equal(O.dequantize(Q, S, Z, group), np.array(g["Wdeq"]))
+
+
+def test_linear_hand_case():
+    g = _load("quant_hand_g8.json")
+    Q, S, Z = O.quantize(np.array(g["W"], np.float32), 8)
+    x = np.array(g["x"])
+    assert np.array_equal(O.linear(x, Q, S, Z, 8), np.array(g["y"]))
+    # bound closed form: row 0 with x0 = ones -> 2e-3 * sum|w'| + 1e-5 = 2e-3*6 + 1e-5
+    tol = O.linear_tolerance(x, Q, S, Z, 8)
+    assert tol[0, 0] == pytest.approx(2e-3 * 6.0 + 1e-5, rel=1e-15)
+    assert tol.shape == (2, 4)
+
+
+def test_quantize_rejects_fp16_overflow():
+    W = np.zeros((1, 128), np.float32)
+    W[0, 0] = 3e6
+    W[0, 1] = -3e6
+    with pytest.raises(ValueError):
+        O.quantize(W)
+
+
+# ------------------------------------------------------ invariants
+
+def _on_grid(rng, N, K, group):
+    G = K // group
+    # fp16-exact positive normal scales
+    s16 = rng.uniform(1e-3, 0.05, (N, G)).astype(np.float16).astype(np.float64)
+    z = rng.integers(0, 16, (N, G))
+    q = rng.integers(0, 16, (N, G, group))
+    q[:, :, 0] = 0
+    q[:, :, 1] = 15
+    for n in range(N):           # scatter the forced extremes
+        for gg in range(G):
+            rng.shuffle(q[n, gg])
+    W = (s16[:, :, None] * (q - z[:, :, None])).reshape(N, K)
+    assert np.array_equal(W.astype(np.float32).astype(np.float64), W)
+    return W.astype(np.float32), s16, z, q.reshape(N, K)
+
+
+@pytest.mark.parametrize("group", [128, 8])
+def test_on_grid_weights_reconstruct_exactly(group):
+    rng = np.random.default_rng([0, 7, group])
+    W, s16, z, q = _on_grid(rng, 6, 4 * group, group)
+    Q, S, Z = O.quantize(W, group)
+    assert np.array_equal(O.fp16_value(S), s16)
+    assert np.array_equal(O.unpack_zeros(Z, W.shape[1] // group), z.astype(np.uint8))
+    assert np.array_equal(O.unpack_codes(Q), q.astype(np.uint8))
+    assert np.array_equal(O.dequantize(Q, S, Z, group), W.astype(np.float64))
+
+
+def test_quantization_error_is_at_most_half_a_step():
+    rng = np.random.default_rng([0, 8])
+    W = (rng.standard_normal((16, 512)) * 0.02).astype(np.float32)
+    Q, S, Z = O.quantize(W)
+    Wd = O.dequantize(Q, S, Z)
+    s = np.repeat(O.fp16_value(S), 128, axis=1)
+    err = np.abs(W.astype(np.float64) - Wd)
+    Wg = W.reshape(16, 4, 128)
+    extreme = ((Wg == Wg.min(axis=2, keepdims=True)) | (Wg == Wg.max(axis=2, keepdims=True))).reshape(16, 512)
+    assert np.all(err[~extreme] <= 0.5 * s[~extreme] * (1 + 1e-12))
+    assert np.all(err[extreme] <= 1.5 * s[extreme])
+    # the relative step of N(0, .02) groups of 128: range ~ 5 sigma -> s ~ 0.0067
+    assert 0.003 < s.mean() < 0.012
+
+
+def _brute_linear(x, Q, S, Z, group):
+    """Scalar loops over packed bytes: byte k//2, nibble k%2; zero byte g//2."""
+    M, K = x.shape
+    N = Q.shape[0]
+    y = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                b = int(Q[n, k // 2])
+                qv = (b >> 4) if (k % 2) else (b & 15)
+                gi = k // group
+                zb = int(Z[n, gi // 2])
+                zv = (zb >> 4) if (gi % 2) else (zb & 15)
+                sv = float(np.uint16(S[n, gi]).view(np.float16))
+                acc += float(x[m, k]) * sv * (qv - zv)
+            y[m, n] = acc
+    return y
+
+
+def test_linear_matches_bruteforce_loops():
+    rng = np.random.default_rng([0, 9])
+    group = 8
+    W = (rng.standard_normal((5, 24)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((3, 24))
+    Q, S, Z = O.quantize(W, group)
+    assert np.allclose(O.linear(x, Q, S, Z, group), _brute_linear(x, Q, S, Z, group), rtol=1e-13, atol=1e-15)
+    # operands not transposed: y[m, n] depends on x row m and weight row n only
+    y = O.linear(x, Q, S, Z, group)
+    y2 = O.linear(x[[2]], Q[[4]], S[[4]], Z[[4]], group)
+    assert y2[0, 0] == pytest.approx(y[2, 4], rel=1e-14)
+
+
+def test_linear_columns_equals_full():
+    rng = np.random.default_rng([0, 10])
+    W = (rng.standard_normal((20, 256)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((2, 256))
+    Q, S, Z = O.quantize(W)
+    yc, tc = O.linear_columns(x, Q, S, Z, [3, 17])
+    assert np.allclose(yc, O.linear(x, Q, S, Z)[:, [3, 17]], rtol=1e-14)
+    assert np.allclose(tc, O.linear_tolerance(x, Q, S, Z)[:, [3, 17]], rtol=1e-14)
+
+
+# ------------------------------------------------------ interleaved layout
+
+def test_repack_hand_bytes():
+    """Byte addresses worked by hand from the layout definition:
+    super-block (T, g) at (T*G+g)*8512; row r codes at r*64; column kk ->
+    word wl=kk//8, offset o=kk%8, slot p=4*(wl%4)+wl//4, nibble e=4*(o%2)+o//2,
+    byte 4p+e//2, high nibble iff e odd; scales at 8192+2r; zeros at
+    8448+r//2 (high nibble iff r odd)."""
+    N, K = 130, 256
+    G = 2
+    q = np.zeros((N, K), np.uint8)
+    q[0, 0] = 5        # T0 g0 r0 kk0: p0 e0 -> byte 0 low
+    q[0, 1] = 7        # kk1: o1 -> e4 -> byte 2 low
+    q[1, 8] = 9        # kk8: wl1 -> p4 -> byte 64+16 low
+    q[2, 127] = 3      # kk127: wl15 o7 -> p15 e7 -> byte 128+60+3 high
+    q[127, 130] = 15   # g1 kk2: p0, o2 -> e1 -> byte 0 high, row 127
+    q[129, 0] = 1      # T1 g0 r1
+    S = np.zeros((N, G), np.uint16)
+    S[3, 1] = 0x1234
+    z = np.zeros((N, G), np.uint8)
+    z[5, 0] = 11
+    buf = O.repack(O.pack_codes(q), S, O.pack_zeros(z), N, K)
+    assert buf.size == 2 * 2 * 8512
+    expect = {0: 0x05, 2: 0x07, 80: 0x09, 191: 0x30,
+              8512 + 8128: 0xF0,
+              8512 + 8192 + 6: 0x34, 8512 + 8192 + 7: 0x12,
+              8450: 0xB0,
+              2 * 8512 + 64: 0x01}
+    for addr, val in expect.items():
+        assert buf[addr] == val, (addr, buf[addr], val)
+    nz = set(np.nonzero(buf)[0].tolist())
+    assert nz == set(expect), nz ^ set(expect)
+
+
+def _brute_tiled_dequant(buf, N, K):
+    """Independent reader of the interleaved layout, element by element."""
+    G = K // 128
+    out = np.zeros((N, K))
+    for n in range(N):
+        T, r = divmod(n, 128)
+        for k in range(K):
+            g, kk = divmod(k, 128)
+            base = (T * G + g) * 8512
+            wl, o = divmod(kk, 8)
+            p = 4 * (wl % 4) + wl // 4
+            e = 4 * (o % 2) + o // 2
+            b = int(buf[base + r * 64 + 4 * p + e // 2])
+            qv = (b >> 4) if e % 2 else (b & 15)
+            sv = float(np.frombuffer(bytes(buf[base + 8192 + 2 * r: base + 8194 + 2 * r]), '<f2')[0])
+            zb = int(buf[base + 8448 + r // 2])
+            zv = (zb >> 4) if r % 2 else (zb & 15)
+            out[n, k] = sv * (qv - zv)
+    return out
+
+
+def test_repack_roundtrip_and_reader():
+    rng = np.random.default_rng([0, 11])
+    N, K = 136, 256   # a full tile + a ragged 8-row tail
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    Q, S, Z = O.quantize(W)
+    buf = O.repack(Q, S, Z, N, K)
+    assert buf.size == O.tiled_bytes(N, K) == 2 * 2 * 8512
+    Q2, S2, Z2 = O.unrepack(buf, N, K)
+    assert np.array_equal(Q, Q2) and np.array_equal(S, S2) and np.array_equal(Z, Z2)
+    sub = [0, 1, 77, 127, 128, 135]
+    ref = O.dequantize(Q, S, Z)
+    got = _brute_tiled_dequant(buf, N, K)
+    assert np.array_equal(got[sub], ref[sub])
+
+
+def test_byte_count_per_weight():
+    # 0.5 B codes + 2 B scale and 0.5 B zero per 128 weights = 0.51953125 B/weight
+    assert O.tiled_bytes(4096, 11008) == 4096 * 11008 * 0.51953125
+    # 7B-class model: 6.74e9 weights -> ~3.5 GB of int4g linears (the FastLLM page,
+    # section 4.2, quotes ~3.8 GB for a 4-bit 7B file including unquantized parts)
+    assert 3.3e9 < 6.74e9 * 0.51953125 < 3.8e9
+
+
+# ------------------------------------------------------ routing
+
+def test_route_ties_and_slot_order():
+    l = np.array([[1.0, 3.0, 3.0, 2.0], [0.0, 0.0, 0.0, 0.0]], np.float32)
+    ids, w = O.route(l, 2, O.SOFTMAX, True)
+    assert ids.tolist() == [[1, 2], [0, 1]]
+    assert np.allclose(w, 0.5, rtol=0, atol=1e-15)
+    ids, w = O.route(l, 3, O.SIGMOID, True)
+    assert ids.tolist() == [[1, 2, 3], [0, 1, 2]]
+    s3, s2 = 1 / (1 + math.exp(-3)), 1 / (1 + math.exp(-2))
+    assert np.allclose(w[0], [s3 / (2 * s3 + s2), s3 / (2 * s3 + s2), s2 / (2 * s3 + s2)], rtol=1e-14)
+    assert np.allclose(w[1], 1 / 3, rtol=1e-14)
+
+
+def test_route_softmax_closed_form():
+    ln3 = float(np.float32(math.log(3.0)))
+    l = np.array([[0.0, ln3, -50.0]], np.float32)
+    ids, w = O.route(l, 2, O.SOFTMAX, True)
+    assert ids.tolist() == [[1, 0]]
+    e = math.exp(ln3)
+    assert w[0].tolist() == pytest.approx([e / (1 + e), 1 / (1 + e)], rel=1e-14)
+    assert w[0, 0] == pytest.approx(0.75, rel=1e-7)
+    # no renorm: plain softmax over all three
+    ids, w = O.route(l, 2, O.SOFTMAX, False)
+    den = 1 + e + math.exp(-50.0)
+    assert w[0].tolist() == pytest.approx([e / den, 1 / den], rel=1e-14)
+    # sigmoid without renorm is the raw gate
+    ids, w = O.route(l, 1, O.SIGMOID, False)
+    assert w[0, 0] == pytest.approx(1 / (1 + math.exp(-ln3)), rel=1e-15)
+
+
+def test_route_renorm_equals_softmax_all_then_renormalise():
+    rng = np.random.default_rng([0, 12])
+    l = rng.standard_normal((5, 16)).astype(np.float32)
+    _, a = O.route(l, 4, O.SOFTMAX, True)
+    _, b = O.route(l, 4, O.SOFTMAX, False)
+    assert np.allclose(a, b / b.sum(axis=1, keepdims=True), rtol=1e-14)
+    assert np.allclose(a.sum(axis=1), 1.0, rtol=1e-14)
+
+
+def test_permute_hand_case_and_invariants():
+    ids = np.array([[2, 0], [0, 1], [2, 1]])
+    off, perm = O.permute(ids, 3)
+    assert off.tolist() == [0, 2, 4, 6]
+    assert perm.tolist() == [1, 2, 3, 5, 0, 4]
+    rng = np.random.default_rng([0, 13])
+    l = rng.standard_normal((37, 24)).astype(np.float32)
+    ids, _ = O.route(l, 5, O.SOFTMAX, True)
+    off, perm = O.permute(ids, 24)
+    assert off[-1] == 37 * 5 and np.all(np.diff(off) >= 0)
+    assert sorted(perm.tolist()) == list(range(37 * 5))
+    flat = ids.reshape(-1)
+    for e in range(24):
+        seg = perm[off[e]:off[e + 1]]
+        assert np.all(flat[seg] == e) and np.all(np.diff(seg) > 0)
+
+
+# ------------------------------------------------------ MoE
+
+def _experts(rng, E, H, I, group):
+    w13, w2 = [], []
+    for _ in range(E):
+        w13.append(O.quantize((rng.standard_normal((2 * I, H)) * 0.05).astype(np.float32), group))
+        w2.append(O.quantize((rng.standard_normal((H, I)) * 0.05).astype(np.float32), group))
+    return w13, w2
+
+
+def _brute_ffn(xv, w13, w2, group):
+    """Scalar loops: gate/up rows, silu via math.exp, down projection."""
+    W13 = _brute_linear(np.eye(w13[0].shape[1] * 2), *w13, group).T   # [2I, H]
+    W2 = _brute_linear(np.eye(w2[0].shape[1] * 2), *w2, group).T       # [H, I]
+    I = W13.shape[0] // 2
+    H = W2.shape[0]
+    h = []
+    for i in range(I):
+        gsum = sum(W13[i, c] * xv[c] for c in range(H))
+        usum = sum(W13[I + i, c] * xv[c] for c in range(H))
+        h.append(gsum / (1 + math.exp(-gsum)) * usum)
+    return np.array([sum(W2[n, i] * h[i] for i in range(I)) for n in range(H)])
+
+
+def test_expert_ffn_matches_bruteforce():
+    rng = np.random.default_rng([0, 14])
+    w13, w2 = _experts(rng, 1, 16, 8, 8)
+    x = rng.standard_normal((2, 16))
+    out, tol = O.expert_ffn(x, w13[0], w2[0], 8)
+    for t in range(2):
+        assert np.allclose(out[t], _brute_ffn(x[t], w13[0], w2[0], 8), rtol=1e-12, atol=1e-15)
+    assert np.all(tol > 0)
+
+
+def test_moe_all_experts_equal_logits_is_mean():
+    rng = np.random.default_rng([0, 15])
+    E, H, I = 4, 16, 8
+    w13, w2 = _experts(rng, E, H, I, 8)
+    x = rng.standard_normal((3, H))
+    logits = np.zeros((3, E), np.float32)
+    y, tol, ids, w = O.moe(x, logits, E, w13, w2, O.SOFTMAX, True, group=8)
+    mean = sum(_brute_ffn(x[0], w13[e], w2[e], 8) for e in range(E)) / E
+    assert np.allclose(y[0], mean, rtol=1e-12, atol=1e-15)
+    assert np.allclose(w, 1.0 / E)
+
+
+def test_moe_single_expert_and_shared():
+    rng = np.random.default_rng([0, 16])
+    E, H, I = 2, 16, 8
+    w13, w2 = _experts(rng, E, H, I, 8)
+    sw13, sw2 = _experts(rng, 1, H, I, 8)
+    x = rng.standard_normal((2, H))
+    logits = np.array([[0.3, -1.0], [-2.0, 0.5]], np.float32)
+    y, tol, ids, w = O.moe(x, logits, 1, w13, w2, O.SOFTMAX, True, group=8)
+    assert ids.tolist() == [[0], [1]] and np.all(w == 1.0)
+    assert np.allclose(y[0], _brute_ffn(x[0], w13[0], w2[0], 8), rtol=1e-12, atol=1e-15)
+    assert np.allclose(y[1], _brute_ffn(x[1], w13[1], w2[1], 8), rtol=1e-12, atol=1e-15)
+    ys, _, _, _ = O.moe(x, logits, 1, w13, w2, O.SIGMOID, True, shared_w13=sw13[0], shared_w2=sw2[0], group=8)
+    assert np.allclose(ys[1], _brute_ffn(x[1], w13[1], w2[1], 8) + _brute_ffn(x[1], sw13[0], sw2[0], 8),
+                       rtol=1e-12, atol=1e-15)
