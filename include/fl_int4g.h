@@ -1,0 +1,179 @@
+/*
+ * fl_int4g.h -- C ABI of the int4g (weight-only INT4, group-quantized) library
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The method: weights are stored as 4-bit codes in groups of 128 along K,
+ * each group sharing one scale and one zero point, and are dequantized inside
+ * the matrix product ("FastLLM: zero-dependency CPU inference framework",
+ * pgsm.cn, section 3.1 "4-bit quantization and weight reordering").  The
+ * linear and MoE layers that use it are selected in fastllm by
+ * `--dtype int4g` / `--moe_dtype int4g`, with `--moe_experts` (top-k) and
+ * `--cuda_se` (shared expert) (fastllm README, gittoolsai mirror, sections
+ * "2. 如何设定推理精度" and "5. 其它参数").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - W is [N, K] in nn.Linear order; y = x . deq(W)^T; x is [M, K] bf16,
+ *    row-major, y is [M, N] bf16, row-major.
+ *  - group must be 128 (the only group size the GPU kernels accept);
+ *    K % 128 == 0.
+ *  - Canonical int4g triple (the storage the quantizer produces):
+ *      q      uint8  [N, K/2]        codes 0..15, low nibble = even k
+ *      scales uint16 [N, K/128]      IEEE fp16 bit patterns
+ *      zeros  uint8  [N, ceil(G/2)]  zero points 0..15, low nibble = even g
+ *    Dequantized weight: w' = s16 * (q - z).
+ *  - Interleaved ("tiled") layout used by the matmul kernels, produced by
+ *    fl_int4g_repack: rows are padded to a multiple of 128; super-block
+ *    (T, g) -- rows 128T..128T+127, group g -- is 8512 contiguous bytes at
+ *    offset (T * G + g) * 8512:
+ *      [0, 8192)     codes, row r at r*64: logical column kk (0..127) goes to
+ *                    32-bit word slot p = 4*(wl%4) + wl/4 (wl = kk/8) and
+ *                    nibble e = 4*(o%2) + o/2 (o = kk%8) inside it, i.e.
+ *                    byte 4p + e/2, high nibble iff e is odd;
+ *      [8192, 8448)  128 fp16 scales, row r at 8192 + 2r (little endian);
+ *      [8448, 8512)  128 zero points, row r in byte 8448 + r/2, low nibble
+ *                    for even r.
+ *    Size: 0.51953125 bytes per weight (the same as the canonical triple),
+ *    plus padding rows.  Each super-block is one contiguous bulk copy.
+ *  - All device pointers must be 16-byte aligned.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream) and
+ *    allocates no memory: the caller owns all buffers, including the
+ *    workspaces whose sizes the *_workspace queries return.
+ *  - Workspaces must be zero-filled before their first use.  A successful
+ *    call leaves the workspace zero-filled again except for its scratch
+ *    areas, so one workspace can be reused by consecutive calls on one
+ *    stream.  Calls that run concurrently must not share a workspace.
+ *  - The first 16 bytes of every workspace are a device status block; kernels
+ *    OR error bits into it instead of trapping.  fl_int4g_status reads and
+ *    clears it.
+ *
+ * Return values: FL_OK (0) or one of the FL_ERR_* codes below.  Argument
+ * errors are detected on the host before anything is launched.
+ */
+#ifndef FL_INT4G_H
+#define FL_INT4G_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fl_stream_t; /* same object as cudaStream_t */
+
+#define FL_OK               0
+#define FL_ERR_ARG          1  /* null/misaligned pointer, bad size, K % 128 != 0, ... */
+#define FL_ERR_WORKSPACE    2  /* workspace smaller than the *_workspace query */
+#define FL_ERR_UNSUPPORTED  3  /* group != 128, shape beyond a kernel limit */
+#define FL_ERR_CUDA         4  /* a CUDA launch or query failed */
+#define FL_ERR_TIMEOUT      5  /* a device-side bounded wait ran out (status word) */
+#define FL_ERR_DEVICE_CHECK 6  /* a device-side check failed (status word) */
+#define FL_ERR_RANGE        7  /* a group scale overflowed fp16 while quantizing (status word) */
+
+#define FL_SOFTMAX 0
+#define FL_SIGMOID 1
+
+/* Human-readable name of a status code. Never NULL. */
+const char* fl_strerror(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fl_int4g_version(void);
+
+/* ---------------------------------------------------------------- status */
+
+/* Reads the device status block at `ws` (any workspace of this library, or
+ * the status buffer given to fl_int4g_quantize), clears it, and stores in
+ * *out FL_OK or the first device-side error recorded (FL_ERR_TIMEOUT,
+ * FL_ERR_DEVICE_CHECK, FL_ERR_RANGE).  Synchronizes `stream`. */
+int fl_int4g_status(void* ws, fl_stream_t stream, int* out);
+
+/* --------------------------------------------------------- a1: quantize */
+
+/* Online int4g quantization of fp32 weights w [N, K] (device) into the
+ * canonical triple (device buffers q, scales, zeros as above).  Per group of
+ * 128 along K, in double precision:
+ *   s = (max - min)/15, s16 = fp16(s) (nearest even),
+ *   z = clamp(round(-min/s16), 0, 15), q = clamp(round(w/s16) + z, 0, 15),
+ * round = half away from zero; a constant group c uses the range
+ * [min(c,0), max(c,0)]; a zero group or s16 == 0 gives s16 = z = q = 0.
+ * (FastLLM page, section 3.1: one scale and one zero point per group of
+ * 128.)  A group whose s16 overflows fp16 is written as zeros and
+ * FL_ERR_RANGE is recorded in the 16-byte device status block `status`
+ * (zero-filled before first use; read it with fl_int4g_status). */
+int fl_int4g_quantize(const float* w, int N, int K, int group,
+                      uint8_t* q, uint16_t* scales, uint8_t* zeros,
+                      void* status, fl_stream_t stream);
+
+/* ------------------------------------------------------------ a2: repack */
+
+/* Bytes of the interleaved layout for an [N, K] matrix (group 128). */
+int fl_int4g_repacked_bytes(int N, int K, int group, size_t* out);
+
+/* Canonical triple -> interleaved layout (FastLLM page, section 3.1:
+ * weights reordered by group so that the matmul reads one contiguous span).
+ * A pure, invertible permutation; bit-exact.  w_out must hold
+ * fl_int4g_repacked_bytes(N, K) bytes; padding rows are written as zero. */
+int fl_int4g_repack(const uint8_t* q, const uint16_t* scales, const uint8_t* zeros,
+                    int N, int K, int group, void* w_out, size_t w_out_bytes,
+                    fl_stream_t stream);
+
+/* Inverse of fl_int4g_repack (for bit-exact round trips). */
+int fl_int4g_unrepack(const void* w, size_t w_bytes, int N, int K, int group,
+                      uint8_t* q, uint16_t* scales, uint8_t* zeros, fl_stream_t stream);
+
+/* -------------------------------------------------- a3/a4: int4g linear */
+
+/* Workspace bytes needed by fl_int4g_linear for this shape. */
+int fl_int4g_linear_workspace(int M, int N, int K, size_t* out);
+
+/* y[m, n] = sum_g s16[n,g] * sum_{k in g} x[m,k] * (q[n,k] - z[n,g]),
+ * fp32 accumulation, bf16 output (FastLLM page, section 3.1: "read 4-bit
+ * weight -> dequantize -> matmul" in one pass).
+ *   x  bf16 [M, K] device, row-major     w  interleaved layout of W [N, K]
+ *   y  bf16 [M, N] device, row-major     ws workspace (see conventions)
+ * M >= 1.  M <= 32 runs the decode kernel (HBM-streaming, register-level
+ * dequantization, split over K across all SMs); larger M runs the prefill
+ * kernel.  Reduction order is fixed, so results are deterministic. */
+int fl_int4g_linear(const void* x, int M, int K, const void* w, int N,
+                    void* y, void* ws, size_t ws_bytes, fl_stream_t stream);
+
+/* ------------------------------------------------------- a5-a7: MoE layer */
+
+/* Workspace bytes needed by fl_moe_int4g. */
+int fl_moe_int4g_workspace(int M, int E, int k, int H, int I, int has_shared, size_t* out);
+
+/* Routed MoE expert FFN with int4g experts (fastllm README, sections
+ * "2. 如何设定推理精度" --moe_dtype int4g and "5. 其它参数" --moe_experts,
+ * --cuda_se):
+ *   route:   top-k of the fp32 router logits [M, E] per token (ties to the
+ *            lower expert index; slots ordered by descending logit, then
+ *            ascending index); weights softmax over the selected k
+ *            (FL_SOFTMAX, renorm=1), softmax over all E (renorm=0), or
+ *            sigmoid of the selected, divided by their sum when renorm=1;
+ *   permute: stable counting sort of assignments t*k+j by expert;
+ *   experts: h = silu(G x) * (U x) with [G; U] = deq(W13_e) [2I, H]
+ *            (gate rows first), h stored as bf16; out = deq(W2_e) h;
+ *   combine: y[t] = sum_j w_{t,j} out_{t,j} (+ shared(x[t]) with weight 1).
+ *   x       bf16 [M, H] device          logits fp32 [M, E] device
+ *   w13     E interleaved [2I, H] matrices, back to back (stride
+ *           fl_int4g_repacked_bytes(2I, H))
+ *   w2      E interleaved [H, I] matrices, back to back
+ *   shared_w13 / shared_w2   interleaved [2I, H] / [H, I] or both NULL
+ *   y       bf16 [M, H] device
+ *   topk_ids int32 [M, k], topk_w fp32 [M, k], expert_offsets int32 [E+1],
+ *   perm int32 [M*k] -- optional device outputs (NULL = not written).
+ * H % 128 == 0, I % 128 == 0, 1 <= k <= E <= 1024. */
+int fl_moe_int4g(const void* x, const float* logits, int M, int H, int E, int k, int I,
+                 int scoring, int renorm,
+                 const void* w13, const void* w2,
+                 const void* shared_w13, const void* shared_w2,
+                 void* y, int32_t* topk_ids, float* topk_w,
+                 int32_t* expert_offsets, int32_t* perm,
+                 void* ws, size_t ws_bytes, fl_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FL_INT4G_H */

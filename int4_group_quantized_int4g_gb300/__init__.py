@@ -1,0 +1,217 @@
+"""Python binding of the int4g C ABI (libfl_int4g.so, declared in include/fl_int4g.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  The library
+is loaded lazily and a missing library is an error: there is no fallback.
+
+Function names match the C entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+__all__ = [
+    "lib", "Int4gError", "FL_SOFTMAX", "FL_SIGMOID", "GROUP",
+    "fl_strerror", "fl_int4g_version", "fl_int4g_status",
+    "fl_int4g_quantize", "fl_int4g_repacked_bytes", "fl_int4g_repack", "fl_int4g_unrepack",
+    "fl_int4g_linear_workspace", "fl_int4g_linear",
+    "fl_moe_int4g_workspace", "fl_moe_int4g",
+]
+
+GROUP = 128
+FL_SOFTMAX = 0
+FL_SIGMOID = 1
+
+_c_size_p = ctypes.POINTER(ctypes.c_size_t)
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+
+# C signatures: name -> (restype, argtypes)
+SIGNATURES = {
+    "fl_strerror": (ctypes.c_char_p, [_i]),
+    "fl_int4g_version": (_i, []),
+    "fl_int4g_status": (_i, [_vp, _vp, ctypes.POINTER(_i)]),
+    "fl_int4g_quantize": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "fl_int4g_repacked_bytes": (_i, [_i, _i, _i, _c_size_p]),
+    "fl_int4g_repack": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, ctypes.c_size_t, _vp]),
+    "fl_int4g_unrepack": (_i, [_vp, ctypes.c_size_t, _i, _i, _i, _vp, _vp, _vp, _vp]),
+    "fl_int4g_linear_workspace": (_i, [_i, _i, _i, _c_size_p]),
+    "fl_int4g_linear": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
+    "fl_moe_int4g_workspace": (_i, [_i, _i, _i, _i, _i, _i, _c_size_p]),
+    "fl_moe_int4g": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
+                          _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+}
+
+_LIB = None
+
+
+class Int4gError(RuntimeError):
+    def __init__(self, where, code):
+        super().__init__(f"{where}: {fl_strerror(code)} (status {code})")
+        self.code = code
+
+
+def lib():
+    """The loaded C library (ctypes.CDLL).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(
+                f"{_build.LIB} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"`")
+        L = ctypes.CDLL(_build.LIB)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _check(where, rc):
+    if rc != 0:
+        raise Int4gError(where, rc)
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_WS = {}
+
+
+def _workspace(nbytes, device):
+    """A zero-filled workspace per (device, stream), grown on demand."""
+    torch = _torch()
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    buf = _WS.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _WS[key] = buf
+    return buf
+
+
+# ------------------------------------------------------------------ wrappers
+
+def fl_strerror(code):
+    return lib().fl_strerror(code).decode()
+
+
+def fl_int4g_version():
+    return lib().fl_int4g_version()
+
+
+def fl_int4g_status(ws, stream=None):
+    out = ctypes.c_int(0)
+    _check("fl_int4g_status", lib().fl_int4g_status(_p(ws), _stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def fl_int4g_repacked_bytes(N, K, group=GROUP):
+    out = ctypes.c_size_t(0)
+    _check("fl_int4g_repacked_bytes", lib().fl_int4g_repacked_bytes(N, K, group, ctypes.byref(out)))
+    return out.value
+
+
+def fl_int4g_quantize(w, group=GROUP, check=True):
+    """fp32 [N, K] CUDA tensor -> canonical (q uint8 [N, K/2], scales int16
+    [N, G] holding fp16 bits, zeros uint8 [N, ceil(G/2)])."""
+    torch = _torch()
+    N, K = w.shape
+    G = K // group
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    s = torch.empty((N, G), dtype=torch.int16, device=w.device)
+    z = torch.empty((N, (G + 1) // 2), dtype=torch.uint8, device=w.device)
+    st = torch.zeros(4, dtype=torch.int32, device=w.device)
+    _check("fl_int4g_quantize", lib().fl_int4g_quantize(_p(w), N, K, group, _p(q), _p(s), _p(z), _p(st), _stream()))
+    if check:
+        _check("fl_int4g_quantize (device)", fl_int4g_status(st))
+    return q, s, z
+
+
+def fl_int4g_repack(q, s, z, N, K, group=GROUP):
+    torch = _torch()
+    nbytes = fl_int4g_repacked_bytes(N, K, group)
+    w = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check("fl_int4g_repack",
+           lib().fl_int4g_repack(_p(q), _p(s), _p(z), N, K, group, _p(w), nbytes, _stream()))
+    return w
+
+
+def fl_int4g_unrepack(w, N, K, group=GROUP):
+    torch = _torch()
+    G = K // group
+    q = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    s = torch.empty((N, G), dtype=torch.int16, device=w.device)
+    z = torch.empty((N, (G + 1) // 2), dtype=torch.uint8, device=w.device)
+    _check("fl_int4g_unrepack",
+           lib().fl_int4g_unrepack(_p(w), w.numel(), N, K, group, _p(q), _p(s), _p(z), _stream()))
+    return q, s, z
+
+
+def fl_int4g_linear_workspace(M, N, K):
+    out = ctypes.c_size_t(0)
+    _check("fl_int4g_linear_workspace", lib().fl_int4g_linear_workspace(M, N, K, ctypes.byref(out)))
+    return out.value
+
+
+def fl_int4g_linear(x, w, N, y=None, ws=None):
+    """y[M, N] bf16 = x[M, K] bf16 . deq(W)^T, W given in the interleaved layout."""
+    torch = _torch()
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    nb = fl_int4g_linear_workspace(M, N, K)
+    if ws is None:
+        ws = _workspace(nb, x.device)
+    _check("fl_int4g_linear",
+           lib().fl_int4g_linear(_p(x), M, K, _p(w), N, _p(y), _p(ws), ws.numel(), _stream()))
+    return y
+
+
+def fl_moe_int4g_workspace(M, E, k, H, I, has_shared):
+    out = ctypes.c_size_t(0)
+    _check("fl_moe_int4g_workspace",
+           lib().fl_moe_int4g_workspace(M, E, k, H, I, int(bool(has_shared)), ctypes.byref(out)))
+    return out.value
+
+
+def fl_moe_int4g(x, logits, k, I, w13, w2, scoring=FL_SOFTMAX, renorm=True, shared_w13=None, shared_w2=None,
+                 y=None, topk_ids=None, topk_w=None, expert_offsets=None, perm=None, ws=None):
+    """Routed MoE layer.  w13 / w2: uint8 CUDA tensors holding the E
+    interleaved expert matrices back to back.  Optional routing outputs are
+    written when given."""
+    torch = _torch()
+    M, H = x.shape
+    E = logits.shape[1]
+    if y is None:
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    has_shared = shared_w13 is not None
+    nb = fl_moe_int4g_workspace(M, E, k, H, I, has_shared)
+    if ws is None:
+        ws = _workspace(nb, x.device)
+    _check("fl_moe_int4g",
+           lib().fl_moe_int4g(_p(x), _p(logits), M, H, E, k, I, scoring, int(bool(renorm)),
+                              _p(w13), _p(w2), _p(shared_w13), _p(shared_w2), _p(y),
+                              _p(topk_ids), _p(topk_w), _p(expert_offsets), _p(perm),
+                              _p(ws), ws.numel(), _stream()))
+    return y

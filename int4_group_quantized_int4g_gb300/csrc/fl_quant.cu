@@ -1,0 +1,238 @@
+// a1 online quantizer and a2 repack / unrepack kernels + their C ABI.
+//
+// Quantization rule (FastLLM page, section 3.1: groups of 128 weights along K,
+// one scale and one zero point per group), evaluated in double precision so
+// that every code decision is taken in one fixed precision:
+//   s = (max - min)/15, s16 = fp16(s), z = clamp(round(-min/s16), 0, 15),
+//   q = clamp(round(w/s16) + z, 0, 15), round = half away from zero.
+#include "fl_common.cuh"
+
+using namespace fl;
+
+namespace {
+
+__device__ __forceinline__ double round_half_away(double v) {
+  double t = trunc(v);
+  if (fabs(v - t) >= 0.5) t += copysign(1.0, v);
+  return t;
+}
+
+__device__ __forceinline__ int clamp15(double v) { return v < 0.0 ? 0 : (v > 15.0 ? 15 : static_cast<int>(v)); }
+
+// One warp per (row n, pair of groups 2gp, 2gp+1): the pair shares a zero byte.
+__global__ void k_quantize(const float* __restrict__ w, int N, int K, int G, uint8_t* __restrict__ q,
+                           uint16_t* __restrict__ sc, uint8_t* __restrict__ zr, int32_t* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int GP = (G + 1) / 2;
+  if (warp >= static_cast<long long>(N) * GP) return;
+  const int n = static_cast<int>(warp / GP);
+  const int gp = static_cast<int>(warp % GP);
+  uint32_t zbyte = 0;
+  for (int h = 0; h < 2; ++h) {
+    const int g = 2 * gp + h;
+    if (g >= G) break;
+    const float4 v = *reinterpret_cast<const float4*>(w + static_cast<size_t>(n) * K + g * kGroup + 4 * lane);
+    float mn = fminf(fminf(v.x, v.y), fminf(v.z, v.w));
+    float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    int bad = isnan(v.x) | isnan(v.y) | isnan(v.z) | isnan(v.w);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    double dmn = mn, dmx = mx;
+    bool zero = false;
+    if (dmn == dmx) {
+      if (dmn == 0.0) zero = true;
+      dmn = fmin(dmn, 0.0);
+      dmx = fmax(dmx, 0.0);
+    }
+    uint16_t sbits = 0;
+    double s16 = 0.0;
+    if (!zero) {
+      const __half hs = __double2half((dmx - dmn) / 15.0);
+      sbits = __half_as_ushort(hs);
+      s16 = static_cast<double>(__half2float(hs));
+      if (bad || isinf(s16) || isnan(s16)) {
+        if (lane == 0) set_status(status, FL_ERR_RANGE, n);
+        zero = true;
+        sbits = 0;
+      } else if (s16 == 0.0) {
+        zero = true;
+      }
+    }
+    int z = 0;
+    uint32_t packed = 0;
+    if (!zero) {
+      z = clamp15(round_half_away(-dmn / s16));
+      const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int qq = clamp15(round_half_away(static_cast<double>(vv[j]) / s16) + z);
+        packed |= static_cast<uint32_t>(qq) << (4 * j);
+      }
+    }
+    *reinterpret_cast<uint16_t*>(q + static_cast<size_t>(n) * (K / 2) + g * (kGroup / 2) + 2 * lane) =
+        static_cast<uint16_t>(packed);
+    if (lane == 0) sc[static_cast<size_t>(n) * G + g] = sbits;
+    zbyte |= static_cast<uint32_t>(z) << (4 * h);
+  }
+  if (lane == 0) zr[static_cast<size_t>(n) * GP + gp] = static_cast<uint8_t>(zbyte);
+}
+
+// Output nibble e holds canonical nibble 2*(e%4) + e/4 (even columns in the
+// low half-word, odd columns in the high half-word).
+__device__ __forceinline__ uint32_t canon_to_tiled_word(uint32_t cw) {
+  uint32_t o = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o |= ((cw >> (4 * (2 * (e & 3) + (e >> 2)))) & 15u) << (4 * e);
+  return o;
+}
+
+__device__ __forceinline__ uint32_t tiled_to_canon_word(uint32_t tw) {
+  uint32_t o = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o |= ((tw >> (4 * e)) & 15u) << (4 * (2 * (e & 3) + (e >> 2)));
+  return o;
+}
+
+// One block per super-block (T, g).
+__global__ void k_repack(const uint8_t* __restrict__ q, const uint16_t* __restrict__ sc,
+                         const uint8_t* __restrict__ zr, int N, int K, int G, uint8_t* __restrict__ out) {
+  const int sbi = blockIdx.x;
+  const int T = sbi / G, g = sbi % G;
+  const int ZB = (G + 1) / 2;
+  uint8_t* dst = out + static_cast<size_t>(sbi) * kSbBytes;
+  for (int wi = threadIdx.x; wi < kSbNib / 4; wi += blockDim.x) {
+    const int r = wi >> 4, p = wi & 15;
+    const int n = T * kRowTile + r;
+    uint32_t o = 0;
+    if (n < N) {
+      const int wl = 4 * (p & 3) + (p >> 2);
+      const uint32_t cw =
+          *reinterpret_cast<const uint32_t*>(q + static_cast<size_t>(n) * (K / 2) + g * (kGroup / 2) + 4 * wl);
+      o = canon_to_tiled_word(cw);
+    }
+    reinterpret_cast<uint32_t*>(dst)[wi] = o;
+  }
+  const int t = threadIdx.x;
+  if (t < kRowTile) {
+    const int n = T * kRowTile + t;
+    reinterpret_cast<uint16_t*>(dst + kSbNib)[t] = n < N ? sc[static_cast<size_t>(n) * G + g] : 0;
+  }
+  if (t < kRowTile / 2) {
+    uint32_t b = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int n = T * kRowTile + 2 * t + h;
+      if (n < N) b |= ((zr[static_cast<size_t>(n) * ZB + g / 2] >> (4 * (g & 1))) & 15u) << (4 * h);
+    }
+    dst[kSbNib + kSbScale + t] = static_cast<uint8_t>(b);
+  }
+}
+
+// One block per (T, pair of groups): a canonical zero byte spans two groups.
+__global__ void k_unrepack(const uint8_t* __restrict__ in, int N, int K, int G, uint8_t* __restrict__ q,
+                           uint16_t* __restrict__ sc, uint8_t* __restrict__ zr) {
+  const int ZB = (G + 1) / 2;
+  const int T = blockIdx.x / ZB, gp = blockIdx.x % ZB;
+  for (int h = 0; h < 2; ++h) {
+    const int g = 2 * gp + h;
+    if (g >= G) break;
+    const uint8_t* src = in + (static_cast<size_t>(T) * G + g) * kSbBytes;
+    for (int wi = threadIdx.x; wi < kSbNib / 4; wi += blockDim.x) {
+      const int r = wi >> 4, p = wi & 15;
+      const int n = T * kRowTile + r;
+      if (n >= N) continue;
+      const int wl = 4 * (p & 3) + (p >> 2);
+      *reinterpret_cast<uint32_t*>(q + static_cast<size_t>(n) * (K / 2) + g * (kGroup / 2) + 4 * wl) =
+          tiled_to_canon_word(reinterpret_cast<const uint32_t*>(src)[wi]);
+    }
+    const int t = threadIdx.x;
+    if (t < kRowTile) {
+      const int n = T * kRowTile + t;
+      if (n < N) sc[static_cast<size_t>(n) * G + g] = reinterpret_cast<const uint16_t*>(src + kSbNib)[t];
+    }
+  }
+  const int t = threadIdx.x;
+  if (t < kRowTile) {
+    const int n = T * kRowTile + t;
+    if (n < N) {
+      uint32_t b = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int g = 2 * gp + h;
+        if (g >= G) break;
+        const uint8_t* src = in + (static_cast<size_t>(T) * G + g) * kSbBytes;
+        b |= ((src[kSbNib + kSbScale + t / 2] >> (4 * (t & 1))) & 15u) << (4 * h);
+      }
+      zr[static_cast<size_t>(n) * ZB + gp] = static_cast<uint8_t>(b);
+    }
+  }
+}
+
+bool shape_ok(int N, int K, int group) { return N >= 1 && K >= kGroup && K % kGroup == 0 && group == kGroup; }
+
+size_t tiled_bytes(int N, int K) {
+  const size_t T = (static_cast<size_t>(N) + kRowTile - 1) / kRowTile;
+  return T * static_cast<size_t>(K / kGroup) * kSbBytes;
+}
+
+}  // namespace
+
+extern "C" int fl_int4g_repacked_bytes(int N, int K, int group, size_t* out) {
+  if (!out) return FL_ERR_ARG;
+  if (group != kGroup) return FL_ERR_UNSUPPORTED;
+  if (N < 1 || K < kGroup || K % kGroup) return FL_ERR_ARG;
+  *out = tiled_bytes(N, K);
+  return FL_OK;
+}
+
+extern "C" int fl_int4g_quantize(const float* w, int N, int K, int group, uint8_t* q, uint16_t* scales,
+                                 uint8_t* zeros, void* status, fl_stream_t stream) {
+  if (group != kGroup) return FL_ERR_UNSUPPORTED;
+  if (!shape_ok(N, K, group) || !w || !q || !scales || !zeros || !status) return FL_ERR_ARG;
+  if (!flh::aligned16(w) || !flh::aligned16(q) || !flh::aligned16(scales) || !flh::aligned16(zeros) ||
+      !flh::aligned16(status))
+    return FL_ERR_ARG;
+  const int G = K / kGroup;
+  const long long warps = static_cast<long long>(N) * ((G + 1) / 2);
+  const int threads = 256;
+  const long long blocks = (warps * 32 + threads - 1) / threads;
+  if (blocks > 0x7fffffffLL) return FL_ERR_UNSUPPORTED;
+  k_quantize<<<static_cast<unsigned>(blocks), threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      w, N, K, G, q, scales, zeros, static_cast<int32_t*>(status));
+  return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+}
+
+extern "C" int fl_int4g_repack(const uint8_t* q, const uint16_t* scales, const uint8_t* zeros, int N, int K,
+                               int group, void* w_out, size_t w_out_bytes, fl_stream_t stream) {
+  if (group != kGroup) return FL_ERR_UNSUPPORTED;
+  if (!shape_ok(N, K, group) || !q || !scales || !zeros || !w_out) return FL_ERR_ARG;
+  if (!flh::aligned16(q) || !flh::aligned16(scales) || !flh::aligned16(zeros) || !flh::aligned16(w_out))
+    return FL_ERR_ARG;
+  if (w_out_bytes < tiled_bytes(N, K)) return FL_ERR_ARG;
+  const int G = K / kGroup;
+  const long long blocks = static_cast<long long>((N + kRowTile - 1) / kRowTile) * G;
+  if (blocks > 0x7fffffffLL) return FL_ERR_UNSUPPORTED;
+  k_repack<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      q, scales, zeros, N, K, G, static_cast<uint8_t*>(w_out));
+  return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+}
+
+extern "C" int fl_int4g_unrepack(const void* w, size_t w_bytes, int N, int K, int group, uint8_t* q,
+                                 uint16_t* scales, uint8_t* zeros, fl_stream_t stream) {
+  if (group != kGroup) return FL_ERR_UNSUPPORTED;
+  if (!shape_ok(N, K, group) || !q || !scales || !zeros || !w) return FL_ERR_ARG;
+  if (!flh::aligned16(q) || !flh::aligned16(scales) || !flh::aligned16(zeros) || !flh::aligned16(w))
+    return FL_ERR_ARG;
+  if (w_bytes < tiled_bytes(N, K)) return FL_ERR_ARG;
+  const int G = K / kGroup;
+  const long long blocks = static_cast<long long>((N + kRowTile - 1) / kRowTile) * ((G + 1) / 2);
+  if (blocks > 0x7fffffffLL) return FL_ERR_UNSUPPORTED;
+  k_unrepack<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint8_t*>(w), N, K, G, q, scales, zeros);
+  return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+}

@@ -19,7 +19,10 @@ What it computes, and where it comes from:
   with round = half away from zero, computed in double.
 * the dequantized linear y = x . deq(W)^T  (same section: "read 4-bit weight ->
   dequantize -> matmul" pipeline), and its elementwise error bound
-  |y - y_ref| <= 2e-3 * sum_k |x||w'| + 1e-5.
+  |y - y_ref| <= 2e-3 * sum_k |x||w'| + 1e-5 on the fp32-accumulated result,
+  widened by the final bf16 store (at most 2^-8 of the stored value: bf16 has
+  8 significant bits, so that store alone can exceed the first term when
+  |y| > 0.51 * sum_k |x||w'|).
 * the tile-interleaved weight layout ("按组重排 ... 连续内存", same section):
   an invertible byte/nibble permutation, restated here from its definition.
 * the routed MoE expert FFN with int4g experts -- fastllm README (gittoolsai
@@ -46,6 +49,7 @@ SB_NIB = 8192        # nibble bytes per super-block: 128 rows x 64 B
 SB_SCALE = 256       # 128 fp16 scales
 SB_ZERO = 64         # 128 4-bit zeros
 SB_BYTES = SB_NIB + SB_SCALE + SB_ZERO   # 8512
+BF16_U = 2.0 ** -8   # unit roundoff of bf16 (8 significant bits): max relative rounding error
 
 
 # --------------------------------------------------------------------------
@@ -192,10 +196,18 @@ def linear(x, Q, S, Z, group=GROUP):
     return np.asarray(x, np.float64) @ Wd.T
 
 
+def _with_output_rounding(bound, y):
+    """A bound on the error before the final bf16 store, widened by that store:
+    rounding v to bf16 moves it by at most BF16_U*|v| <= BF16_U*(|y| + bound)."""
+    return bound * (1.0 + BF16_U) + BF16_U * np.abs(y)
+
+
 def linear_tolerance(x, Q, S, Z, group=GROUP, rel=2e-3, abs_=1e-5):
-    """Elementwise bound rel * sum_k |x[m,k]| |w'[n,k]| + abs_."""
+    """Elementwise bound rel * sum_k |x[m,k]| |w'[n,k]| + abs_ on the fp32
+    result, plus the rounding of the bf16 output (half an ulp, <= 2^-8 |y|)."""
     Wd = dequantize(Q, S, Z, group)
-    return rel * (np.abs(np.asarray(x, np.float64)) @ np.abs(Wd).T) + abs_
+    x = np.asarray(x, np.float64)
+    return _with_output_rounding(rel * (np.abs(x) @ np.abs(Wd).T) + abs_, x @ Wd.T)
 
 
 def linear_columns(x, Q, S, Z, cols, group=GROUP):
@@ -204,7 +216,8 @@ def linear_columns(x, Q, S, Z, cols, group=GROUP):
     cols = np.asarray(cols)
     Wd = dequantize(Q[cols], S[cols], Z[cols], group)
     x = np.asarray(x, np.float64)
-    return x @ Wd.T, 2e-3 * (np.abs(x) @ np.abs(Wd).T) + 1e-5
+    y = x @ Wd.T
+    return y, _with_output_rounding(2e-3 * (np.abs(x) @ np.abs(Wd).T) + 1e-5, y)
 
 
 # --------------------------------------------------------------------------
@@ -381,9 +394,9 @@ def expert_ffn(x, w13, w2, group=GROUP):
     w2  = (Q, S, Z) of [H, I].
     h = silu(G x) * (U x);  out = W2 h.
     Returns (out [T, H], tol_out [T, H]) where tol_out bounds the error of a
-    path that rounds h to bf16 and computes both projections to the linear
-    bound (2e-3 relative to sum |a||w'|):
-      tol_h = 2e-3 (|silu'(g)| A_g |u| + |silu(g)| A_u) + 2e-3 |h|
+    path that computes both projections to the linear bound (2e-3 relative
+    to sum |a||w'|, fp32 accumulation) and stores h in bf16:
+      tol_h = 2e-3 (|silu'(g)| A_g |u| + |silu(g)| A_u) + 2^-8 |h|
       tol_out = 2e-3 |h| |W2'|^T + tol_h |W2'|^T
     """
     W13 = dequantize(*w13, group=group)
@@ -395,7 +408,7 @@ def expert_ffn(x, w13, w2, group=GROUP):
     g, u = gu[:, :I], gu[:, I:]
     Ag, Au = A[:, :I], A[:, I:]
     h = silu(g) * u
-    tol_h = 2e-3 * (np.abs(silu_grad(g)) * Ag * np.abs(u) + np.abs(silu(g)) * Au) + 2e-3 * np.abs(h)
+    tol_h = 2e-3 * (np.abs(silu_grad(g)) * Ag * np.abs(u) + np.abs(silu(g)) * Au) + BF16_U * np.abs(h)
     out = h @ W2.T
     tol = 2e-3 * (np.abs(h) @ np.abs(W2).T) + tol_h @ np.abs(W2).T
     return out, tol
@@ -409,7 +422,8 @@ def moe(x, logits, k, w13, w2, scoring=SOFTMAX, renorm=True,
     (any indexable, fetched only for experts that receive tokens).
     y[t] = sum_j w_{t,j} * expert_{ids[t,j]}(x[t])  (+ shared(x[t]) * 1).
     Returns (y, tol, ids, weights) with tol the propagated elementwise bound
-    (the per-expert bound above, weighted by the gate weights, + 1e-5).
+    (the per-expert bound above, weighted by the gate weights, + 1e-5),
+    widened by the final bf16 store of y.
     """
     x = np.asarray(x, np.float64)
     M, H = x.shape
@@ -427,4 +441,4 @@ def moe(x, logits, k, w13, w2, scoring=SOFTMAX, renorm=True,
         out, t_out = expert_ffn(x, shared_w13, shared_w2, group)
         y += out
         tol += t_out
-    return y, tol + 1e-5, ids, wts
+    return y, _with_output_rounding(tol + 1e-5, y), ids, wts

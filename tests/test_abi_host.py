@@ -1,0 +1,69 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every
+symbol include/fl_int4g.h declares, and rejects bad arguments before
+launching anything.  No GPU needed (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import int4_group_quantized_int4g_gb300 as fl
+from int4_group_quantized_int4g_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fl_int4g.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return fl.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fl_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(fl.SIGNATURES), set(names) ^ set(fl.SIGNATURES)
+
+
+def test_status_strings_and_version(L):
+    for code in range(8):
+        assert isinstance(fl.fl_strerror(code), str) and fl.fl_strerror(code)
+    assert fl.fl_strerror(0) == "ok"
+    assert fl.fl_int4g_version() >= 100
+
+
+def test_repacked_bytes(L):
+    assert fl.fl_int4g_repacked_bytes(4096, 11008) == 32 * 86 * 8512
+    assert fl.fl_int4g_repacked_bytes(200, 384) == 2 * 3 * 8512     # padded to 2 row tiles
+    out = ctypes.c_size_t(0)
+    assert L.fl_int4g_repacked_bytes(128, 100, 128, ctypes.byref(out)) == 1      # K % 128
+    assert L.fl_int4g_repacked_bytes(128, 256, 64, ctypes.byref(out)) == 3       # group 64
+    assert L.fl_int4g_repacked_bytes(0, 256, 128, ctypes.byref(out)) == 1
+
+
+def test_argument_errors_are_caught_on_the_host(L):
+    size = ctypes.c_size_t(0)
+    assert L.fl_int4g_linear_workspace(1, 4096, 4096, ctypes.byref(size)) == 0 and size.value > 0
+    assert L.fl_int4g_linear_workspace(1, 4096, 4000, ctypes.byref(size)) == 1
+    fake = ctypes.c_void_p(0x10000)      # aligned, never dereferenced on the host
+    odd = ctypes.c_void_p(0x10008)
+    null = None
+    # null and misaligned pointers, bad K
+    assert L.fl_int4g_linear(null, 1, 256, fake, 128, fake, fake, 1 << 20, None) == 1
+    assert L.fl_int4g_linear(odd, 1, 256, fake, 128, fake, fake, 1 << 20, None) == 1
+    assert L.fl_int4g_linear(fake, 1, 200, fake, 128, fake, fake, 1 << 20, None) == 1
+    assert L.fl_int4g_linear(fake, 0, 256, fake, 128, fake, fake, 1 << 20, None) == 1
+    # workspace too small
+    assert L.fl_int4g_linear(fake, 1, 256, fake, 128, fake, fake, 16, None) == 2
+    assert L.fl_int4g_repack(fake, fake, fake, 128, 256, 128, fake, 100, None) == 1
+    assert L.fl_int4g_repack(fake, fake, fake, 128, 256, 64, fake, 1 << 20, None) == 3
+    assert L.fl_int4g_quantize(fake, 128, 256, 128, fake, fake, null, fake, None) == 1
+    assert L.fl_int4g_status(null, None, ctypes.byref(ctypes.c_int())) == 1

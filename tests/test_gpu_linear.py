@@ -1,0 +1,186 @@
+"""GPU parity: quantizer, repack and int4g linear through the C ABI against
+the CPU oracle on the same seeded inputs.
+
+Bar: codes, scales, zeros and the interleaved bytes bit-exact; y within
+|y - y_ref| <= 2e-3 * sum_k |x||w'| + 1e-5 elementwise (fp32 accumulation,
+bf16 output)."""
+import numpy as np
+import pytest
+import torch
+
+import int4_group_quantized_int4g_gb300 as fl
+from int4_group_quantized_int4g_gb300 import inputs
+from oracle import int4g_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from int4_group_quantized_int4g_gb300 import _build
+    _build.build()
+    fl.lib()
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def bf16_dev(bits):
+    return to_dev(bits.view(np.int16)).view(torch.bfloat16)
+
+
+def quantize_dev(W):
+    q, s, z = fl.fl_int4g_quantize(to_dev(W))
+    return q, s, z
+
+
+def canon_host(q, s, z):
+    return q.cpu().numpy(), s.cpu().numpy().view(np.uint16), z.cpu().numpy()
+
+
+# ------------------------------------------------------------ a1 quantizer
+
+def _edge_weights():
+    rng = np.random.default_rng([0, 40])
+    W = (rng.standard_normal((7, 1024)) * 0.02).astype(np.float32)
+    W[0, 0:128] = 0.0                          # zero group
+    W[0, 128:256] = 0.37                       # constant positive
+    W[0, 256:384] = -1.25                      # constant negative
+    W[1, 0:128] = np.float32(1e-9) * rng.standard_normal(128).astype(np.float32)   # s16 -> 0
+    W[1, 128:256] = np.float32(3e-6) * rng.standard_normal(128).astype(np.float32)  # fp16 subnormal scale
+    W[2, 0:128] = np.abs(W[2, 0:128]) + 0.5    # all positive: clamped zero point
+    W[2, 128:256] = -np.abs(W[2, 128:256]) - 0.5
+    # exact rounding ties: on a grid with step 0.25 plus half steps
+    W[3, 0:128] = (np.arange(128) % 16 - 7.5).astype(np.float32) * np.float32(0.25)
+    W[4, :] *= 50                              # large values
+    return W
+
+
+@pytest.mark.parametrize("shape", [(200, 384), (3, 1024), (129, 1152)])
+def test_quantizer_bit_exact(shape):
+    N, K = shape
+    W = inputs.dense_weight(N, K, layer=40 + N)
+    Q, S, Z = O.quantize(W)
+    got = canon_host(*quantize_dev(W))
+    assert np.array_equal(got[0], Q)
+    assert np.array_equal(got[1], S)
+    assert np.array_equal(got[2], Z)
+
+
+def test_quantizer_edge_groups_bit_exact():
+    W = _edge_weights()
+    Q, S, Z = O.quantize(W)
+    got = canon_host(*quantize_dev(W))
+    assert np.array_equal(got[0], Q) and np.array_equal(got[1], S) and np.array_equal(got[2], Z)
+
+
+def test_quantizer_reports_fp16_overflow():
+    W = np.zeros((2, 256), np.float32)
+    W[1, 130] = 4e6
+    W[1, 131] = -4e6
+    with pytest.raises(fl.Int4gError) as e:
+        quantize_dev(W)
+    assert e.value.code == 7
+
+
+# ------------------------------------------------------------ a2 repack
+
+@pytest.mark.parametrize("shape", [(200, 384), (128, 128), (300, 1280)])
+def test_repack_bit_exact_and_invertible(shape):
+    N, K = shape
+    W = inputs.dense_weight(N, K, layer=50 + N)
+    Q, S, Z = O.quantize(W)
+    w = fl.fl_int4g_repack(to_dev(Q), to_dev(S.view(np.int16)), to_dev(Z), N, K)
+    assert np.array_equal(w.cpu().numpy(), O.repack(Q, S, Z, N, K))
+    back = canon_host(*fl.fl_int4g_unrepack(w, N, K))
+    assert np.array_equal(back[0], Q) and np.array_equal(back[1], S) and np.array_equal(back[2], Z)
+
+
+# ------------------------------------------------------------ a3 linear
+
+def _linear_case(M, N, K, layer):
+    W = inputs.dense_weight(N, K, layer=layer)
+    xb = inputs.activations(M, K, stream=layer)
+    Q, S, Z = O.quantize(W)
+    w = fl.fl_int4g_repack(to_dev(Q), to_dev(S.view(np.int16)), to_dev(Z), N, K)
+    return W, xb, Q, S, Z, w
+
+
+def _check(y, xb, Q, S, Z):
+    xf = O.bf16_value(xb)
+    ref, tol = O.linear(xf, Q, S, Z), O.linear_tolerance(xf, Q, S, Z)
+    got = y.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got))
+    bad = err > tol
+    assert not bad.any(), f"{bad.sum()} elements out of bound; worst err/tol {np.max(err / tol):.3f} at {np.unravel_index(np.argmax(err / tol), err.shape)}"
+    return float(np.max(err / tol))
+
+
+@pytest.mark.parametrize("M", [1, 2, 7, 8, 9, 16, 17, 31, 32, 33, 40])
+@pytest.mark.parametrize("NK", [(200, 384), (512, 1280), (136, 128)])
+def test_linear_parity_small(M, NK):
+    N, K = NK
+    _, xb, Q, S, Z, w = _linear_case(M, N, K, layer=60 + K)
+    y = fl.fl_int4g_linear(bf16_dev(xb), w, N)
+    _check(y, xb, Q, S, Z)
+
+
+def test_linear_config1_full():
+    """M=1, K=1024, N=3072 (Qwen3-0.6B up_proj shape), every output checked."""
+    M, N, K = 1, 3072, 1024
+    W = inputs.dense_weight(N, K, layer=0, outliers=False)
+    xb = inputs.activations(M, K, stream=0)
+    Q, S, Z = O.quantize(W)
+    q, s, z = quantize_dev(W)
+    assert np.array_equal(canon_host(q, s, z)[0], Q)
+    w = fl.fl_int4g_repack(q, s, z, N, K)
+    y = fl.fl_int4g_linear(bf16_dev(xb), w, N)
+    _check(y, xb, Q, S, Z)
+
+
+def test_linear_deterministic_and_workspace_reuse():
+    M, N, K = 8, 1024, 4096
+    _, xb, Q, S, Z, w = _linear_case(M, N, K, layer=70)
+    x = bf16_dev(xb)
+    y1 = fl.fl_int4g_linear(x, w, N).clone()
+    y2 = fl.fl_int4g_linear(x, w, N).clone()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    _check(y1, xb, Q, S, Z)
+
+
+def test_linear_workspace_too_small():
+    M, N, K = 1, 256, 256
+    _, xb, Q, S, Z, w = _linear_case(M, N, K, layer=71)
+    ws = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(fl.Int4gError) as e:
+        fl.fl_int4g_linear(bf16_dev(xb), w, N, ws=ws)
+    assert e.value.code == 2
+
+
+LLAMA = [(4096, 12288), (4096, 11008), (11008, 4096)]
+
+
+@pytest.mark.parametrize("KN", LLAMA)
+def test_linear_llama_decode_sampled(KN):
+    """Llama-7B-shaped decode linears at full size, M in {1, 8, 32}, on 96
+    sampled output columns (the oracle dequantizes just those rows)."""
+    K, N = KN
+    W = inputs.dense_weight(N, K, layer=K + N)
+    q, s, z = quantize_dev(W)
+    w = fl.fl_int4g_repack(q, s, z, N, K)
+    cols = np.sort(inputs.rng(6, K, N).choice(N, 96, replace=False))
+    cols = np.unique(np.concatenate([cols, [0, N - 1]]))
+    Qc, Sc, Zc = O.quantize(W[cols])
+    qh, sh, zh = canon_host(q, s, z)
+    assert np.array_equal(qh[cols], Qc) and np.array_equal(sh[cols], Sc) and np.array_equal(zh[cols], Zc)
+    for M in (1, 8, 32):
+        xb = inputs.activations(M, K, stream=M)
+        y = fl.fl_int4g_linear(bf16_dev(xb), w, N)
+        xf = O.bf16_value(xb)
+        ref, tol = O.linear(xf, Qc, Sc, Zc), O.linear_tolerance(xf, Qc, Sc, Zc)
+        got = y.float().cpu().numpy().astype(np.float64)[:, cols]
+        assert np.all(np.abs(got - ref) <= tol), (M, np.max(np.abs(got - ref) / tol))

@@ -73,9 +73,10 @@ def test_linear_hand_case():
     Q, S, Z = O.quantize(np.array(g["W"], np.float32), 8)
     x = np.array(g["x"])
     assert np.array_equal(O.linear(x, Q, S, Z, 8), np.array(g["y"]))
-    # bound closed form: row 0 with x0 = ones -> 2e-3 * sum|w'| + 1e-5 = 2e-3*6 + 1e-5
+    # bound closed form: row 0 with x0 = ones: sum|w'| = 6, y = 3, and the bf16
+    # store adds 2^-8 of (|y| + bound): (2e-3*6 + 1e-5)(1 + 2^-8) + 3 * 2^-8
     tol = O.linear_tolerance(x, Q, S, Z, 8)
-    assert tol[0, 0] == pytest.approx(2e-3 * 6.0 + 1e-5, rel=1e-15)
+    assert tol[0, 0] == pytest.approx((2e-3 * 6.0 + 1e-5) * (1 + 2 ** -8) + 3.0 * 2 ** -8, rel=1e-15)
     assert tol.shape == (2, 4)
 
 
