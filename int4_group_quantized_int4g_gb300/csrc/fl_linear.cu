@@ -28,35 +28,48 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kXRowStride = 320;  // 256 B of x per row + 64 B pad: conflict-free B-fragment loads
 constexpr int kMaxTokens = 32;
+// Ticket counters live at a fixed offset with room for kMaxRowTiles row tiles,
+// so that a workspace reused across shapes never finds another shape's
+// scratch partial sums where its counters are (they must be zero on entry).
+constexpr int kMaxRowTiles = 8192;  // N <= 1,048,576
 
 struct RowsParams {
   const uint8_t* w;
   const __nv_bfloat16* x;
   __nv_bfloat16* y;
-  float* part;       // [P * maxseg][128][Mp] fp32 partial sums
+  float* part;       // [P + T][128][Mp] fp32 partial sums (slot = CTA + tile)
   int32_t* cnt;      // [T][8] tickets (zero between calls)
   int32_t* status;   // 16-byte status block
-  long long U;       // units = T * G
+  int U;             // units = T * G
   int M, K, N, T, G, P;
-  int maxseg;
   int stages;
   uint32_t stage_bytes;
 };
 
-__host__ __device__ __forceinline__ long long unit_begin(long long c, long long U, int P) { return c * U / P; }
-__host__ __device__ __forceinline__ int cta_of_unit(long long u, long long U, int P) {
-  return static_cast<int>(((u + 1) * P - 1) / U);
+// CTA c owns units [unit_begin(c), unit_begin(c+1)); cta_of_unit inverts it.
+__host__ __device__ __forceinline__ int unit_begin(int c, int U, int P) {
+  return static_cast<int>(static_cast<long long>(c) * U / P);
+}
+__host__ __device__ __forceinline__ int cta_of_unit(int u, int U, int P) {
+  return static_cast<int>((static_cast<long long>(u + 1) * P - 1) / U);
 }
 
+// Partial sums of row tile T from CTA c go to slot c + T.  The slots are
+// unique (the CTAs covering tile T precede those covering tile T+1) and those
+// of one tile are contiguous, so its last CTA reads them as one block.
+//
+// store_tile: a row tile computed whole by this CTA is written to y as bf16;
+// otherwise the warp's 16 x Mp partial sums go to the tile's slot and the
+// function returns true (a ticket is owed, taken by ticket_tile after the
+// main loop so that no warp waits on an atomic in the middle of its stream).
 template <int NT>
-__device__ __forceinline__ void flush_tile(const RowsParams& p, long long T, int c, long long u0, long long u1,
-                                           int warp, int lane, float (&tot)[NT][4]) {
+__device__ __forceinline__ bool store_tile(const RowsParams& p, int T, int c, int u0, int u1, int warp, int lane,
+                                           float (&tot)[NT][4]) {
   constexpr int Mp = 8 * NT;
   const int gid = lane >> 2, tig = lane & 3;
-  const long long tu0 = T * p.G, tu1 = (T + 1) * p.G;
-  const int rbase = static_cast<int>(T) * kRowTile + warp * 16;
+  const int tu0 = T * p.G, tu1 = (T + 1) * p.G;
+  const int rbase = T * kRowTile + warp * 16;
   if (tu0 >= u0 && tu1 <= u1) {
-    // this CTA computed the whole row tile: write bf16 directly
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -66,44 +79,149 @@ __device__ __forceinline__ void flush_tile(const RowsParams& p, long long T, int
         if (n < p.N && m < p.M) p.y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(tot[nt][e]);
       }
     }
-    return;
+    return false;
   }
-  const int seg = static_cast<int>(T - u0 / p.G);
-  float* pp = p.part + ((static_cast<size_t>(c) * p.maxseg + seg) * kRowTile + warp * 16) * Mp;
+  constexpr size_t kSlot = static_cast<size_t>(kRowTile) * Mp;   // floats per slot
+  float* pp = p.part + static_cast<size_t>(c + T) * kSlot + warp * 16 * Mp;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    *reinterpret_cast<float2*>(pp + gid * Mp + nt * 8 + 2 * tig) = make_float2(tot[nt][0], tot[nt][1]);
-    *reinterpret_cast<float2*>(pp + (gid + 8) * Mp + nt * 8 + 2 * tig) = make_float2(tot[nt][2], tot[nt][3]);
+    __stcg(reinterpret_cast<float2*>(pp + gid * Mp + nt * 8 + 2 * tig), make_float2(tot[nt][0], tot[nt][1]));
+    __stcg(reinterpret_cast<float2*>(pp + (gid + 8) * Mp + nt * 8 + 2 * tig), make_float2(tot[nt][2], tot[nt][3]));
   }
-  __threadfence();
+  return true;
+}
+
+// Ticket for a row tile whose partials this warp stored; the last of the
+// tile's CTAs to arrive sums all partials in CTA order and writes y.
+template <int NT>
+__device__ __forceinline__ void ticket_tile(const RowsParams& p, int T, int warp, int lane) {
+  constexpr int Mp = 8 * NT;
+  constexpr size_t kSlot = static_cast<size_t>(kRowTile) * Mp;
+  const int tu0 = T * p.G, tu1 = (T + 1) * p.G;
+  // the warp's partial stores are ordered before lane 0's ticket by the warp
+  // barrier and published at GPU scope by lane 0's release fence
   __syncwarp();
   const int cf = cta_of_unit(tu0, p.U, p.P), cl = cta_of_unit(tu1 - 1, p.U, p.P);
   int last = 0;
-  if (lane == 0) last = atomicAdd(&p.cnt[T * kConsumerWarps + warp], 1) == cl - cf;
+  if (lane == 0) {
+    fence_acq_rel_gpu();
+    last = atomicAdd(&p.cnt[T * kConsumerWarps + warp], 1) == cl - cf;
+    if (last) fence_acq_rel_gpu();
+  }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
-  __threadfence();
-  for (int e = lane; e < 16 * Mp; e += 32) {
-    const int row = e / Mp, m = e % Mp;
-    float sum = 0.f;
-    for (int cc = cf; cc <= cl; ++cc) {
-      const int sg = static_cast<int>(T - unit_begin(cc, p.U, p.P) / p.G);
-      sum += __ldcg(p.part + ((static_cast<size_t>(cc) * p.maxseg + sg) * kRowTile + warp * 16 + row) * Mp + m);
+  const int np = cl - cf + 1;
+  const int rbase = T * kRowTile + warp * 16;
+  const float* base = p.part + static_cast<size_t>(cf + T) * kSlot + warp * 16 * Mp;
+#pragma unroll
+  for (int e4 = lane; e4 < 4 * Mp; e4 += 32) {
+    // fixed summation order (CTA order) whatever order the loads complete in
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int j = 0;
+    for (; j + 4 <= np; j += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) v[t] = __ldcg(reinterpret_cast<const float4*>(base + (j + t) * kSlot) + e4);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) acc.x += v[t].x, acc.y += v[t].y, acc.z += v[t].z, acc.w += v[t].w;
     }
+    for (; j < np; ++j) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(base + j * kSlot) + e4);
+      acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+    }
+    const int row = (4 * e4) / Mp, m0 = (4 * e4) % Mp;
     const int n = rbase + row;
-    if (n < p.N && m < p.M) p.y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(sum);
+    if (n < p.N) {
+      const float r[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        if (m0 + t < p.M) p.y[static_cast<size_t>(m0 + t) * p.N + n] = __float2bfloat16_rn(r[t]);
+    }
   }
   if (lane == 0) p.cnt[T * kConsumerWarps + warp] = 0;
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) k_linear_rows(const RowsParams p) {
+// One super-block through the tensor cores, for one consumer warp: acc[nt]
+// (rows r0 and r0+8 of the tile, the lane's two tokens of token tile nt) =
+// sum over the group of x * (q - z)   (FOLD: of x * (128 + q));
+// s0/s1 receive the rows' fp16 scales, z0/z1 their zero points.
+//
+// The 16 bytes a lane reads per row hold logical columns 8*(4j+tig)+0..7
+// (j = word), each word giving 4 bf16 pairs (128+q) by one LOP3.  MMA step
+// (j, h) uses pairs 2h, 2h+1 of word j as A and x[m][8*(4j+tig)+4h .. +3]
+// as B, which is the same permutation of K on both operands.
+//
+// FOLD: the (128+q) codes go to the MMA as they are; the caller removes
+// (128+z) * sum_k x[m,k] per row and token, instead of a bf16 subtract per
+// pair on the ALU.  Two accumulator chains halve the dependent-MMA latency.
+template <int NT, bool FOLD>
+__device__ __forceinline__ void unit_dot(const uint8_t* sb, const uint8_t* sx, int M, int r0, int gid, int tig,
+                                         float (&acc)[NT][4], float& s0, float& s1, uint32_t& z0, uint32_t& z1) {
+  const uint4 wa = *reinterpret_cast<const uint4*>(sb + r0 * 64 + tig * 16);
+  const uint4 wb = *reinterpret_cast<const uint4*>(sb + (r0 + 8) * 64 + tig * 16);
+  const __half* sc = reinterpret_cast<const __half*>(sb + kSbNib);
+  s0 = __half2float(sc[r0]);
+  s1 = __half2float(sc[r0 + 8]);
+  const uint32_t zsh = (r0 & 1) * 4;
+  z0 = (sb[kSbNib + kSbScale + (r0 >> 1)] >> zsh) & 15u;
+  z1 = (sb[kSbNib + kSbScale + (r0 >> 1) + 4] >> zsh) & 15u;
+  const uint32_t zz0 = bf16_bias_pair(z0), zz1 = bf16_bias_pair(z1);
+  float acc2[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f, acc2[nt][e] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t qa = (&wa.x)[j], qb = (&wb.x)[j];
+    uint32_t a[4], b[4];
+#pragma unroll
+    for (int pi = 0; pi < 4; ++pi) {
+      a[pi] = nib_pair_bf16(qa, pi);
+      b[pi] = nib_pair_bf16(qb, pi);
+      if (!FOLD) {
+        a[pi] = bf16x2_sub(a[pi], zz0);
+        b[pi] = bf16x2_sub(b[pi], zz1);
+      }
+    }
+    uint4 xv[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int m = nt * 8 + gid;
+      xv[nt] = m < M ? *reinterpret_cast<const uint4*>(sx + m * kXRowStride + (4 * j + tig) * 16)
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma_bf16_16816(acc[nt], a[0], b[0], a[1], b[1], xv[nt].x, xv[nt].y);
+      mma_bf16_16816(acc2[nt], a[2], b[2], a[3], b[3], xv[nt].z, xv[nt].w);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
+}
+
+// NT token tiles of 8; UPS super-blocks per pipeline stage (2 gives each
+// warp two independent MMA chains and 17 KB bulk copies).  One CTA per SM,
+// sized to leave room for the next kernel's CTA (programmatic launch), which
+// prefetches its weights while this one computes.
+template <int NT, int UPS>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) k_linear_rows(const RowsParams p) {
+  constexpr bool FOLD = NT <= 2;
+  constexpr int Mp = 8 * NT;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
   uint64_t* empty = full + p.stages;
+  float* xsum = reinterpret_cast<float*>(empty + p.stages);   // [group slot][Mp]: sum_k x over each group
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
-  const long long u0 = unit_begin(c, p.U, p.P), u1 = unit_begin(c + 1, p.U, p.P);
+  const int u0 = unit_begin(c, p.U, p.P), u1 = unit_begin(c + 1, p.U, p.P);
+  const int nstage = (u1 - u0 + UPS - 1) / UPS;   // stages this CTA fills, in order
+  const uint32_t xoff = UPS * kSbBytes;           // x slices follow the super-blocks
+  const int g0 = u0 % p.G;
+  const int nslot = (u1 - u0) < p.G ? (u1 - u0) : p.G;   // distinct groups, from g0 on (mod G)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -113,37 +231,87 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear_rows(const RowsParams p)
     fence_mbar_init();
   }
   __syncthreads();
+  // the next kernel in the stream may start prefetching its weights now
+  pdl_launch_dependents();
 
   if (warp == kConsumerWarps) {
     // ---------------- producer warp
     const uint64_t pol = policy_evict_first();
-    const uint32_t tx = kSbBytes + static_cast<uint32_t>(p.M) * 256u;
-    long long i = 0;
-    for (long long u = u0; u < u1; ++u, ++i) {
-      const int s = static_cast<int>(i % p.stages);
-      if (i >= p.stages) {
-        const uint32_t par = static_cast<uint32_t>((i / p.stages) - 1) & 1u;
-        if (!mbar_wait(&empty[s], par)) {
-          if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 1);
-          // let the copies already issued land before the CTA retires
-          for (long long j = (i > p.stages ? i - p.stages : 0); j < i; ++j)
-            mbar_wait(&full[j % p.stages], static_cast<uint32_t>(j / p.stages) & 1u);
-          return;
-        }
+    auto issue_w = [&](int k, int slot) {   // weights of stage k (contiguous super-blocks)
+      const int ua = u0 + k * UPS, n = min(UPS, u1 - ua);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(n) * (kSbBytes + p.M * 256u));
+        bulk_g2s_hint(smem + static_cast<size_t>(slot) * p.stage_bytes, p.w + static_cast<size_t>(ua) * kSbBytes,
+                      static_cast<uint32_t>(n) * kSbBytes, &full[slot], pol);
       }
-      uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-      const int g = static_cast<int>(u % p.G);
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], tx);
+    };
+    auto issue_x = [&](int k, int slot) {   // the M token rows' slices of stage k's groups
+      const int ua = u0 + k * UPS, n = min(UPS, u1 - ua);
+      uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes + xoff;
+      for (int idx = lane; idx < n * p.M; idx += 32) {
+        const int i = idx / p.M, m = idx - i * p.M;
+        const int g = (ua + i) % p.G;
+        bulk_g2s(st + (i * p.M + m) * kXRowStride, p.x + static_cast<size_t>(m) * p.K + g * kGroup, 256u,
+                 &full[slot]);
+      }
+    };
+    // Weights do not depend on the previous kernel: fill the first stages
+    // before waiting for it; x (its output) is copied after.
+    const int pre = nstage < p.stages ? nstage : p.stages;
+    for (int k = 0; k < pre; ++k) issue_w(k, k);
+    __syncwarp();
+    pdl_wait();
+    for (int k = 0; k < pre; ++k) issue_x(k, k);
+    int s = pre % p.stages;
+    uint32_t ph = pre == p.stages ? 1u : 0u;
+    for (int k = pre; k < nstage; ++k) {
+      if (!mbar_wait(&empty[s], ph ^ 1u)) {
+        if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 1);
+        // let the copies already issued land before the CTA retires
+        for (int j = 0; j < p.stages; ++j) {
+          const int nf = k / p.stages + (j < k % p.stages ? 1 : 0);
+          if (nf > 0) mbar_wait(&full[j], static_cast<uint32_t>(nf - 1) & 1u);
+        }
+        return;
+      }
+      issue_w(k, s);
       __syncwarp();
-      if (lane == 0) bulk_g2s_hint(st, p.w + static_cast<size_t>(u) * kSbBytes, kSbBytes, &full[s], pol);
-      for (int m = lane; m < p.M; m += 32)
-        bulk_g2s(st + kSbBytes + m * kXRowStride, p.x + static_cast<size_t>(m) * p.K + g * kGroup, 256u,
-                 &full[s]);
+      issue_x(k, s);
+      if (++s == p.stages) s = 0, ph ^= 1u;
     }
     return;
   }
 
   // ---------------- consumer warps: rows warp*16 .. warp*16+15 of each tile
+  // (they read x and write y and the workspace: only once the previous kernel is done)
+  pdl_wait();
+  if (FOLD) {
+    // per-group token sums of x for this CTA's groups: one thread per
+    // (group slot, token), its 16 loads in flight at once, summed in k order
+    for (int idx = threadIdx.x; idx < nslot * Mp; idx += kConsumerWarps * 32) {
+      const int i = idx / Mp, m = idx - i * Mp;
+      float v = 0.f;
+      if (m < p.M) {
+        int g = g0 + i;
+        if (g >= p.G) g -= p.G;
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K + g * kGroup);
+        uint4 q[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) q[t] = __ldg(src + t);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const uint32_t w4[4] = {q[t].x, q[t].y, q[t].z, q[t].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            v += __uint_as_float(w4[h] << 16);
+            v += __uint_as_float(w4[h] & 0xffff0000u);
+          }
+        }
+      }
+      xsum[idx] = v;
+    }
+    named_bar(1, kConsumerWarps * 32);
+  }
   const int gid = lane >> 2, tig = lane & 3;
   const int r0 = warp * 16 + gid;
   float tot[NT][4];
@@ -151,86 +319,69 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear_rows(const RowsParams p)
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) tot[nt][e] = 0.f;
-  long long curT = -1;
-  long long i = 0;
-  for (long long u = u0; u < u1; ++u, ++i) {
-    const long long T = u / p.G;
-    if (T != curT) {
-      if (curT >= 0) {
-        flush_tile<NT>(p, curT, c, u0, u1, warp, lane, tot);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) tot[nt][e] = 0.f;
-      }
-      curT = T;
-    }
-    const int s = static_cast<int>(i % p.stages);
-    if (!mbar_wait(&full[s], static_cast<uint32_t>(i / p.stages) & 1u)) {
+  int curT = u0 / p.G, g = g0, slot = 0, s = 0, owed0 = -1;
+  uint32_t ph = 0;
+  for (int k = 0; k < nstage; ++k) {
+    const int ua = u0 + k * UPS, n = min(UPS, u1 - ua);
+    if (!mbar_wait(&full[s], ph)) {
       if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 2);
       return;
     }
     const uint8_t* sb = smem + static_cast<size_t>(s) * p.stage_bytes;
-    const uint8_t* sx = sb + kSbBytes;
-
-    const __half* sc = reinterpret_cast<const __half*>(sb + kSbNib);
-    const float s0 = __half2float(sc[r0]);
-    const float s1 = __half2float(sc[r0 + 8]);
-    const uint32_t zb0 = sb[kSbNib + kSbScale + (r0 >> 1)];
-    const uint32_t zb1 = sb[kSbNib + kSbScale + (r0 >> 1) + 4];
-    const uint32_t sh = (r0 & 1) * 4;
-    const uint32_t zz0 = bf16_bias_pair((zb0 >> sh) & 15u);
-    const uint32_t zz1 = bf16_bias_pair((zb1 >> sh) & 15u);
-    const uint4 wa = *reinterpret_cast<const uint4*>(sb + r0 * 64 + tig * 16);
-    const uint4 wb = *reinterpret_cast<const uint4*>(sb + (r0 + 8) * 64 + tig * 16);
-
-    float acc[NT][4];
+    float acc[UPS][NT][4];
+    float sc[UPS][2];
+    uint32_t zr[UPS][2];
+    // Every slot of the stage is computed, in one basic block so that the
+    // compiler interleaves the independent MMA chains; a slot past the end
+    // of the range holds stale shared memory and its result is dropped.
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t qa = (&wa.x)[j], qb = (&wb.x)[j];
-      uint32_t a[4], b[4];
-#pragma unroll
-      for (int pi = 0; pi < 4; ++pi) {
-        a[pi] = bf16x2_sub(nib_pair_bf16(qa, pi), zz0);
-        b[pi] = bf16x2_sub(nib_pair_bf16(qb, pi), zz1);
-      }
-      uint4 xv[NT];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int m = nt * 8 + gid;
-        xv[nt] = m < p.M ? *reinterpret_cast<const uint4*>(sx + m * kXRowStride + (4 * j + tig) * 16)
-                         : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_bf16_16816(acc[nt], a[2 * h], b[2 * h], a[2 * h + 1], b[2 * h + 1], (&xv[nt].x)[2 * h],
-                         (&xv[nt].x)[2 * h + 1]);
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      tot[nt][0] = fmaf(s0, acc[nt][0], tot[nt][0]);
-      tot[nt][1] = fmaf(s0, acc[nt][1], tot[nt][1]);
-      tot[nt][2] = fmaf(s1, acc[nt][2], tot[nt][2]);
-      tot[nt][3] = fmaf(s1, acc[nt][3], tot[nt][3]);
-    }
+    for (int i = 0; i < UPS; ++i)
+      unit_dot<NT, FOLD>(sb + i * kSbBytes, sb + xoff + i * p.M * kXRowStride, p.M, r0, gid, tig, acc[i],
+                         sc[i][0], sc[i][1], zr[i][0], zr[i][1]);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+    for (int i = 0; i < UPS; ++i) {
+      if (i < n) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float2 xs = make_float2(0.f, 0.f);
+          if (FOLD) xs = *reinterpret_cast<const float2*>(xsum + (slot < nslot ? slot : 0) * Mp + nt * 8 + 2 * tig);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float v = acc[i][nt][e];
+            if (FOLD) v = fmaf(-static_cast<float>(128u + zr[i][e >> 1]), (e & 1) ? xs.y : xs.x, v);
+            tot[nt][e] = fmaf(sc[i][e >> 1], v, tot[nt][e]);
+          }
+        }
+        ++slot;
+        if (++g == p.G) {
+          g = 0;
+          if (ua + i + 1 < u1) {
+            // row tile finished inside this CTA's range: store it now,
+            // take its ticket after the stream
+            if (store_tile<NT>(p, curT, c, u0, u1, warp, lane, tot)) owed0 = curT;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) tot[nt][e] = 0.f;
+            ++curT;
+          }
+        }
+        if (slot == nslot) slot = 0;
+      }
+    }
+    if (++s == p.stages) s = 0, ph ^= 1u;
   }
-  if (curT >= 0) flush_tile<NT>(p, curT, c, u0, u1, warp, lane, tot);
+  const bool owed1 = store_tile<NT>(p, curT, c, u0, u1, warp, lane, tot);
+  // only the first and the last row tile of a CTA's range can be partial
+  if (owed0 >= 0) ticket_tile<NT>(p, owed0, warp, lane);
+  if (owed1) ticket_tile<NT>(p, curT, warp, lane);
 }
 
 // ------------------------------------------------------------------ plan
 struct RowsPlan {
-  int T, G, P, NT, maxseg, stages;
-  long long U;
+  int T, G, P, NT, ups, stages, U;
   uint32_t stage_bytes;
   size_t smem, cnt_off, part_off, ws_bytes;
 };
@@ -239,40 +390,54 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl) {
   if (M < 1 || M > kMaxTokens || N < 1 || K < kGroup || K % kGroup || sms < 1) return false;
+  if ((N + kRowTile - 1) / kRowTile > kMaxRowTiles) return false;
   pl->T = (N + kRowTile - 1) / kRowTile;
   pl->G = K / kGroup;
-  pl->U = static_cast<long long>(pl->T) * pl->G;
-  pl->P = static_cast<int>(pl->U < sms ? pl->U : sms);
+  const long long U = static_cast<long long>(pl->T) * pl->G;
+  if (U > (1LL << 30)) return false;
+  pl->U = static_cast<int>(U);
   pl->NT = (M + 7) / 8;
-  int maxseg = 1;
-  for (int c = 0; c < pl->P; ++c) {
-    const long long a = unit_begin(c, pl->U, pl->P), b = unit_begin(c + 1, pl->U, pl->P);
-    const int segs = static_cast<int>((b - 1) / pl->G - a / pl->G + 1);
-    if (segs > maxseg) maxseg = segs;
-  }
-  pl->maxseg = maxseg;
-  pl->stage_bytes = static_cast<uint32_t>(align_up(kSbBytes + static_cast<size_t>(M) * kXRowStride, 128));
-  int stages = static_cast<int>((200u * 1024u) / pl->stage_bytes);
-  pl->stages = stages > 12 ? 12 : stages;
-  pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes + 2 * pl->stages * sizeof(uint64_t);
+  pl->ups = pl->NT <= 2 ? 2 : 1;
+  // M <= 8: two CTAs per SM (four consumer warps per scheduler)
+  const long long slots = static_cast<long long>(sms) * (pl->NT == 1 ? 2 : 1);
+  pl->P = static_cast<int>(U < slots ? U : slots);
+  pl->stage_bytes = static_cast<uint32_t>(
+      align_up(static_cast<size_t>(pl->ups) * (kSbBytes + static_cast<size_t>(M) * kXRowStride), 128));
+  const size_t budget = pl->NT == 1 ? 100u * 1024u : 200u * 1024u;
+  int stages = static_cast<int>(budget / pl->stage_bytes);
+  pl->stages = stages > 12 ? 12 : (stages < 2 ? 2 : stages);
+  const int units_max = (pl->U + pl->P - 1) / pl->P;
+  const int nslot = units_max < pl->G ? units_max : pl->G;
+  pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes + 2 * pl->stages * sizeof(uint64_t) +
+             static_cast<size_t>(nslot) * 8 * pl->NT * sizeof(float);
   pl->cnt_off = kStatusBytes;
-  pl->part_off = align_up(pl->cnt_off + static_cast<size_t>(pl->T) * kConsumerWarps * 4, 256);
-  pl->ws_bytes = pl->part_off + static_cast<size_t>(pl->P) * pl->maxseg * kRowTile * (8 * pl->NT) * 4;
+  pl->part_off = align_up(pl->cnt_off + static_cast<size_t>(kMaxRowTiles) * kConsumerWarps * 4, 256);
+  pl->ws_bytes = pl->part_off + static_cast<size_t>(pl->P + pl->T) * kRowTile * (8 * pl->NT) * 4;
   return true;
 }
 
-template <int NT>
+template <int NT, int UPS>
 int launch_rows(const RowsPlan& pl, const RowsParams& prm, cudaStream_t s) {
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(k_linear_rows<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(k_linear_rows<NT, UPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024) != cudaSuccess)
       return FL_ERR_CUDA;
     attr_done[dev] = true;
   }
-  k_linear_rows<NT><<<pl.P, kThreads, pl.smem, s>>>(prm);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.P);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k_linear_rows<NT, UPS>, prm) != cudaSuccess) return FL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
@@ -305,14 +470,13 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   prm.T = pl.T;
   prm.G = pl.G;
   prm.P = pl.P;
-  prm.maxseg = pl.maxseg;
   prm.stages = pl.stages;
   prm.stage_bytes = pl.stage_bytes;
   switch (pl.NT) {
-    case 1: return launch_rows<1>(pl, prm, stream);
-    case 2: return launch_rows<2>(pl, prm, stream);
-    case 3: return launch_rows<3>(pl, prm, stream);
-    default: return launch_rows<4>(pl, prm, stream);
+    case 1: return launch_rows<1, 2>(pl, prm, stream);
+    case 2: return launch_rows<2, 2>(pl, prm, stream);
+    case 3: return launch_rows<3, 1>(pl, prm, stream);
+    default: return launch_rows<4, 1>(pl, prm, stream);
   }
 }
 

@@ -184,3 +184,16 @@ def test_linear_llama_decode_sampled(KN):
         ref, tol = O.linear(xf, Qc, Sc, Zc), O.linear_tolerance(xf, Qc, Sc, Zc)
         got = y.float().cpu().numpy().astype(np.float64)[:, cols]
         assert np.all(np.abs(got - ref) <= tol), (M, np.max(np.abs(got - ref) / tol))
+
+
+def test_linear_one_workspace_across_shapes():
+    """One workspace serves shapes with different tile counts in turn: a call
+    must not find the previous shape's scratch where its counters are."""
+    shapes = [(32, 512, 1280), (1, 3072, 1024), (8, 200, 384), (32, 1024, 2048), (1, 3072, 1024)]
+    nb = max(fl.fl_int4g_linear_workspace(M, N, K) for (M, N, K) in shapes)
+    ws = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+    for i, (M, N, K) in enumerate(shapes):
+        _, xb, Q, S, Z, w = _linear_case(M, N, K, layer=80 + i)
+        y = fl.fl_int4g_linear(bf16_dev(xb), w, N, ws=ws)
+        _check(y, xb, Q, S, Z)
+    assert fl.fl_int4g_status(ws) == 0
