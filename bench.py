@@ -35,6 +35,13 @@ METRIC = "int4g GEMV weight GB/s (% HBM peak); MoE layer tokens/s; GEMM % bf16 p
 BYTES_PER_WEIGHT = 0.51953125          # 0.5 B code + 2 B scale / 128 + 0.5 B zero / 128
 LLAMA = [("qkv", 4096, 12288), ("gate", 4096, 11008), ("up", 4096, 11008), ("down", 11008, 4096)]
 DECODE_M = [1, 8, 32]
+# DRAM traffic / algorithmic bytes of k_linear_rows, from one ncu capture of
+# the M=1 fused-QKV launch (profiles/k_linear_rows_m1_qkv_full.md):
+# 26.204672 MB read, 0 written, for 26.181632 MB of weights + x + y.
+# Traffic grows in proportion to the super-blocks a launch streams, so the
+# per-launch traffic of the step is scaled from it.  Reset to None whenever the
+# kernel changes after that capture.
+TRAFFIC_RATIO = 26.204672 / 26.181632
 WORKLOAD = "llama7b-decode-linears int4g g128: (K,N) in {(4096,12288),(4096,11008)x2,(11008,4096)} x M in {1,8,32}"
 
 
@@ -276,7 +283,8 @@ def run_gpu(args):
             "peak_source": pk["source"] + " burst copy",
             "unit": "GB/s",
             "frac": round(achieved / pk["hbm_gbs"], 4),
-            "traffic": None,
+            "traffic": (round(algo_bytes / len(calls) * TRAFFIC_RATIO / 1e6, 3) if TRAFFIC_RATIO else None),
+            "traffic_unit": "MB per launch (scaled from the ncu capture of the M=1 fused-QKV launch)",
         },
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": len(calls) * args.steps,
@@ -295,39 +303,44 @@ import numpy as np
 from oracle import int4g_oracle as O
 from int4_group_quantized_int4g_gb300 import inputs
 rows = {rows}
-tot_bytes = 0.0
-t_all = 0.0
+mats = []
 for name, K, N in {mats!r}:
     W = inputs.dense_weight(rows, K, layer=K + N)
-    Q, S, Z = O.quantize(W)
-    x = O.bf16_value(inputs.activations(1, K, stream=1))
-    t = time.perf_counter()
-    y = O.linear(x, Q, S, Z)
-    t_all += time.perf_counter() - t
-    tot_bytes += 0.51953125 * rows * K
+    mats.append((K, O.quantize(W)))
+tot_bytes = 0.0
+t_all = 0.0
+while t_all < {min_seconds}:
+    for M in (1, 8, 32):
+        for K, (Q, S, Z) in mats:
+            x = O.bf16_value(inputs.activations(M, K, stream=M))
+            t = time.perf_counter()
+            y = O.linear(x, Q, S, Z)
+            t_all += time.perf_counter() - t
+            tot_bytes += 0.51953125 * rows * K
 print(json.dumps({{"bytes": tot_bytes, "seconds": t_all}}))
 """
 
 
-def cpu_baseline(rows=2048):
-    """The oracle's dequantized linear (M=1) on a 2048-row slice of each of the
-    4 Llama matrices, one thread, in a child process (BLAS pinned to 1 thread)."""
+def cpu_baseline(rows=2048, min_seconds=10.0):
+    """The oracle's dequantized linear at M = 1, 8, 32 on a 2048-row slice of
+    each of the 4 Llama matrices, repeated until about 10 s of oracle time,
+    one thread, in a child process (BLAS pinned to 1 thread)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = _ORACLE_SAMPLE.format(root=ROOT, rows=rows, mats=LLAMA)
+    code = _ORACLE_SAMPLE.format(root=ROOT, rows=rows, mats=LLAMA, min_seconds=min_seconds)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
         return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": round(d["bytes"] / d["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"M=1 dequantized linear on {rows} output rows of each Llama matrix "
-                      f"({d['bytes'] / 1e6:.1f} MB of int4g weights, {d['seconds']:.2f} s, float64 numpy)"}
+            "sample": f"dequantized linear at M=1,8,32 on {rows} output rows of each Llama matrix, repeated "
+                      f"({d['bytes'] / 1e6:.1f} MB of int4g weights in {d['seconds']:.2f} s of oracle time, float64 numpy)"}
 
 
 def run_reference(args):
     """The CPU oracle as the reference arm: each step is the bounded sample."""
     steps = []
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(rows=256)
+        cb = cpu_baseline(rows=256, min_seconds=1.0)
         if i >= args.warmup:
             steps.append(cb["value"])
     value = statistics.mean(steps)
@@ -337,7 +350,8 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "M=1 dequantized linear on 256 output rows of each Llama matrix per step"},
+                         "sample": "per step: dequantized linear at M=1,8,32 on 256 output rows of each Llama "
+                                   "matrix, repeated to about 1 s of oracle time"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
