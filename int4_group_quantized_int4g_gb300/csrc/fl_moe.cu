@@ -1,10 +1,583 @@
-// a5-a7: routed MoE layer with int4g experts (route, permute, grouped
-// gate/up + SwiGLU, grouped down + weighted combine).
+// a5-a7: routed MoE layer with int4g experts.
+//
+// fastllm README (gittoolsai mirror), "2. 如何设定推理精度" (--moe_dtype int4g)
+// and "5. 其它参数" (--moe_experts = top-k, --cuda_se = shared expert on the
+// GPU): the expert FFNs hold int4g weights; each token runs through its top-k
+// experts and an always-on shared expert.
+//
+// Pipeline, one stream, no host synchronisation:
+//   k_moe_route    one warp per token: top-k of the fp32 logits, gate weights
+//   k_moe_permute  one CTA: stable counting sort of the M*k assignments by
+//                  expert, token segments of <= 32 rows per expert (the shared
+//                  expert is one more expert holding every token with weight
+//                  1), the device-side work plan, zeroed ticket counters
+//   k_moe_rows<0>  grouped gate/up: h = silu(G x) * (U x), bf16 [pos, I]
+//   k_moe_rows<1>  grouped down: out = w_pos * (W2 h), fp32 [pos, H]
+//   k_moe_combine  y[t] = sum_j out[slot (t,j)] + shared out[t], bf16
+// The grouped kernels stream each active expert's super-blocks once per
+// 32-token segment, with the same register-dequant mma.sync consumer as the
+// decode linear, split over K across all SMs with a ticket hand-off.
 #include "fl_common.cuh"
+#include "fl_rows.cuh"
+
+using namespace fl;
+
+namespace {
+
+constexpr int kSegRows = 32;          // tokens per segment (4 token tiles of 8)
+constexpr int kNT = 4;
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxE = 1024;
+constexpr int kMaxAssign = 16384;     // M * k handled by the one-CTA permute
+
+struct MoePlan {
+  int nseg;   // segments (routed + shared)
+  int U;      // units of each grouped kernel: nseg * tiles * groups
+  int pad[14];
+};
+
+// ------------------------------------------------------------------ route
+// Order used by the selection: larger logit first, equal logits -> lower index.
+__device__ __forceinline__ bool better(float v, int e, float bv, int be) { return v > bv || (v == bv && e < be); }
+
+__global__ void k_moe_route(const float* __restrict__ logits, int M, int E, int k, int scoring, int renorm,
+                            int32_t* __restrict__ ids, float* __restrict__ wts, int32_t* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= M) return;
+  constexpr int kPer = kMaxE / 32;
+  float v[kPer];
+  uint32_t taken = 0;
+  const float* l = logits + static_cast<size_t>(t) * E;
+  int bad = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    float x = -INFINITY;
+    if (e < E) {
+      x = l[e];
+      if (isnan(x)) bad = 1, x = -INFINITY;
+    }
+    v[i] = x;
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, FL_ERR_DEVICE_CHECK, t);
+  float selv[32];   // k <= 32 handled per token (checked on the host)
+  int sele[32];
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, be)) bv = v[i], be = e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (better(ov, oe, bv, be)) bv = ov, be = oe;
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    selv[j] = bv;
+    sele[j] = be;
+  }
+  // gate weights in fp32
+  float den = 0.f;
+  if (scoring == FL_SOFTMAX) {
+    const float lmax = selv[0];
+    if (renorm) {
+      for (int j = 0; j < k; ++j) den += expf(selv[j] - lmax);
+    } else {
+      float part = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if (lane + 32 * i < E) part += expf(v[i] - lmax);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      den = part;
+    }
+  } else {
+    if (renorm)
+      for (int j = 0; j < k; ++j) den += 1.f / (1.f + expf(-selv[j]));
+    else
+      den = 1.f;
+  }
+  if (lane == 0) {
+    for (int j = 0; j < k; ++j) {
+      const float num = scoring == FL_SOFTMAX ? expf(selv[j] - selv[0]) : 1.f / (1.f + expf(-selv[j]));
+      ids[static_cast<size_t>(t) * k + j] = sele[j];
+      wts[static_cast<size_t>(t) * k + j] = num / den;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ permute
+struct PermuteArgs {
+  const int32_t* ids;
+  const float* wts;
+  int M, E, k, TT13, TT2;       // TT: row tiles of the grouped kernels' outputs
+  int G13, G2;                  // groups along K of the two grouped kernels
+  int has_shared;
+  int32_t* offsets;             // [E+1]
+  int32_t* perm;                // [M*k]
+  int32_t* inv;                 // [M*k]
+  int32_t* tok_of_pos;          // [M*k + M]
+  float* wpos;                  // [M*k + M]
+  int32_t* seg_e;               // [nseg_max]
+  int32_t* seg_pos;
+  int32_t* seg_n;
+  MoePlan* plan;
+  int32_t* cnt13;               // counters to zero: [nseg_max * TT13 * 8]
+  int32_t* cnt2;                // [nseg_max * TT2 * 8]
+  int32_t* user_offsets;        // optional copies
+  int32_t* user_perm;
+};
+
+__global__ void __launch_bounds__(1024, 1) k_moe_permute(const PermuteArgs a) {
+  extern __shared__ int32_t psm[];
+  pdl_wait();   // ids / weights come from k_moe_route
+  const int E = a.E, n = a.M * a.k;
+  int32_t* counts = psm;                       // [32][E]
+  int32_t* local = counts + 32 * E;            // [n]
+  int32_t* tot = local + n;                    // [E + 1]
+  int32_t* nch = tot + (E + 1);                // [E + 1] segment starts
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < 32 * E; i += blockDim.x) counts[i] = 0;
+  __syncthreads();
+  // per-warp stable ranks: warp w owns assignments [w*C, (w+1)*C)
+  const int C = (n + 31) / 32;
+  const int i0 = warp * C, i1 = min(n, i0 + C);
+  for (int base = i0; base < i1; base += 32) {
+    const int i = base + lane;
+    const bool act = i < i1;
+    const unsigned am = __ballot_sync(0xffffffffu, act);
+    if (act) {
+      const int e = a.ids[i];
+      const unsigned mask = __match_any_sync(am, e);
+      const int rank = __popc(mask & ((1u << lane) - 1u));
+      const int before = counts[warp * E + e];
+      local[i] = before + rank;
+      __syncwarp(am);
+      if (lane == __ffs(mask) - 1) counts[warp * E + e] = before + __popc(mask);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  // totals, then per-expert base offsets for every warp
+  for (int e = tid; e < E; e += blockDim.x) {
+    int s = 0;
+    for (int w = 0; w < 32; ++w) s += counts[w * E + e];
+    tot[e] = s;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0, seg = 0;
+    for (int e = 0; e < E; ++e) {
+      const int c = tot[e];
+      tot[e] = run;                              // exclusive scan -> offsets
+      nch[e] = seg;                              // first segment of expert e
+      run += c;
+      seg += (c + kSegRows - 1) / kSegRows;
+    }
+    tot[E] = run;
+    nch[E] = seg;
+    const int nshared = a.has_shared ? (a.M + kSegRows - 1) / kSegRows : 0;
+    a.plan->nseg = seg + nshared;
+    a.plan->U = (seg + nshared) * a.TT13 * a.G13;   // == (seg + nshared) * TT2 * G2
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = tot[e];
+    for (int w = 0; w < 32; ++w) {
+      const int c = counts[w * E + e];
+      counts[w * E + e] = run;
+      run += c;
+    }
+  }
+  for (int e = tid; e <= E; e += blockDim.x) {
+    a.offsets[e] = tot[e];
+    if (a.user_offsets) a.user_offsets[e] = tot[e];
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int w = i / C;
+    const int e = a.ids[i];
+    const int pos = counts[w * E + e] + local[i];
+    a.perm[pos] = i;
+    a.inv[i] = pos;
+    a.tok_of_pos[pos] = i / a.k;
+    a.wpos[pos] = a.wts[i];
+    if (a.user_perm) a.user_perm[pos] = i;
+  }
+  // shared expert: positions n + t hold token t with weight 1
+  for (int t = tid; t < (a.has_shared ? a.M : 0); t += blockDim.x) {
+    a.tok_of_pos[n + t] = t;
+    a.wpos[n + t] = 1.f;
+  }
+  // segments
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int c = tot[e + 1] - tot[e];
+    for (int s = 0; s * kSegRows < c; ++s) {
+      const int si = nch[e] + s;
+      a.seg_e[si] = e;
+      a.seg_pos[si] = tot[e] + s * kSegRows;
+      a.seg_n[si] = min(kSegRows, c - s * kSegRows);
+    }
+  }
+  if (a.has_shared) {
+    const int ns = (a.M + kSegRows - 1) / kSegRows;
+    for (int s = tid; s < ns; s += blockDim.x) {
+      const int si = nch[E] + s;
+      a.seg_e[si] = E;   // E denotes the shared expert
+      a.seg_pos[si] = n + s * kSegRows;
+      a.seg_n[si] = min(kSegRows, a.M - s * kSegRows);
+    }
+  }
+  // zero the ticket counters the grouped kernels will use
+  const int nseg = nch[E] + (a.has_shared ? (a.M + kSegRows - 1) / kSegRows : 0);
+  for (int i = tid; i < nseg * a.TT13 * kConsumerWarps; i += blockDim.x) a.cnt13[i] = 0;
+  for (int i = tid; i < nseg * a.TT2 * kConsumerWarps; i += blockDim.x) a.cnt2[i] = 0;
+}
+
+// ------------------------------------------------------------------ grouped rows
+// MODE 0: gate/up.  A unit is (segment, tile pair a, group g): super-blocks of
+//         gate tile a and up tile a + I/128 of the segment's expert; the
+//         segment's token rows of x.  Output h = silu(gate) * up, bf16.
+// MODE 1: down.  A unit is (segment, tile, group) of W2; x rows = h rows of
+//         the segment's positions.  Output out = w_pos * sum, fp32.
+struct MoeRowsParams {
+  const uint8_t* w;            // routed experts back to back
+  const uint8_t* w_shared;     // shared expert (or null)
+  size_t wbytes;               // bytes of one expert's matrix
+  const __nv_bfloat16* x;      // MODE 0: x [M, K]; MODE 1: h [pos, K]
+  int K, G, TT;                // K = reduction length, G = K/128, TT = output tiles
+  int up_off;                  // MODE 0: I/128
+  int E, Nout;                 // Nout = output row length (I or H)
+  const int32_t* seg_e;
+  const int32_t* seg_pos;
+  const int32_t* seg_n;
+  const int32_t* tok_of_pos;
+  const float* wpos;
+  const MoePlan* plan;
+  __nv_bfloat16* h;            // MODE 0 output [pos, I]
+  float* out;                  // MODE 1 output [pos, H]
+  float* part;                 // [2P][128][32][VALS] partial sums
+  int32_t* cnt;                // [nseg * TT][8] tickets
+  int32_t* status;
+  int P, stages;
+  uint32_t stage_bytes;
+};
+
+template <int MODE>
+struct MoeIO {
+  static constexpr int kSB = MODE == 0 ? 2 : 1;     // super-blocks per unit
+  static constexpr int kVals = MODE == 0 ? 2 : 1;   // partial values per element
+};
+
+__device__ __forceinline__ int unit_begin_d(int c, int U, int P) {
+  return static_cast<int>(static_cast<long long>(c) * U / P);
+}
+__device__ __forceinline__ int cta_of_unit_d(int u, int U, int P) {
+  return static_cast<int>((static_cast<long long>(u + 1) * P - 1) / U);
+}
+
+// Output of one finished (segment, tile) for the warp's 16 rows.
+template <int MODE>
+__device__ __forceinline__ void emit(const MoeRowsParams& p, int seg, int tile, int warp, int lane,
+                                     const float (&tg)[kNT][4], const float (&tu)[kNT][4]) {
+  const int gid = lane >> 2, tig = lane & 3;
+  const int pos0 = p.seg_pos[seg], nt_ok = p.seg_n[seg];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int m = nt * 8 + 2 * tig + (e & 1);
+      const int row = tile * kRowTile + warp * 16 + gid + (e >> 1) * 8;
+      if (m >= nt_ok) continue;
+      const size_t o = static_cast<size_t>(pos0 + m) * p.Nout + row;
+      if (MODE == 0) {
+        const float g = tg[nt][e];
+        p.h[o] = __float2bfloat16_rn(g / (1.f + expf(-g)) * tu[nt][e]);
+      } else {
+        p.out[o] = p.wpos[pos0 + m] * tg[nt][e];
+      }
+    }
+}
+
+template <int MODE>
+__device__ __forceinline__ float* slot_ptr(const MoeRowsParams& p, int c, bool second, int warp) {
+  constexpr size_t kSlot = static_cast<size_t>(kRowTile) * (8 * kNT) * MoeIO<MODE>::kVals;
+  return p.part + (static_cast<size_t>(2 * c + (second ? 1 : 0))) * kSlot +
+         static_cast<size_t>(warp) * 16 * (8 * kNT) * MoeIO<MODE>::kVals;
+}
+
+template <int MODE>
+__device__ __forceinline__ void ticket(const MoeRowsParams& p, int U, int Pe, int gt, int warp, int lane) {
+  constexpr int Mp = 8 * kNT;
+  constexpr int V = MoeIO<MODE>::kVals;
+  const int tu0 = gt * p.G, tu1 = (gt + 1) * p.G;
+  __syncwarp();
+  const int cf = cta_of_unit_d(tu0, U, Pe), cl = cta_of_unit_d(tu1 - 1, U, Pe);
+  int last = 0;
+  if (lane == 0) {
+    fence_acq_rel_gpu();
+    last = atomicAdd(&p.cnt[gt * kConsumerWarps + warp], 1) == cl - cf;
+    if (last) fence_acq_rel_gpu();
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  const int seg = gt / p.TT, tile = gt - seg * p.TT;
+  const int gid = lane >> 2, tig = lane & 3;
+  float tg[kNT][4], tu[kNT][4];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) tg[nt][e] = 0.f, tu[nt][e] = 0.f;
+  for (int cc = cf; cc <= cl; ++cc) {   // CTA order: deterministic
+    const bool second = gt != unit_begin_d(cc, U, Pe) / p.G;
+    const float* sp = slot_ptr<MODE>(p, cc, second, warp);
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float* q = sp + ((gid + 8 * hh) * Mp + nt * 8 + 2 * tig) * V;
+        if (V == 2) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(q));
+          tg[nt][2 * hh] += v.x, tu[nt][2 * hh] += v.y, tg[nt][2 * hh + 1] += v.z, tu[nt][2 * hh + 1] += v.w;
+        } else {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(q));
+          tg[nt][2 * hh] += v.x, tg[nt][2 * hh + 1] += v.y;
+        }
+      }
+    }
+  }
+  emit<MODE>(p, seg, tile, warp, lane, tg, tu);
+  if (lane == 0) p.cnt[gt * kConsumerWarps + warp] = 0;
+}
+
+template <int MODE>
+__device__ __forceinline__ bool store(const MoeRowsParams& p, int gt, int c, int u0, int u1, int warp,
+                                      int lane, const float (&tg)[kNT][4], const float (&tu)[kNT][4]) {
+  constexpr int Mp = 8 * kNT;
+  constexpr int V = MoeIO<MODE>::kVals;
+  const int tu0 = gt * p.G, tu1 = (gt + 1) * p.G;
+  if (tu0 >= u0 && tu1 <= u1) {
+    const int seg = gt / p.TT;
+    emit<MODE>(p, seg, gt - seg * p.TT, warp, lane, tg, tu);
+    return false;
+  }
+  const int gid = lane >> 2, tig = lane & 3;
+  float* sp = slot_ptr<MODE>(p, c, gt != u0 / p.G, warp);
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float* q = sp + ((gid + 8 * hh) * Mp + nt * 8 + 2 * tig) * V;
+      if (V == 2)
+        __stcg(reinterpret_cast<float4*>(q),
+               make_float4(tg[nt][2 * hh], tu[nt][2 * hh], tg[nt][2 * hh + 1], tu[nt][2 * hh + 1]));
+      else
+        __stcg(reinterpret_cast<float2*>(q), make_float2(tg[nt][2 * hh], tg[nt][2 * hh + 1]));
+    }
+  return true;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p) {
+  constexpr int SB = MoeIO<MODE>::kSB;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
+  uint64_t* empty = full + p.stages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();   // the plan, segments and x/h come from the previous kernels
+  const int U = p.plan->U;
+  // the work is split over min(P, U) CTAs, so that every working CTA owns at
+  // least one unit (the ticket hand-off counts on it); the rest retire
+  const int Pe = U < p.P ? U : p.P;
+  if (c >= Pe) return;
+  const int u0 = unit_begin_d(c, U, Pe), u1 = unit_begin_d(c + 1, U, Pe);
+  const int TG = p.TT * p.G;
+  const uint32_t xoff = SB * kSbBytes;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer: super-block(s) + the segment's x rows
+    const uint64_t pol = policy_evict_first();
+    int s = 0, fills = 0;
+    uint32_t ph = 0;
+    for (int u = u0; u < u1; ++u) {
+      if (fills >= p.stages && !mbar_wait(&empty[s], ph ^ 1u)) {
+        if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 11);
+        for (int j = 0; j < p.stages; ++j) {
+          const int nf = fills / p.stages + (j < fills % p.stages ? 1 : 0);
+          if (nf > 0) mbar_wait(&full[j], static_cast<uint32_t>(nf - 1) & 1u);
+        }
+        return;
+      }
+      const int seg = u / TG, rem = u - seg * TG, tile = rem / p.G, g = rem - tile * p.G;
+      const int e = p.seg_e[seg], pos0 = p.seg_pos[seg], nt_ok = p.seg_n[seg];
+      const uint8_t* base = e == p.E ? p.w_shared : p.w + static_cast<size_t>(e) * p.wbytes;
+      uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(SB * kSbBytes + nt_ok * 256));
+        bulk_g2s_hint(st, base + (static_cast<size_t>(tile) * p.G + g) * kSbBytes, kSbBytes, &full[s], pol);
+        if (SB == 2)
+          bulk_g2s_hint(st + kSbBytes, base + (static_cast<size_t>(tile + p.up_off) * p.G + g) * kSbBytes, kSbBytes,
+                        &full[s], pol);
+      }
+      __syncwarp();
+      if (lane < nt_ok) {
+        const int row = MODE == 0 ? p.tok_of_pos[pos0 + lane] : pos0 + lane;
+        bulk_g2s(st + xoff + lane * kXRowStride, p.x + static_cast<size_t>(row) * p.K + g * kGroup, 256u, &full[s]);
+      }
+      ++fills;
+      if (++s == p.stages) s = 0, ph ^= 1u;
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int gid = lane >> 2, tig = lane & 3;
+  const int r0 = warp * 16 + gid;
+  float tg[kNT][4], tu[kNT][4];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) tg[nt][e] = 0.f, tu[nt][e] = 0.f;
+  int s = 0, owed0 = -1;
+  uint32_t ph = 0;
+  int gt = u0 / p.G;
+  for (int u = u0; u < u1; ++u) {
+    const int seg = u / TG;
+    const int nt_ok = p.seg_n[seg];
+    if (!mbar_wait(&full[s], ph)) {
+      if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 12);
+      return;
+    }
+    const uint8_t* sb = smem + static_cast<size_t>(s) * p.stage_bytes;
+    float ag[kNT][4], au[kNT][4];
+    float s0g, s1g, s0u = 0.f, s1u = 0.f;
+    uint32_t z0, z1;
+    const int ntiles = (nt_ok + 7) / 8;
+    unit_dot<kNT, false>(sb, sb + xoff, nt_ok, r0, gid, tig, ag, s0g, s1g, z0, z1, ntiles);
+    if (SB == 2) unit_dot<kNT, false>(sb + kSbBytes, sb + xoff, nt_ok, r0, gid, tig, au, s0u, s1u, z0, z1, ntiles);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        tg[nt][e] = fmaf(e < 2 ? s0g : s1g, ag[nt][e], tg[nt][e]);
+        if (SB == 2) tu[nt][e] = fmaf(e < 2 ? s0u : s1u, au[nt][e], tu[nt][e]);
+      }
+    if (++s == p.stages) s = 0, ph ^= 1u;
+    if ((u + 1) % p.G == 0 && u + 1 < u1) {
+      if (store<MODE>(p, gt, c, u0, u1, warp, lane, tg, tu)) owed0 = gt;
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tg[nt][e] = 0.f, tu[nt][e] = 0.f;
+      ++gt;
+    }
+  }
+  const bool owed1 = store<MODE>(p, gt, c, u0, u1, warp, lane, tg, tu);
+  if (owed0 >= 0) ticket<MODE>(p, U, Pe, owed0, warp, lane);
+  if (owed1) ticket<MODE>(p, U, Pe, gt, warp, lane);
+}
+
+// ------------------------------------------------------------------ combine
+__global__ void k_moe_combine(const float* __restrict__ out, const int32_t* __restrict__ inv, int M, int k, int H,
+                              int has_shared, __nv_bfloat16* __restrict__ y) {
+  const int t = blockIdx.y;
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= M || n >= H) return;
+  pdl_wait();
+  float acc = 0.f;
+  for (int j = 0; j < k; ++j) acc += out[static_cast<size_t>(inv[t * k + j]) * H + n];
+  if (has_shared) acc += out[static_cast<size_t>(M * k + t) * H + n];
+  y[static_cast<size_t>(t) * H + n] = __float2bfloat16_rn(acc);
+}
+
+// ------------------------------------------------------------------ host plan
+size_t al(size_t v) { return (v + 255) / 256 * 256; }
+
+struct MoeLayout {
+  size_t plan, ids, wts, offsets, perm, inv, tok, wpos, sege, segp, segn, h, out, cnt13, cnt2, part13, part2, total;
+  int nseg_max, P, stages13, stages2;
+  uint32_t stage13, stage2;
+};
+
+bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeLayout* L) {
+  if (M < 1 || E < 1 || E > kMaxE || k < 1 || k > E || k > 32 || H < kGroup || I < kGroup || H % kGroup ||
+      I % kGroup || sms < 1)
+    return false;
+  if (static_cast<long long>(M) * k > kMaxAssign) return false;
+  const int n = M * k, npos = n + (has_shared ? M : 0);
+  L->nseg_max = std::min(E, n) + (n + kSegRows - 1) / kSegRows + (has_shared ? (M + kSegRows - 1) / kSegRows : 0);
+  L->P = sms;
+  const int TT13 = I / kRowTile, TT2 = H / kRowTile;
+  size_t o = kStatusBytes;
+  L->plan = o; o = al(o + sizeof(MoePlan));
+  L->ids = o; o = al(o + 4ull * n);
+  L->wts = o; o = al(o + 4ull * n);
+  L->offsets = o; o = al(o + 4ull * (E + 1));
+  L->perm = o; o = al(o + 4ull * n);
+  L->inv = o; o = al(o + 4ull * n);
+  L->tok = o; o = al(o + 4ull * npos);
+  L->wpos = o; o = al(o + 4ull * npos);
+  L->sege = o; o = al(o + 4ull * L->nseg_max);
+  L->segp = o; o = al(o + 4ull * L->nseg_max);
+  L->segn = o; o = al(o + 4ull * L->nseg_max);
+  L->h = o; o = al(o + 2ull * npos * I);
+  L->out = o; o = al(o + 4ull * npos * H);
+  L->cnt13 = o; o = al(o + 4ull * L->nseg_max * TT13 * kConsumerWarps);
+  L->cnt2 = o; o = al(o + 4ull * L->nseg_max * TT2 * kConsumerWarps);
+  L->part13 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * kNT * 2);
+  L->part2 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * kNT);
+  L->total = o;
+  L->stage13 = static_cast<uint32_t>((2 * kSbBytes + kSegRows * kXRowStride + 127) / 128 * 128);
+  L->stage2 = static_cast<uint32_t>((kSbBytes + kSegRows * kXRowStride + 127) / 128 * 128);
+  L->stages13 = std::min(8, static_cast<int>((200u * 1024u) / L->stage13));
+  L->stages2 = std::min(12, static_cast<int>((200u * 1024u) / L->stage2));
+  return true;
+}
+
+// Launch with programmatic dependent launch: the kernel may start while the
+// previous one in the stream finishes and must griddepcontrol.wait before
+// touching what that kernel writes or reads.
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace
 
 extern "C" int fl_moe_int4g_workspace(int M, int E, int k, int H, int I, int has_shared, size_t* out) {
-  (void)M; (void)E; (void)k; (void)H; (void)I; (void)has_shared; (void)out;
-  return FL_ERR_UNSUPPORTED;
+  if (!out) return FL_ERR_ARG;
+  MoeLayout L;
+  if (!moe_layout(M, E, k, H, I, has_shared, flh::sm_count(), &L)) return FL_ERR_ARG;
+  *out = L.total;
+  return FL_OK;
 }
 
 extern "C" int fl_moe_int4g(const void* x, const float* logits, int M, int H, int E, int k, int I, int scoring,
@@ -12,5 +585,115 @@ extern "C" int fl_moe_int4g(const void* x, const float* logits, int M, int H, in
                             const void* shared_w2, void* y, int32_t* topk_ids, float* topk_w,
                             int32_t* expert_offsets, int32_t* perm, void* ws, size_t ws_bytes,
                             fl_stream_t stream) {
-  return FL_ERR_UNSUPPORTED;
+  if (!x || !logits || !w13 || !w2 || !y || !ws) return FL_ERR_ARG;
+  if ((shared_w13 == nullptr) != (shared_w2 == nullptr)) return FL_ERR_ARG;
+  if (scoring != FL_SOFTMAX && scoring != FL_SIGMOID) return FL_ERR_ARG;
+  if (!flh::aligned16(x) || !flh::aligned16(w13) || !flh::aligned16(w2) || !flh::aligned16(y) ||
+      !flh::aligned16(ws) || (shared_w13 && (!flh::aligned16(shared_w13) || !flh::aligned16(shared_w2))))
+    return FL_ERR_ARG;
+  const int has_shared = shared_w13 != nullptr;
+  MoeLayout L;
+  if (!moe_layout(M, E, k, H, I, has_shared, flh::sm_count(), &L)) return FL_ERR_ARG;
+  if (ws_bytes < L.total) return FL_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* W = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(W);
+  int32_t* ids = topk_ids ? topk_ids : reinterpret_cast<int32_t*>(W + L.ids);
+  float* wts = topk_w ? topk_w : reinterpret_cast<float*>(W + L.wts);
+  MoePlan* plan = reinterpret_cast<MoePlan*>(W + L.plan);
+  const size_t b13 = static_cast<size_t>(2 * I / kRowTile) * (H / kGroup) * kSbBytes;
+  const size_t b2 = static_cast<size_t>(H / kRowTile) * (I / kGroup) * kSbBytes;
+
+  // route
+  {
+    const int warps = 8;
+    // plain launch: the logits come from whatever ran before this call
+    k_moe_route<<<dim3((M + warps - 1) / warps), dim3(32 * warps), 0, s>>>(logits, M, E, k, scoring, renorm, ids,
+                                                                            wts, status);
+    if (cudaGetLastError() != cudaSuccess) return FL_ERR_CUDA;
+  }
+  // permute
+  {
+    PermuteArgs a;
+    a.ids = ids;
+    a.wts = wts;
+    a.M = M;
+    a.E = E;
+    a.k = k;
+    a.TT13 = I / kRowTile;
+    a.TT2 = H / kRowTile;
+    a.G13 = H / kGroup;
+    a.G2 = I / kGroup;
+    a.has_shared = has_shared;
+    a.offsets = reinterpret_cast<int32_t*>(W + L.offsets);
+    a.perm = reinterpret_cast<int32_t*>(W + L.perm);
+    a.inv = reinterpret_cast<int32_t*>(W + L.inv);
+    a.tok_of_pos = reinterpret_cast<int32_t*>(W + L.tok);
+    a.wpos = reinterpret_cast<float*>(W + L.wpos);
+    a.seg_e = reinterpret_cast<int32_t*>(W + L.sege);
+    a.seg_pos = reinterpret_cast<int32_t*>(W + L.segp);
+    a.seg_n = reinterpret_cast<int32_t*>(W + L.segn);
+    a.plan = plan;
+    a.cnt13 = reinterpret_cast<int32_t*>(W + L.cnt13);
+    a.cnt2 = reinterpret_cast<int32_t*>(W + L.cnt2);
+    a.user_offsets = expert_offsets;
+    a.user_perm = perm;
+    const size_t smem = 4ull * (32 * E + M * k + 2 * (E + 1));
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+      if (cudaFuncSetAttribute(k_moe_permute, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+          cudaSuccess)
+        return FL_ERR_CUDA;
+      attr_done[dev] = true;
+    }
+    if (smem > 227 * 1024) return FL_ERR_UNSUPPORTED;
+    if (launch_pdl(k_moe_permute, dim3(1), dim3(1024), smem, s, a) != cudaSuccess) return FL_ERR_CUDA;
+  }
+  // grouped gate/up + SwiGLU, then grouped down
+  for (int mode = 0; mode < 2; ++mode) {
+    MoeRowsParams p;
+    p.w = static_cast<const uint8_t*>(mode == 0 ? w13 : w2);
+    p.w_shared = static_cast<const uint8_t*>(mode == 0 ? shared_w13 : shared_w2);
+    p.wbytes = mode == 0 ? b13 : b2;
+    p.x = mode == 0 ? static_cast<const __nv_bfloat16*>(x) : reinterpret_cast<const __nv_bfloat16*>(W + L.h);
+    p.K = mode == 0 ? H : I;
+    p.G = p.K / kGroup;
+    p.TT = mode == 0 ? I / kRowTile : H / kRowTile;
+    p.up_off = I / kRowTile;
+    p.E = E;
+    p.Nout = mode == 0 ? I : H;
+    p.seg_e = reinterpret_cast<const int32_t*>(W + L.sege);
+    p.seg_pos = reinterpret_cast<const int32_t*>(W + L.segp);
+    p.seg_n = reinterpret_cast<const int32_t*>(W + L.segn);
+    p.tok_of_pos = reinterpret_cast<const int32_t*>(W + L.tok);
+    p.wpos = reinterpret_cast<const float*>(W + L.wpos);
+    p.plan = plan;
+    p.h = reinterpret_cast<__nv_bfloat16*>(W + L.h);
+    p.out = reinterpret_cast<float*>(W + L.out);
+    p.part = reinterpret_cast<float*>(W + (mode == 0 ? L.part13 : L.part2));
+    p.cnt = reinterpret_cast<int32_t*>(W + (mode == 0 ? L.cnt13 : L.cnt2));
+    p.status = status;
+    p.P = L.P;
+    p.stages = mode == 0 ? L.stages13 : L.stages2;
+    p.stage_bytes = mode == 0 ? L.stage13 : L.stage2;
+    const size_t smem = static_cast<size_t>(p.stages) * p.stage_bytes + 2 * p.stages * sizeof(uint64_t);
+    static bool attr_done[2][64] = {{false}};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    auto kern = mode == 0 ? k_moe_rows<0> : k_moe_rows<1>;
+    if (dev >= 0 && dev < 64 && !attr_done[mode][dev]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+        return FL_ERR_CUDA;
+      attr_done[mode][dev] = true;
+    }
+    if (launch_pdl(kern, dim3(L.P), dim3(kThreads), smem, s, p) != cudaSuccess) return FL_ERR_CUDA;
+  }
+  // combine
+  if (launch_pdl(k_moe_combine, dim3((H + 255) / 256, M), dim3(256), 0, s,
+                 reinterpret_cast<const float*>(W + L.out), reinterpret_cast<const int32_t*>(W + L.inv), M, k, H,
+                 has_shared, static_cast<__nv_bfloat16*>(y)) != cudaSuccess)
+    return FL_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }

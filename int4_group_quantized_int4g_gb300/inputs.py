@@ -70,7 +70,8 @@ def hot_experts(E, hot, seed=SEED):
 
 
 def _seed64(*stream, seed=SEED):
-    h = hashlib.sha256(repr((seed,) + tuple(stream)).encode()).digest()
+    # integers only: numpy and Python integers of the same value give one seed
+    h = hashlib.sha256(repr((int(seed),) + tuple(int(v) for v in stream)).encode()).digest()
     return int.from_bytes(h[:8], "little") & ((1 << 63) - 1)
 
 

@@ -120,12 +120,45 @@ def quantize_group(w):
 
 
 def quantize(W, group=GROUP):
-    """W fp32 [N, K] -> canonical triple (Q, S, Z).
+    """W fp32 [N, K] -> canonical triple (Q, S, Z), by quantize_group applied
+    to every group (written with array operations over all groups at once;
+    quantize_loops() is the same rule one group at a time, and the pins check
+    that the two agree bit for bit).
 
     Q uint8 [N, K/2]       two codes per byte, low nibble = even k
     S uint16 [N, G]        fp16 scale bits, G = K / group
     Z uint8 [N, ceil(G/2)] two zero points per byte, low nibble = even g
     """
+    W = np.asarray(W, dtype=np.float32)
+    N, K = W.shape
+    if K % group != 0 or K % 2 != 0:
+        raise ValueError("K must be a multiple of the group size")
+    G = K // group
+    w = W.reshape(N, G, group).astype(np.float64)
+    mn = w.min(axis=2)
+    mx = w.max(axis=2)
+    const = mn == mx
+    zero = const & (mn == 0.0)
+    mn = np.where(const, np.minimum(mn, 0.0), mn)
+    mx = np.where(const, np.maximum(mx, 0.0), mx)
+    with np.errstate(invalid='ignore', over='ignore', divide='ignore'):
+        s = (mx - mn) / QMAX
+        sbits = fp16_bits(s)
+        s16 = fp16_value(sbits)
+        if (~zero & ~np.isfinite(s16)).any():
+            raise ValueError("group scale overflows fp16")
+        zero = zero | (s16 == 0.0)
+        safe = np.where(zero, 1.0, s16)
+        z = np.clip(round_half_away(-mn / safe), 0, QMAX)
+        q = np.clip(round_half_away(w / safe[:, :, None]) + z[:, :, None], 0, QMAX)
+    z = np.where(zero, 0, z).astype(np.uint8)
+    q = np.where(zero[:, :, None], 0, q).astype(np.uint8).reshape(N, K)
+    S = np.where(zero, 0, sbits).astype(np.uint16)
+    return pack_codes(q), S, pack_zeros(z)
+
+
+def quantize_loops(W, group=GROUP):
+    """quantize(), one group at a time through quantize_group."""
     W = np.asarray(W, dtype=np.float32)
     N, K = W.shape
     if K % group != 0 or K % 2 != 0:

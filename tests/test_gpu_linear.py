@@ -117,6 +117,10 @@ def _check(y, xb, Q, S, Z):
     assert np.all(np.isfinite(got))
     bad = err > tol
     assert not bad.any(), f"{bad.sum()} elements out of bound; worst err/tol {np.max(err / tol):.3f} at {np.unravel_index(np.argmax(err / tol), err.shape)}"
+    # aggregate sanity check beside the elementwise bound: relative RMS error
+    # near the bf16 rounding floor of the output
+    rel = np.sqrt(np.mean(err ** 2) / np.mean(ref ** 2))
+    assert rel <= 1e-2, f"relative RMS error {rel:.3e}"
     return float(np.max(err / tol))
 
 
@@ -184,6 +188,7 @@ def test_linear_llama_decode_sampled(KN):
         ref, tol = O.linear(xf, Qc, Sc, Zc), O.linear_tolerance(xf, Qc, Sc, Zc)
         got = y.float().cpu().numpy().astype(np.float64)[:, cols]
         assert np.all(np.abs(got - ref) <= tol), (M, np.max(np.abs(got - ref) / tol))
+        assert np.sqrt(np.mean((got - ref) ** 2) / np.mean(ref ** 2)) <= 1e-2
 
 
 def test_linear_one_workspace_across_shapes():

@@ -1,0 +1,213 @@
+"""GPU parity of the routed MoE layer (route, permute, grouped gate/up +
+SwiGLU, grouped down, weighted combine, shared expert) through the C ABI
+against the CPU oracle on the same seeded inputs.
+
+Bar: top-k ids, expert offsets and the permutation bit-exact; gate weights
+within 1e-5 relative; y within the oracle's propagated elementwise bound."""
+import numpy as np
+import pytest
+import torch
+
+import int4_group_quantized_int4g_gb300 as fl
+from int4_group_quantized_int4g_gb300 import inputs
+from oracle import int4g_oracle as O
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from int4_group_quantized_int4g_gb300 import _build
+    _build.build()
+    fl.lib()
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def bf16_dev(bits):
+    return to_dev(bits.view(np.int16)).view(torch.bfloat16)
+
+
+def repack_dev(Q, S, Z, N, K):
+    return fl.fl_int4g_repack(to_dev(Q), to_dev(S.view(np.int16)), to_dev(Z), N, K)
+
+
+def host_experts(E, H, I, layer):
+    """Canonical triples (oracle quantizer) of E experts; numpy weights."""
+    w13, w2 = [], []
+    for e in range(E):
+        w13.append(O.quantize(inputs.expert_weight(2 * I, H, layer, e, 0)))
+        w2.append(O.quantize(inputs.expert_weight(H, I, layer, e, 1)))
+    return w13, w2
+
+
+def stack_dev(trips, N, K):
+    return torch.cat([repack_dev(*t, N, K) for t in trips])
+
+
+def run_moe(xb, logits, k, I, w13_d, w2_d, scoring, renorm, sw13=None, sw2=None):
+    M, H = xb.shape
+    E = logits.shape[1]
+    ids = torch.empty((M, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((M, k), dtype=torch.float32, device=DEV)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(M * k, dtype=torch.int32, device=DEV)
+    ws = torch.zeros(fl.fl_moe_int4g_workspace(M, E, k, H, I, sw13 is not None), dtype=torch.uint8, device=DEV)
+    y = fl.fl_moe_int4g(bf16_dev(xb), to_dev(logits), k, I, w13_d, w2_d, scoring=scoring, renorm=renorm,
+                        shared_w13=sw13, shared_w2=sw2, topk_ids=ids, topk_w=wts, expert_offsets=offs, perm=perm,
+                        ws=ws)
+    torch.cuda.synchronize()
+    assert fl.fl_int4g_status(ws) == 0
+    return y, ids, wts, offs, perm
+
+
+def check_y(y, ref, tol, rows=None):
+    """The elementwise bound, plus an aggregate check: the propagated MoE bound
+    is loose (first-order worst case), so the relative RMS error must also stay
+    near the bf16 rounding floor of the output (~2.4e-3 observed)."""
+    got = y.float().cpu().numpy().astype(np.float64)
+    if rows is not None:
+        got = got[rows]
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got))
+    assert np.all(err <= tol), f"worst err/tol {np.max(err / tol):.3f} at {np.unravel_index(np.argmax(err / tol), err.shape)}"
+    rel = np.sqrt(np.mean(err ** 2) / np.mean(ref ** 2))
+    assert rel <= 1e-2, f"relative RMS error {rel:.3e}"
+
+
+def check_routing(logits, k, scoring, renorm, ids, wts, offs, perm):
+    E = logits.shape[1]
+    rid, rw = O.route(logits, k, scoring, renorm)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.allclose(wts.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+    roff, rperm = O.permute(rid, E)
+    assert np.array_equal(offs.cpu().numpy(), roff)
+    assert np.array_equal(perm.cpu().numpy(), rperm)
+
+
+@pytest.fixture(scope="module")
+def small():
+    E, H, I = 8, 256, 256
+    w13, w2 = host_experts(E, H, I, layer=500)
+    sw13, sw2 = host_experts(1, H, I, layer=501)
+    return dict(E=E, H=H, I=I, w13=w13, w2=w2, sw13=sw13[0], sw2=sw2[0],
+                w13_d=stack_dev(w13, 2 * I, H), w2_d=stack_dev(w2, H, I),
+                sw13_d=repack_dev(*sw13[0], 2 * I, H), sw2_d=repack_dev(*sw2[0], H, I))
+
+
+@pytest.mark.parametrize("M", [1, 5, 37, 70])
+@pytest.mark.parametrize("mode", ["softmax", "sigmoid_shared", "softmax_norenorm"])
+def test_moe_small_parity(small, M, mode):
+    E, H, I = small["E"], small["H"], small["I"]
+    k = 3
+    xb = inputs.activations(M, H, stream=600 + M)
+    logits = inputs.router_logits(M, E, stream=600 + M)
+    scoring = fl.FL_SIGMOID if mode.startswith("sigmoid") else fl.FL_SOFTMAX
+    renorm = mode != "softmax_norenorm"
+    shared = mode.endswith("shared")
+    y, ids, wts, offs, perm = run_moe(xb, logits, k, I, small["w13_d"], small["w2_d"], scoring, renorm,
+                                      small["sw13_d"] if shared else None, small["sw2_d"] if shared else None)
+    check_routing(logits, k, scoring, renorm, ids, wts, offs, perm)
+    ref, tol, _, _ = O.moe(O.bf16_value(xb), logits, k, small["w13"], small["w2"], scoring, renorm,
+                           small["sw13"] if shared else None, small["sw2"] if shared else None)
+    check_y(y, ref, tol)
+
+
+def test_moe_routing_ties_and_all_experts(small):
+    """Tied logits (quarter steps) and k = E: ids and permutation bit-exact."""
+    E, H, I = small["E"], small["H"], small["I"]
+    M = 33
+    rng = np.random.default_rng([0, 610])
+    logits = (np.round(rng.standard_normal((M, E)) * 2) / 4).astype(np.float32)
+    xb = inputs.activations(M, H, stream=610)
+    for k in (2, E):
+        y, ids, wts, offs, perm = run_moe(xb, logits, k, I, small["w13_d"], small["w2_d"], fl.FL_SOFTMAX, True)
+        check_routing(logits, k, fl.FL_SOFTMAX, True, ids, wts, offs, perm)
+        ref, tol, _, _ = O.moe(O.bf16_value(xb), logits, k, small["w13"], small["w2"], O.SOFTMAX, True)
+        check_y(y, ref, tol)
+
+
+def test_moe_deterministic(small):
+    M = 37
+    xb = inputs.activations(M, small["H"], stream=620)
+    logits = inputs.router_logits(M, small["E"], stream=620)
+    a = run_moe(xb, logits, 3, small["I"], small["w13_d"], small["w2_d"], fl.FL_SIGMOID, True,
+                small["sw13_d"], small["sw2_d"])[0].clone()
+    b = run_moe(xb, logits, 3, small["I"], small["w13_d"], small["w2_d"], fl.FL_SIGMOID, True,
+                small["sw13_d"], small["sw2_d"])[0].clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ------------------------------------------------------------------ full sizes
+
+class DeviceExperts:
+    """Expert weights drawn on the device (seeded), quantized and repacked on
+    the device; fp32 weights of any expert can be redrawn for the oracle."""
+
+    def __init__(self, E, H, I, layer, shared):
+        self.E, self.H, self.I, self.layer = E, H, I, layer
+        self.w13 = torch.cat([self._packed(e, 0) for e in range(E)])
+        self.w2 = torch.cat([self._packed(e, 1) for e in range(E)])
+        self.sw13 = self._packed(E, 0) if shared else None
+        self.sw2 = self._packed(E, 1) if shared else None
+
+    def fp32(self, e, which):
+        N, K = (2 * self.I, self.H) if which == 0 else (self.H, self.I)
+        return inputs.device_normal((N, K), 1, self.layer, e, which, device=DEV)
+
+    def _packed(self, e, which):
+        W = self.fp32(e, which)
+        N, K = W.shape
+        q, s, z = fl.fl_int4g_quantize(W)
+        return fl.fl_int4g_repack(q, s, z, N, K)
+
+    def oracle_triples(self, e, which):
+        return O.quantize(self.fp32(e, which).cpu().numpy())
+
+
+class LazyTriples:
+    def __init__(self, ex, which):
+        self.ex, self.which, self.cache = ex, which, {}
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = self.ex.oracle_triples(e, self.which)
+        return self.cache[e]
+
+
+def sampled_check(ex, xb, logits, k, scoring, y, ids, sample):
+    w13 = LazyTriples(ex, 0)
+    w2 = LazyTriples(ex, 1)
+    sw13 = ex.oracle_triples(ex.E, 0) if ex.sw13 is not None else None
+    sw2 = ex.oracle_triples(ex.E, 1) if ex.sw2 is not None else None
+    ref, tol, rid, _ = O.moe(O.bf16_value(xb[sample]), logits[sample], k, w13, w2, scoring, True, sw13, sw2)
+    assert np.array_equal(ids.cpu().numpy()[sample], rid)
+    check_y(y, ref, tol, rows=sample)
+
+
+def test_moe_qwen3_shaped():
+    """128 experts, hidden 2048, intermediate 768, top-8 softmax; M in {1, 64, 256}."""
+    ex = DeviceExperts(128, 2048, 768, layer=700, shared=False)
+    for M in (1, 64, 256):
+        xb = inputs.activations(M, 2048, stream=700 + M)
+        logits = inputs.router_logits(M, 128, stream=700 + M)
+        y, ids, wts, offs, perm = run_moe(xb, logits, 8, 768, ex.w13, ex.w2, fl.FL_SOFTMAX, True)
+        check_routing(logits, 8, fl.FL_SOFTMAX, True, ids, wts, offs, perm)
+        sample = np.unique([0, M - 1])
+        sampled_check(ex, xb, logits, 8, O.SOFTMAX, y, ids, sample)
+
+
+def test_moe_deepseek_shaped():
+    """256 routed experts + 1 shared, hidden 7168, intermediate 2048, top-8
+    sigmoid renormalised, skewed logits; M in {1, 16} (sampled tokens)."""
+    ex = DeviceExperts(256, 7168, 2048, layer=800, shared=True)
+    for M in (1, 16):
+        xb = inputs.activations(M, 7168, stream=800 + M)
+        logits = inputs.router_logits(M, 256, stream=800 + M, hot=51)
+        y, ids, wts, offs, perm = run_moe(xb, logits, 8, 2048, ex.w13, ex.w2, fl.FL_SIGMOID, True, ex.sw13, ex.sw2)
+        check_routing(logits, 8, fl.FL_SIGMOID, True, ids, wts, offs, perm)
+        sampled_check(ex, xb, logits, 8, O.SIGMOID, y, ids, np.array([M - 1]))

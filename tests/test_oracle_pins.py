@@ -80,12 +80,38 @@ def test_linear_hand_case():
     assert tol.shape == (2, 4)
 
 
+def _edge_matrix():
+    rng = np.random.default_rng([0, 41])
+    W = (rng.standard_normal((9, 1024)) * 0.02).astype(np.float32)
+    W[0, 0:128] = 0.0
+    W[0, 128:256] = 0.37
+    W[0, 256:384] = -1.25
+    W[1, 0:128] = np.float32(1e-9) * rng.standard_normal(128).astype(np.float32)
+    W[1, 128:256] = np.float32(3e-6) * rng.standard_normal(128).astype(np.float32)
+    W[2, 0:128] = np.abs(W[2, 0:128]) + 0.5
+    W[2, 128:256] = -np.abs(W[2, 128:256]) - 0.5
+    W[3, 0:128] = (np.arange(128) % 16 - 7.5).astype(np.float32) * np.float32(0.25)
+    W[4, :] *= 50
+    W[5, ::7] *= 20
+    return W
+
+
+@pytest.mark.parametrize("group", [128, 8, 4])
+def test_vectorised_quantizer_equals_group_loop(group):
+    for W in (_edge_matrix(), (np.random.default_rng([0, 42]).standard_normal((17, 256)) * 0.02).astype(np.float32)):
+        a = O.quantize(W, group)
+        b = O.quantize_loops(W, group)
+        assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
 def test_quantize_rejects_fp16_overflow():
     W = np.zeros((1, 128), np.float32)
     W[0, 0] = 3e6
     W[0, 1] = -3e6
     with pytest.raises(ValueError):
         O.quantize(W)
+    with pytest.raises(ValueError):
+        O.quantize_loops(W)
 
 
 # ------------------------------------------------------ invariants
