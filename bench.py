@@ -133,6 +133,101 @@ def build_weights(torch, fl, inputs, n_layers, dev):
     return mats
 
 
+QWEN = dict(name="qwen3-moe", E=128, H=2048, I=768, k=8, scoring=0, shared=False, hot=0, Ms=(1, 64, 256))
+DSV3 = dict(name="deepseek-v3-moe", E=256, H=7168, I=2048, k=8, scoring=1, shared=True, hot=51, Ms=(1, 16, 128, 1024))
+PREFILL = [(512, 4096, 11008), (512, 11008, 4096), (2048, 4096, 11008), (2048, 11008, 4096)]
+
+
+def _flush_l2(torch, buf):
+    buf.add_(1)          # 256 MB read+write: evicts the 129 MB L2
+
+
+def _median_time(torch, fn, flush, reps, stream):
+    """Median CUDA-event time of fn() over reps calls, L2 flushed before each."""
+    ts = []
+    for _ in range(reps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def run_moe_section(torch, np, fl, inputs, dev, pk, reps):
+    """MoE layer tokens/s for the Qwen3- and DeepSeek-V3-shaped configs."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    flushbuf = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    for cfg in (QWEN, DSV3):
+        E, H, I, k = cfg["E"], cfg["H"], cfg["I"], cfg["k"]
+
+        def packed(e, which, layer=1000):
+            N, K = (2 * I, H) if which == 0 else (H, I)
+            W = inputs.device_normal((N, K), 1, layer, e, which, device=dev)
+            q, s, z = fl.fl_int4g_quantize(W)
+            del W
+            return fl.fl_int4g_repack(q, s, z, N, K)
+
+        w13 = torch.cat([packed(e, 0) for e in range(E)])
+        w2 = torch.cat([packed(e, 1) for e in range(E)])
+        sw13 = packed(E, 0) if cfg["shared"] else None
+        sw2 = packed(E, 1) if cfg["shared"] else None
+        eb = (w13.numel() + w2.numel()) / E
+        sb = (sw13.numel() + sw2.numel()) if cfg["shared"] else 0
+        res = {}
+        for M in cfg["Ms"]:
+            x = torch.from_numpy(inputs.activations(M, H, stream=M).view(np.int16)).to(dev).view(torch.bfloat16)
+            lg = torch.from_numpy(inputs.router_logits(M, E, stream=M, hot=cfg["hot"])).to(dev)
+            y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+            ids = torch.empty((M, k), dtype=torch.int32, device=dev)
+            ws = torch.zeros(fl.fl_moe_int4g_workspace(M, E, k, H, I, cfg["shared"]), dtype=torch.uint8, device=dev)
+
+            def call():
+                fl.fl_moe_int4g(x, lg, k, I, w13, w2, scoring=cfg["scoring"], renorm=True, shared_w13=sw13,
+                                shared_w2=sw2, y=y, topk_ids=ids, ws=ws)
+            call()
+            torch.cuda.synchronize()
+            assert fl.fl_int4g_status(ws) == 0
+            ms = _median_time(torch, call, lambda: _flush_l2(torch, flushbuf), reps, stream)
+            touched = int(torch.unique(ids).numel())
+            nbytes = touched * eb + sb + 2 * M * H * 2
+            flops = 2.0 * (M * k + (M if cfg["shared"] else 0)) * 3 * H * I
+            t_roof = max(nbytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+            res[str(M)] = {"ms": round(ms, 4), "tokens_per_s": round(M / (ms * 1e-3), 1),
+                           "experts_touched": touched, "weight_GB": round(nbytes / 1e9, 4),
+                           "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                           "roofline_frac_of_measured": round(t_roof / (ms * 1e-3), 4)}
+        out[cfg["name"]] = res
+        del w13, w2, sw13, sw2
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_gemm_section(torch, np, fl, inputs, dev, pk, reps):
+    """Prefill int4g GEMM TFLOP/s (M in {512, 2048})."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    flushbuf = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    for M, K, N in PREFILL:
+        W = inputs.device_normal((N, K), 1, 77, K, N, device=dev)
+        q, s, z = fl.fl_int4g_quantize(W)
+        del W
+        w = fl.fl_int4g_repack(q, s, z, N, K)
+        x = torch.from_numpy(inputs.activations(M, K, stream=M).view(np.int16)).to(dev).view(torch.bfloat16)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(fl.fl_int4g_linear_workspace(M, N, K), dtype=torch.uint8, device=dev)
+        call = lambda: fl.fl_int4g_linear(x, w, N, y=y, ws=ws)
+        call()
+        ms = _median_time(torch, call, lambda: _flush_l2(torch, flushbuf), reps, stream)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        out[f"M{M}_K{K}_N{N}"] = {"ms": round(ms, 4), "TFLOPs": round(tf, 2),
+                                 "frac_of_measured_bf16": round(tf / pk["bf16_tflops"], 4)}
+    return out
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -252,6 +347,11 @@ def run_gpu(args):
     e2e_ms = a0.elapsed_time(a1) / args.steps
     e2e_value = wbytes / (e2e_ms * 1e-3) / 1e9
 
+    sections = {}
+    if not args.no_sections:
+        sections["moe"] = run_moe_section(torch, np, fl, inputs, dev, pk, reps=5)
+        sections["gemm"] = run_gemm_section(torch, np, fl, inputs, dev, pk, reps=3)
+
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -289,6 +389,7 @@ def run_gpu(args):
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": len(calls) * args.steps,
         "clocks": clocks,
+        "sections": sections,
     }
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline()
@@ -411,6 +512,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sections", action="store_true", help="skip the MoE and prefill GEMM sections")
     ap.add_argument("--case", choices=["linear"], help="time one shape on its own (profiling)")
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--K", type=int, default=4096)
