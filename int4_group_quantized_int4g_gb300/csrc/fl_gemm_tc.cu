@@ -1,0 +1,367 @@
+// a4: int4g prefill GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// y[m, n] = sum_k x[m, k] * w'[n, k] for M tokens, the dense contraction of the
+// int4g linear (FastLLM page, section 3.1: 4-bit codes dequantized inside the
+// matmul; fastllm README section 2: --dtype int4g applies to every linear).
+//
+// One CTA computes a 128 (weight rows n) x BN (tokens m) tile of y^T with
+// tcgen05.mma kind::f16 (bf16 in, fp32 accumulate in tensor memory):
+//   warp 0        producer: per group of 128 along K, the tile's token block
+//                 of x by TMA (two 64-column boxes, 128-byte swizzle) and the
+//                 weight super-block (8512 B) by a 1-D bulk copy;
+//   warp 1        allocates tensor memory; lane 0 issues the 8 MMAs of a group
+//                 (K = 16 each) and commits them to mbarriers;
+//   warps 4..11   dequantize the super-block into the A operand in shared
+//                 memory (K-major, 128-byte swizzle): each weight becomes the
+//                 correctly rounded bf16 of s16 * (q - z);
+//   warps 4..7    epilogue: tcgen05.ld of the accumulator, bf16 store of y.
+// The dequantized value bf16(s16*(q-z)) is computed exactly: s16 = s_hi +
+// s_lo with s_hi = bf16(s16) and s_lo exact in bf16 (<= 3 bits), t =
+// s_lo*(q-z) is exact, and fma(s_hi, q-z, t) rounds once.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "fl_common.cuh"
+
+using namespace fl;
+
+namespace {
+
+constexpr int kTcThreads = 12 * 32;
+constexpr int kDeqWarp0 = 4;            // warps 4..11 dequantize; 4..7 also run the epilogue
+constexpr int kABytes = 128 * 128 * 2;  // A tile of one group: 128 rows x 128 k bf16 (two 16 KB halves)
+
+template <int BN>
+struct TcCfg {
+  static constexpr int kBBytes = BN * 128 * 2;          // B tile of one group: BN rows x 128 k bf16
+  static constexpr int kStages = BN == 256 ? 2 : 3;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSbBytes + 64;   // + padding to keep 1 KB alignment
+  static constexpr int kStageStride = (kStageBytes + 1023) / 1024 * 1024;
+  static constexpr int kSmem = kStages * kStageStride + 1024 /*align slack*/ + 256 /*barriers*/;
+  static constexpr uint32_t kTmemCols = BN;             // fp32 accumulator columns (power of 2)
+};
+
+struct TcParams {
+  const uint8_t* w;
+  __nv_bfloat16* y;
+  int32_t* status;
+  int M, N, K, G, mtiles;
+};
+
+// ------------------------------------------------------------ tcgen05 helpers
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of the calling warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// TMA 2-D tile load global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 B apart (SBO), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;                  // LBO (unused for swizzled K-major)
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;          // SBO
+  d |= static_cast<uint64_t>(1u) << 46;                  // version
+  d |= static_cast<uint64_t>(2u) << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+template <int BN>
+__device__ __forceinline__ uint32_t idesc_bf16() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+// bf16x2 helpers with a single rounding
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t bfma2(uint32_t a, uint32_t b, uint32_t c) {
+  __nv_bfloat162 r = __hfma2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b),
+                             *reinterpret_cast<__nv_bfloat162*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
+  using C = TcCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* bars = smem + C::kStages * C::kStageStride;
+  uint64_t* full = reinterpret_cast<uint64_t*>(bars);          // B + super-block landed
+  uint64_t* afull = full + C::kStages;                         // A dequantized
+  uint64_t* empty = afull + C::kStages;                        // MMAs of the stage done
+  uint64_t* dfull = empty + C::kStages;                        // accumulator final
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfull + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = blockIdx.x / p.mtiles, mt = blockIdx.x % p.mtiles;
+  auto stage_a = [&](int s) { return smem + s * C::kStageStride; };
+  auto stage_b = [&](int s) { return smem + s * C::kStageStride + kABytes; };
+  auto stage_sb = [&](int s) { return smem + s * C::kStageStride + kABytes + C::kBBytes; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&afull[s], 8);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(dfull, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_d = *tmem_slot;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- producer
+    if (lane == 0) {
+      pdl_wait();
+      const uint64_t pol = policy_evict_first();
+      int s = 0;
+      uint32_t ph = 0;
+      for (int g = 0; g < p.G; ++g) {
+        if (g >= C::kStages && !mbar_wait(&empty[s], ph ^ 1u)) {
+          set_status(p.status, FL_ERR_TIMEOUT, 21);
+          atomicExch(abort_flag, 1);
+          // let the copies already issued land before the CTA retires
+          for (int j = 0; j < C::kStages; ++j) {
+            const int nf = g / C::kStages + (j < g % C::kStages ? 1 : 0);
+            if (nf > 0) mbar_wait(&full[j], static_cast<uint32_t>(nf - 1) & 1u);
+          }
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], C::kBBytes + kSbBytes);
+        tma_load_2d(stage_b(s), &xmap, g * kGroup, mt * BN, &full[s]);
+        tma_load_2d(stage_b(s) + BN * 128, &xmap, g * kGroup + 64, mt * BN, &full[s]);
+        bulk_g2s_hint(stage_sb(s), p.w + (static_cast<size_t>(nt) * p.G + g) * kSbBytes, kSbBytes, &full[s], pol);
+        if (++s == C::kStages) s = 0, ph ^= 1u;
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16<BN>();
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int g = 0; g < p.G; ++g) {
+        if (!mbar_wait(&afull[s], ph)) {
+          set_status(p.status, FL_ERR_TIMEOUT, 22);
+          atomicExch(abort_flag, 1);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(stage_a(s)), b0 = smem_u32(stage_b(s));
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem_d, sw128_desc(a0 + h * 16384 + kk * 32), sw128_desc(b0 + h * BN * 128 + kk * 32), idesc,
+                      (g | h | kk) != 0);
+        umma_commit(&empty[s]);
+        if (++s == C::kStages) s = 0, ph ^= 1u;
+      }
+      if (ok) umma_commit(dfull);
+    }
+  } else if (warp >= kDeqWarp0) {
+    // ---------------- dequant: thread = weight row r, chunk pair kh of the row's codes
+    const int q = warp & 3, kh = (warp - kDeqWarp0) >> 2;
+    const int r = q * 32 + lane;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int g = 0; g < p.G; ++g) {
+      if (!mbar_wait(&full[s], ph)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 23);
+        ok = false;
+        break;
+      }
+      const uint8_t* sb = stage_sb(s);
+      const float sf = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
+      const __nv_bfloat16 shi = __float2bfloat16_rn(sf);
+      const __nv_bfloat16 slo = __float2bfloat16_rn(sf - __bfloat162float(shi));   // exact remainder
+      const uint32_t hi2 = static_cast<uint32_t>(__bfloat16_as_ushort(shi)) * 0x00010001u;
+      const uint32_t lo2 = static_cast<uint32_t>(__bfloat16_as_ushort(slo)) * 0x00010001u;
+      const uint32_t z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
+      const uint32_t zz = bf16_bias_pair(z);
+      uint8_t* a = stage_a(s);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int cidx = 2 * kh + ((cc + (r >> 1)) & 1);   // alternate the chunk order: fewer bank conflicts
+        const uint4 wv = *reinterpret_cast<const uint4*>(sb + r * 64 + cidx * 16);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t word = (&wv.x)[j];
+          uint32_t o[4];
+#pragma unroll
+          for (int pi = 0; pi < 4; ++pi) {
+            const uint32_t qz = bf16x2_sub(nib_pair_bf16(word, pi), zz);
+            o[pi] = bfma2(hi2, qz, bmul2(lo2, qz));
+          }
+          const int wl = cidx + 4 * j;                      // logical 8-column chunk 0..15
+          const int half = wl >> 3, c = wl & 7;
+          *reinterpret_cast<uint4*>(a + half * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[s]);
+      if (++s == C::kStages) s = 0, ph ^= 1u;
+    }
+    if (warp < kDeqWarp0 + 4) {
+      // ---------------- epilogue: rows q*32+lane, tokens of the tile
+      if (ok && mbar_wait(dfull, 0)) {
+        tc_fence_after();
+        const int n = nt * kRowTile + r;
+#pragma unroll 1
+        for (int j = 0; j < BN; j += 32) {
+          float v[32];
+          tmem_ld32(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + j, v);
+          if (n < p.N) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int m = mt * BN + j + i;
+              if (m < p.M) p.y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(v[i]);
+            }
+          }
+        }
+      } else if (ok) {
+        set_status(p.status, FL_ERR_TIMEOUT, 24);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_d, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+template <int BN>
+int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_t* status, cudaStream_t s) {
+  using C = TcCfg<BN>;
+  auto enc = encode_fn();
+  if (!enc) return FL_ERR_CUDA;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BN)};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return FL_ERR_CUDA;
+  TcParams p;
+  p.w = static_cast<const uint8_t*>(w);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.status = status;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.G = K / kGroup;
+  p.mtiles = (M + BN - 1) / BN;
+  const int ntiles = (N + kRowTile - 1) / kRowTile;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+      return FL_ERR_CUDA;
+    attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ntiles * p.mtiles));
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k_gemm_tc<BN>, map, p) != cudaSuccess) return FL_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+}
+
+}  // namespace
+
+// Prefill path of fl_int4g_linear (M >= 64): one tcgen05 kernel launch.
+int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_t* status, cudaStream_t s) {
+  if (M >= 1024) return launch_tc<256>(x, M, K, w, N, y, status, s);
+  return launch_tc<128>(x, M, K, w, N, y, status, s);
+}

@@ -424,21 +424,24 @@ static bool linear_args_ok(const void* x, int M, int K, const void* w, int N, co
   return flh::aligned16(x) && flh::aligned16(w) && flh::aligned16(y) && flh::aligned16(ws);
 }
 
+int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_t* status, cudaStream_t s);
+
 extern "C" int fl_int4g_linear_workspace(int M, int N, int K, size_t* out) {
   if (!out || M < 1 || N < 1 || K < kGroup || K % kGroup) return FL_ERR_ARG;
-  // M > 32 runs 32-token chunks of the decode kernel on one workspace
-  return fl_linear_rows_workspace(M < kMaxTokens ? M : kMaxTokens, N, K, out);
+  if (M > kMaxTokens) {
+    *out = kStatusBytes;   // the prefill kernel needs only the status block
+    return FL_OK;
+  }
+  return fl_linear_rows_workspace(M, N, K, out);
 }
 
 extern "C" int fl_int4g_linear(const void* x, int M, int K, const void* w, int N, void* y, void* ws,
                                size_t ws_bytes, fl_stream_t stream) {
   if (!linear_args_ok(x, M, K, w, N, y, ws)) return FL_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  for (int m0 = 0; m0 < M; m0 += kMaxTokens) {
-    const int mm = M - m0 < kMaxTokens ? M - m0 : kMaxTokens;
-    const int rc = fl_linear_rows(static_cast<const __nv_bfloat16*>(x) + static_cast<size_t>(m0) * K, mm, K, w, N,
-                                  static_cast<__nv_bfloat16*>(y) + static_cast<size_t>(m0) * N, ws, ws_bytes, s);
-    if (rc != FL_OK) return rc;
+  if (M > kMaxTokens) {
+    if (ws_bytes < kStatusBytes) return FL_ERR_WORKSPACE;
+    return fl_linear_tc(x, M, K, w, N, y, static_cast<int32_t*>(ws), s);
   }
-  return FL_OK;
+  return fl_linear_rows(x, M, K, w, N, y, ws, ws_bytes, s);
 }

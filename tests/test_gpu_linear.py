@@ -202,3 +202,34 @@ def test_linear_one_workspace_across_shapes():
         y = fl.fl_int4g_linear(bf16_dev(xb), w, N, ws=ws)
         _check(y, xb, Q, S, Z)
     assert fl.fl_int4g_status(ws) == 0
+
+
+# ------------------------------------------------------------ a4 prefill (tcgen05)
+
+@pytest.mark.parametrize("M", [33, 64, 127, 128, 129, 300, 1000, 1100])
+@pytest.mark.parametrize("NK", [(200, 384), (384, 1280)])
+def test_prefill_parity_small(M, NK):
+    N, K = NK
+    _, xb, Q, S, Z, w = _linear_case(M, N, K, layer=90 + K)
+    y = fl.fl_int4g_linear(bf16_dev(xb), w, N)
+    _check(y, xb, Q, S, Z)
+
+
+@pytest.mark.parametrize("KN", [(4096, 11008), (11008, 4096)])
+def test_prefill_full_size_sampled(KN):
+    """Prefill shapes M in {512, 2048} at full size, 64 sampled output columns
+    (all tokens) against the oracle."""
+    K, N = KN
+    W = inputs.dense_weight(N, K, layer=K + N + 1)
+    q, s, z = quantize_dev(W)
+    w = fl.fl_int4g_repack(q, s, z, N, K)
+    cols = np.unique(np.concatenate([np.sort(inputs.rng(7, K, N).choice(N, 64, replace=False)), [0, N - 1]]))
+    Qc, Sc, Zc = O.quantize(W[cols])
+    for M in (512, 2048):
+        xb = inputs.activations(M, K, stream=M + 1)
+        y = fl.fl_int4g_linear(bf16_dev(xb), w, N)
+        xf = O.bf16_value(xb)
+        ref, tol = O.linear_columns(xf, Qc, Sc, Zc, np.arange(len(cols)))
+        got = y.float().cpu().numpy().astype(np.float64)[:, cols]
+        assert np.all(np.abs(got - ref) <= tol), (M, np.max(np.abs(got - ref) / tol))
+        assert np.sqrt(np.mean((got - ref) ** 2) / np.mean(ref ** 2)) <= 1e-2
