@@ -138,6 +138,26 @@ int fl_int4g_linear_workspace(int M, int N, int K, size_t* out);
 int fl_int4g_linear(const void* x, int M, int K, const void* w, int N,
                     void* y, void* ws, size_t ws_bytes, fl_stream_t stream);
 
+/* Decode linear (M <= 32) that allocates nothing and takes no workspace.
+ * Not a step of the method: the pages have no counterpart; it exists for
+ * callers that cannot allocate device memory where they call (cudaMalloc can
+ * synchronize the device or fail under memory pressure, so latency-critical
+ * loops and code inside frameworks that own all allocations avoid it).
+ * Same arguments and result as fl_int4g_linear for M <= 32; the split-K
+ * scratch lives in a 16 MiB array inside the library that every GPU loading
+ * the library holds until exit.
+ *  - The first call on a device looks up that array's device address
+ *    (cudaGetSymbolAddress) with the device current: make it before any
+ *    stream capture.
+ *  - Each call clears the array's status and counter region on `stream`
+ *    (cudaMemsetAsync) before the kernel; all calls share the array, so calls
+ *    whose executions overlap on the GPU (different streams, or graphs
+ *    launched concurrently) race and must be serialized by the caller.
+ *  - FL_ERR_UNSUPPORTED for M > 32; FL_ERR_WORKSPACE when the shape needs more
+ *    scratch than the 16 MiB array (large N at M = 32); FL_ERR_ARG as for
+ *    fl_int4g_linear.  Device-side status is not reported by this variant. */
+int fl_int4g_linear_noalloc(const void* x, int M, int K, const void* w, int N, void* y, fl_stream_t stream);
+
 /* ------------------------------------------------------- a5-a7: MoE layer */
 
 /* Workspace bytes needed by fl_moe_int4g. */

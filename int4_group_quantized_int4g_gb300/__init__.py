@@ -17,7 +17,7 @@ __all__ = [
     "lib", "Int4gError", "FL_SOFTMAX", "FL_SIGMOID", "GROUP",
     "fl_strerror", "fl_int4g_version", "fl_int4g_status",
     "fl_int4g_quantize", "fl_int4g_repacked_bytes", "fl_int4g_repack", "fl_int4g_unrepack",
-    "fl_int4g_linear_workspace", "fl_int4g_linear",
+    "fl_int4g_linear_workspace", "fl_int4g_linear", "fl_int4g_linear_noalloc",
     "fl_moe_int4g_workspace", "fl_moe_int4g",
 ]
 
@@ -40,6 +40,7 @@ SIGNATURES = {
     "fl_int4g_unrepack": (_i, [_vp, ctypes.c_size_t, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "fl_int4g_linear_workspace": (_i, [_i, _i, _i, _c_size_p]),
     "fl_int4g_linear": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
+    "fl_int4g_linear_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp]),
     "fl_moe_int4g_workspace": (_i, [_i, _i, _i, _i, _i, _i, _c_size_p]),
     "fl_moe_int4g": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
                           _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
@@ -185,6 +186,19 @@ def fl_int4g_linear(x, w, N, y=None, ws=None):
         ws = _workspace(nb, x.device)
     _check("fl_int4g_linear",
            lib().fl_int4g_linear(_p(x), M, K, _p(w), N, _p(y), _p(ws), ws.numel(), _stream()))
+    return y
+
+
+def fl_int4g_linear_noalloc(x, w, N, y=None):
+    """Decode linear (M <= 32) with no workspace: for callers that cannot
+    allocate device memory where they call.  The library keeps the scratch in
+    a fixed device array shared by all calls (do not overlap calls on the GPU);
+    make the first call on a device before any stream capture."""
+    torch = _torch()
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check("fl_int4g_linear_noalloc", lib().fl_int4g_linear_noalloc(_p(x), M, K, _p(w), N, _p(y), _stream()))
     return y
 
 
