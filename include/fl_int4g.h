@@ -28,8 +28,12 @@
  *    offset (T * G + g) * 8512:
  *      [0, 8192)     codes, row r at r*64: logical column kk (0..127) goes to
  *                    32-bit word slot p = 4*(wl%4) + wl/4 (wl = kk/8) and
- *                    nibble e = 4*(o%2) + o/2 (o = kk%8) inside it, i.e.
- *                    byte 4p + e/2, high nibble iff e is odd;
+ *                    nibble e = 4*(o%2) + o/2 (o = kk%8) inside it; slot p
+ *                    is word p%4 of 16-byte chunk c = p/4, and chunk c of
+ *                    row r is stored at 16-byte position (c + (r/2)%4) % 4,
+ *                    i.e. byte 16*pos + 4*(p%4) + e/2, high nibble iff e odd
+ *                    (the rotation makes lanes that read one chunk of
+ *                    consecutive rows hit distinct shared-memory banks);
  *      [8192, 8448)  128 fp16 scales, row r at 8192 + 2r (little endian);
  *      [8448, 8512)  128 zero points, row r in byte 8448 + r/2, low nibble
  *                    for even r.

@@ -19,6 +19,7 @@
 // s_lo with s_hi = bf16(s16) and s_lo exact in bf16 (<= 3 bits), t =
 // s_lo*(q-z) is exact, and fma(s_hi, q-z, t) rounds once.
 #include <cuda.h>
+#include <type_traits>
 #include <cudaTypedefs.h>
 
 #include "fl_common.cuh"
@@ -90,6 +91,31 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive 32-bit columns of the calling warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// MMA with the A operand in tensor memory (M = 128 rows = lanes, K packed two
+// 16-bit elements per 32-bit column), B in shared memory.
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // TMA 2-D tile load global -> shared, completion counted on `bar`.
@@ -246,8 +272,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       uint8_t* a = stage_a(s);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int cidx = 2 * kh + ((cc + (r >> 1)) & 1);   // alternate the chunk order: fewer bank conflicts
-        const uint4 wv = *reinterpret_cast<const uint4*>(sb + r * 64 + cidx * 16);
+        const int cidx = 2 * kh + cc;
+        const uint4 wv = *reinterpret_cast<const uint4*>(sb + r * 64 + ((cidx + (r >> 1)) & 3) * 16);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t word = (&wv.x)[j];
@@ -358,10 +384,390 @@ int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
+// ======================================================================
+// Decode (M <= 32) on tcgen05: the stream of super-blocks of the decode
+// linear, split over K across the SMs exactly like the mma.sync kernel (CTA c
+// owns units [c*U/P, (c+1)*U/P) in layout order, a row tile split across CTAs
+// is finished by the last CTA to take its ticket, partials summed in CTA
+// order), but the dot products run on tcgen05:
+//   warp 0        producer: super-block by 1-D bulk copy, the x tile (NB token
+//                 rows x 128 k, rows past M read as zero) by TMA
+//   warp 1        TMEM allocation; lane 0 issues 8 MMAs per super-block into
+//                 one of two accumulator buffers (N = NB tokens)
+//   warps 4..11   dequantize: exact (q - z) bf16 into the swizzled A tile
+//   warps 12..15  epilogue: per super-block, read the accumulator (row r =
+//                 lane of the warp's TMEM quadrant) and add s16 * D into
+//                 register sums; at a row tile's end, write or hand off.
+// The fp16 scale is applied to the fp32 group sum (no rounding of s*(q-z)).
+struct TdParams {
+  const uint8_t* w;
+  __nv_bfloat16* y;
+  float* part;
+  int32_t* cnt;
+  int32_t* status;
+  int U, M, K, N, T, G, P;
+};
+
+template <int NB>
+struct TdCfg {
+  static constexpr int kXBytes = NB * 256;                        // NB rows x 128 k bf16 (two swizzled halves)
+  static constexpr int kSbRing = 20;                              // super-blocks in flight per CTA
+  static constexpr int kARing = 4;                                // dequantized A tiles (tensor memory) + x tiles
+  static constexpr int kDRing = 8;                                // accumulators in tensor memory
+  static constexpr int kSmem = kARing * kXBytes + kSbRing * kSbBytes + 1024 + 512;
+  static constexpr uint32_t kTmemCols = 512;                      // A ring 4 x 64 columns, D ring 8 x NB
+};
+
+constexpr int kTdThreads = 16 * 32;
+constexpr int kTdDeq0 = 4, kTdEpi0 = 12;
+
+__host__ __device__ __forceinline__ int td_unit_begin(int c, int U, int P) {
+  return static_cast<int>(static_cast<long long>(c) * U / P);
+}
+__host__ __device__ __forceinline__ int td_cta_of_unit(int u, int U, int P) {
+  return static_cast<int>((static_cast<long long>(u + 1) * P - 1) / U);
+}
+
+// Final sums of row tile T for this epilogue thread's row: write them or hand
+// them off (returns true when a ticket is owed).
+template <int NB>
+__device__ __forceinline__ bool td_store(const TdParams& p, int T, int c, int u0, int u1, int r, const float* tot) {
+  const int n = T * kRowTile + r;
+  if (T * p.G >= u0 && (T + 1) * p.G <= u1) {
+    if (n < p.N) {
+#pragma unroll
+      for (int m = 0; m < NB; ++m)
+        if (m < p.M) p.y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(tot[m]);
+    }
+    return false;
+  }
+  float* pp = p.part + (static_cast<size_t>(c + T) * kRowTile + r) * NB;
+#pragma unroll
+  for (int m = 0; m < NB; m += 4) __stcg(reinterpret_cast<float4*>(pp + m), make_float4(tot[m], tot[m + 1], tot[m + 2], tot[m + 3]));
+  return true;
+}
+
+template <int NB>
+__device__ __forceinline__ void td_ticket(const TdParams& p, int T, int q, int lane) {
+  __syncwarp();
+  const int cf = td_cta_of_unit(T * p.G, p.U, p.P), cl = td_cta_of_unit((T + 1) * p.G - 1, p.U, p.P);
+  int last = 0;
+  if (lane == 0) {
+    fence_acq_rel_gpu();
+    last = atomicAdd(&p.cnt[T * 8 + q], 1) == cl - cf;
+    if (last) fence_acq_rel_gpu();
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  const int r = q * 32 + lane;
+  const int n = T * kRowTile + r;
+  float acc[NB];
+#pragma unroll
+  for (int m = 0; m < NB; ++m) acc[m] = 0.f;
+  for (int cc = cf; cc <= cl; ++cc) {   // CTA order: deterministic
+    const float* pp = p.part + (static_cast<size_t>(cc + T) * kRowTile + r) * NB;
+#pragma unroll
+    for (int m = 0; m < NB; m += 4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(pp + m));
+      acc[m] += v.x, acc[m + 1] += v.y, acc[m + 2] += v.z, acc[m + 3] += v.w;
+    }
+  }
+  if (n < p.N) {
+#pragma unroll
+    for (int m = 0; m < NB; ++m)
+      if (m < p.M) p.y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(acc[m]);
+  }
+  __syncwarp();
+  if (lane == 0) p.cnt[T * 8 + q] = 0;
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_constant__ CUtensorMap xmap, const TdParams p) {
+  using C = TdCfg<NB>;
+  constexpr int RS = C::kSbRing, RA = C::kARing;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* xbuf = smem;                                    // [RA][NB*256] (1 KB aligned)
+  uint8_t* sbuf = xbuf + RA * C::kXBytes;                  // [RS][8512]
+  uint64_t* sb_full = reinterpret_cast<uint64_t*>(sbuf + RS * kSbBytes);
+  uint64_t* sb_empty = sb_full + RS;   // dequant (8 warps) + epilogue (4 warps)
+  uint64_t* x_full = sb_empty + RS;    // x tile landed
+  uint64_t* a_full = x_full + RA;      // A tile dequantized (8 warps)
+  uint64_t* a_empty = a_full + RA;     // MMAs on the A/x slot done
+  constexpr int RD = C::kDRing;
+  uint64_t* dfull = a_empty + RA;      // [RD]
+  uint64_t* dempty = dfull + RD;       // [RD]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + RD);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  const int u0 = td_unit_begin(c, p.U, p.P), u1 = td_unit_begin(c + 1, p.U, p.P);
+  const int nu = u1 - u0;
+
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < RS; ++j) {
+      mbar_init(&sb_full[j], 1);
+      mbar_init(&sb_empty[j], 8 + 4);
+    }
+    for (int a = 0; a < RA; ++a) {
+      mbar_init(&x_full[a], 1);
+      mbar_init(&a_full[a], 8);
+      mbar_init(&a_empty[a], 1);
+    }
+    for (int b = 0; b < RD; ++b) {
+      mbar_init(&dfull[b], 1);
+      mbar_init(&dempty[b], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_d = *tmem_slot;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- super-block producer (weights only: they do not depend on the previous kernel)
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      for (int i = 0; i < nu; ++i) {
+        const int j = i % RS;
+        if (i >= RS && !mbar_wait(&sb_empty[j], ((i / RS) - 1) & 1u)) {
+          set_status(p.status, FL_ERR_TIMEOUT, 31);
+          for (int jj = 0; jj < RS; ++jj) {
+            const int nf = i / RS + (jj < i % RS ? 1 : 0);
+            if (nf > 0) mbar_wait(&sb_full[jj], static_cast<uint32_t>(nf - 1) & 1u);
+          }
+          break;
+        }
+        mbar_arrive_expect_tx(&sb_full[j], kSbBytes);
+        bulk_g2s_hint(sbuf + j * kSbBytes, p.w + static_cast<size_t>(u0 + i) * kSbBytes, kSbBytes, &sb_full[j], pol);
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- x producer: the tile of x for each super-block's group
+    if (lane == 0) {
+      pdl_wait();
+      for (int i = 0; i < nu; ++i) {
+        const int a = i % RA;
+        if (i >= RA && !mbar_wait(&a_empty[a], ((i / RA) - 1) & 1u)) {
+          set_status(p.status, FL_ERR_TIMEOUT, 35);
+          for (int aa = 0; aa < RA; ++aa) {
+            const int nf = i / RA + (aa < i % RA ? 1 : 0);
+            if (nf > 0) mbar_wait(&x_full[aa], static_cast<uint32_t>(nf - 1) & 1u);
+          }
+          break;
+        }
+        const int g = (u0 + i) % p.G;
+        mbar_arrive_expect_tx(&x_full[a], C::kXBytes);
+        tma_load_2d(xbuf + a * C::kXBytes, &xmap, g * kGroup, 0, &x_full[a]);
+        tma_load_2d(xbuf + a * C::kXBytes + NB * 128, &xmap, g * kGroup + 64, 0, &x_full[a]);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16<NB>();
+      for (int i = 0; i < nu; ++i) {
+        const int a = i % RA, b = i % RD;
+        const uint32_t pa = (i / RA) & 1u;
+        if (!mbar_wait(&a_full[a], pa) || !mbar_wait(&x_full[a], pa) ||
+            (i >= RD && !mbar_wait(&dempty[b], ((i / RD) - 1) & 1u))) {
+          set_status(p.status, FL_ERR_TIMEOUT, 32);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t x0 = smem_u32(xbuf + a * C::kXBytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_ta(tmem_d + 256 + b * NB, tmem_d + a * 64 + h * 32 + kk * 8,
+                         sw128_desc(x0 + h * NB * 128 + kk * 32), idesc, (h | kk) != 0);
+        umma_commit(&a_empty[a]);
+        umma_commit(&dfull[b]);
+      }
+    }
+  } else if (warp >= kTdDeq0 && warp < kTdEpi0) {
+    // ---------------- dequant: thread = (row r, K half h) -> exact (q - z) bf16 into the A ring in
+    // tensor memory: row r = lane of the warp's quadrant, column c holds k = 2c, 2c+1 of the half
+    const int q = warp & 3, h = (warp - kTdDeq0) >> 2;
+    const int r = q * 32 + lane;
+    const uint32_t trow = static_cast<uint32_t>(q * 32) << 16;
+    // software pipeline: the tensor-memory store of super-block i completes
+    // while super-block i+1 is dequantized; i is signalled after that
+    int prev = -1;
+    for (int i = 0; i < nu; ++i) {
+      const int j = i % RS, a = i % RA;
+      if (!mbar_wait(&sb_full[j], (i / RS) & 1u) || (i >= RA && !mbar_wait(&a_empty[a], ((i / RA) - 1) & 1u))) {
+        set_status(p.status, FL_ERR_TIMEOUT, 33);
+        break;
+      }
+      tc_fence_after();
+      const uint8_t* sb = sbuf + j * kSbBytes;
+      const uint32_t z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
+      const uint32_t zz = bf16_bias_pair(z);
+      // logical 8-column chunks wl = 8h .. 8h+7 live in word slot p = 4*(wl%4) + wl/4,
+      // i.e. in 16-byte chunk p/4 = wl%4, word p%4 = wl/4
+      uint4 cv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) cv[t] = *reinterpret_cast<const uint4*>(sb + r * 64 + ((t + (r >> 1)) & 3) * 16);
+      uint32_t o[32];
+      // h is uniform across the warp: two static copies keep cv in registers
+      auto unpack = [&](auto H) {
+        constexpr int hh = decltype(H)::value;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int wl = 8 * hh + t;
+          const uint32_t word = (&cv[wl & 3].x)[wl >> 2];
+#pragma unroll
+          for (int pi = 0; pi < 4; ++pi) o[4 * t + pi] = bf16x2_sub(nib_pair_bf16(word, pi), zz);
+        }
+      };
+      if (h == 0)
+        unpack(std::integral_constant<int, 0>());
+      else
+        unpack(std::integral_constant<int, 1>());
+      if (prev >= 0) {
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&a_full[prev % RA]);
+          mbar_arrive(&sb_empty[prev % RS]);
+        }
+      }
+      tmem_st32(tmem_d + trow + a * 64 + h * 32, o);
+      prev = i;
+    }
+    if (prev >= 0) {
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&a_full[prev % RA]);
+        mbar_arrive(&sb_empty[prev % RS]);
+      }
+    }
+  } else if (warp >= kTdEpi0) {
+    // ---------------- epilogue: row r of every super-block, all tokens
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    pdl_wait();   // y and the workspace: only once the previous kernel is done
+    float tot[NB];
+#pragma unroll
+    for (int m = 0; m < NB; ++m) tot[m] = 0.f;
+    int T = u0 / p.G, owed0 = -1;
+    bool ok = true;
+    for (int i = 0; i < nu; ++i) {
+      const int b = i % RD, j = i % RS;
+      if (!mbar_wait(&dfull[b], (i / RD) & 1u) || !mbar_wait(&sb_full[j], (i / RS) & 1u)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 34);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float sc = __half2float(reinterpret_cast<const __half*>(sbuf + j * kSbBytes + kSbNib)[r]);
+      float v[32];
+      tmem_ld32(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + 256 + b * NB, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&dempty[b]);
+        mbar_arrive(&sb_empty[j]);
+      }
+#pragma unroll
+      for (int m = 0; m < NB; ++m) tot[m] = fmaf(sc, v[m], tot[m]);
+      const int u = u0 + i;
+      if ((u + 1) % p.G == 0 && u + 1 < u1) {
+        if (td_store<NB>(p, T, c, u0, u1, r, tot)) owed0 = T;
+#pragma unroll
+        for (int m = 0; m < NB; ++m) tot[m] = 0.f;
+        ++T;
+      }
+    }
+    if (ok && nu > 0) {
+      const bool owed1 = td_store<NB>(p, T, c, u0, u1, r, tot);
+      if (owed0 >= 0) td_ticket<NB>(p, owed0, q, lane);
+      if (owed1) td_ticket<NB>(p, T, q, lane);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_d, C::kTmemCols);
+  }
+}
+
+template <int NB>
+int launch_tcdec(const void* x, int M, int K, const void* w, int N, void* y, void* ws, size_t cnt_off,
+                 size_t part_off, cudaStream_t s) {
+  using C = TdCfg<NB>;
+  auto enc = encode_fn();
+  if (!enc) return FL_ERR_CUDA;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(NB)};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return FL_ERR_CUDA;
+  TdParams p;
+  p.w = static_cast<const uint8_t*>(w);
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.status = static_cast<int32_t*>(ws);
+  p.cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + cnt_off);
+  p.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + part_off);
+  p.M = M;
+  p.K = K;
+  p.N = N;
+  p.T = (N + kRowTile - 1) / kRowTile;
+  p.G = K / kGroup;
+  p.U = p.T * p.G;
+  const int sms = flh::sm_count();
+  p.P = p.U < sms ? p.U : sms;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(k_linear_tcdec<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+      return FL_ERR_CUDA;
+    attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.P));
+  cfg.blockDim = dim3(kTdThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k_linear_tcdec<NB>, map, p) != cudaSuccess) return FL_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+}
+
 }  // namespace
 
 // Prefill path of fl_int4g_linear (M >= 64): one tcgen05 kernel launch.
 int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_t* status, cudaStream_t s) {
   if (M >= 1024) return launch_tc<256>(x, M, K, w, N, y, status, s);
   return launch_tc<128>(x, M, K, w, N, y, status, s);
+}
+
+// Decode path of fl_int4g_linear on tcgen05 (M <= 32); the workspace layout is
+// the decode kernel's: status, counters at cnt_off, partial slots at part_off
+// ((P + T) slots of 128 rows x NB floats).
+int fl_linear_tcdec(const void* x, int M, int K, const void* w, int N, void* y, void* ws, size_t cnt_off,
+                    size_t part_off, cudaStream_t s) {
+  if (M <= 16) return launch_tcdec<16>(x, M, K, w, N, y, ws, cnt_off, part_off, s);
+  return launch_tcdec<32>(x, M, K, w, N, y, ws, cnt_off, part_off, s);
 }

@@ -425,6 +425,24 @@ static bool linear_args_ok(const void* x, int M, int K, const void* w, int N, co
 }
 
 int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_t* status, cudaStream_t s);
+int fl_linear_tcdec(const void* x, int M, int K, const void* w, int N, void* y, void* ws, size_t cnt_off,
+                    size_t part_off, cudaStream_t s);
+
+// Workspace of the tcgen05 decode kernel: the decode layout (status, fixed
+// counter region) with (min(U, SMs) + T) partial slots of 128 rows x NB floats,
+// NB = 16 for M <= 16, else 32.
+static bool tcdec_plan(int M, int N, int K, size_t* cnt_off, size_t* part_off, size_t* total) {
+  RowsPlan pl;
+  if (!make_rows_plan(M, N, K, flh::sm_count(), &pl)) return false;
+  const int NB = M <= 16 ? 16 : 32;
+  const long long sms = flh::sm_count();
+  const long long P = pl.U < sms ? pl.U : sms;
+  *cnt_off = pl.cnt_off;
+  *part_off = pl.part_off;
+  *total = pl.part_off + static_cast<size_t>(P + pl.T) * kRowTile * NB * 4;
+  if (*total < pl.ws_bytes) *total = pl.ws_bytes;
+  return true;
+}
 
 extern "C" int fl_int4g_linear_workspace(int M, int N, int K, size_t* out) {
   if (!out || M < 1 || N < 1 || K < kGroup || K % kGroup) return FL_ERR_ARG;
@@ -432,7 +450,8 @@ extern "C" int fl_int4g_linear_workspace(int M, int N, int K, size_t* out) {
     *out = kStatusBytes;   // the prefill kernel needs only the status block
     return FL_OK;
   }
-  return fl_linear_rows_workspace(M, N, K, out);
+  size_t a, b;
+  return tcdec_plan(M, N, K, &a, &b, out) ? FL_OK : FL_ERR_ARG;
 }
 
 extern "C" int fl_int4g_linear(const void* x, int M, int K, const void* w, int N, void* y, void* ws,
@@ -443,5 +462,11 @@ extern "C" int fl_int4g_linear(const void* x, int M, int K, const void* w, int N
     if (ws_bytes < kStatusBytes) return FL_ERR_WORKSPACE;
     return fl_linear_tc(x, M, K, w, N, y, static_cast<int32_t*>(ws), s);
   }
-  return fl_linear_rows(x, M, K, w, N, y, ws, ws_bytes, s);
+  size_t cnt_off, part_off, need;
+  if (!tcdec_plan(M, N, K, &cnt_off, &part_off, &need)) return FL_ERR_ARG;
+  if (ws_bytes < need) return FL_ERR_WORKSPACE;
+  // M <= 16: the register-dequant mma.sync stream is faster (one warp hand-off
+  // per two super-blocks); 16 < M <= 32: tcgen05 (mma.sync issue-bound there)
+  if (M <= 16) return fl_linear_rows(x, M, K, w, N, y, ws, ws_bytes, s);
+  return fl_linear_tcdec(x, M, K, w, N, y, ws, cnt_off, part_off, s);
 }

@@ -106,10 +106,12 @@ __global__ void k_repack(const uint8_t* __restrict__ q, const uint16_t* __restri
   const int ZB = (G + 1) / 2;
   uint8_t* dst = out + static_cast<size_t>(sbi) * kSbBytes;
   for (int wi = threadIdx.x; wi < kSbNib / 4; wi += blockDim.x) {
-    const int r = wi >> 4, p = wi & 15;
+    const int r = wi >> 4, pw = wi & 15;
     const int n = T * kRowTile + r;
     uint32_t o = 0;
     if (n < N) {
+      // word pw of the row is word pw%4 of chunk (pw/4 - (r/2)%4) % 4, i.e. slot p
+      const int p = 4 * (((pw >> 2) - (r >> 1)) & 3) + (pw & 3);
       const int wl = 4 * (p & 3) + (p >> 2);
       const uint32_t cw =
           *reinterpret_cast<const uint32_t*>(q + static_cast<size_t>(n) * (K / 2) + g * (kGroup / 2) + 4 * wl);
@@ -143,9 +145,10 @@ __global__ void k_unrepack(const uint8_t* __restrict__ in, int N, int K, int G, 
     if (g >= G) break;
     const uint8_t* src = in + (static_cast<size_t>(T) * G + g) * kSbBytes;
     for (int wi = threadIdx.x; wi < kSbNib / 4; wi += blockDim.x) {
-      const int r = wi >> 4, p = wi & 15;
+      const int r = wi >> 4, pw = wi & 15;
       const int n = T * kRowTile + r;
       if (n >= N) continue;
+      const int p = 4 * (((pw >> 2) - (r >> 1)) & 3) + (pw & 3);
       const int wl = 4 * (p & 3) + (p >> 2);
       *reinterpret_cast<uint32_t*>(q + static_cast<size_t>(n) * (K / 2) + g * (kGroup / 2) + 4 * wl) =
           tiled_to_canon_word(reinterpret_cast<const uint32_t*>(src)[wi]);

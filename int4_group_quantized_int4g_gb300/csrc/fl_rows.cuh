@@ -26,8 +26,10 @@ template <int NT, bool FOLD>
 __device__ __forceinline__ void unit_dot(const uint8_t* sb, const uint8_t* sx, int M, int r0, int gid, int tig,
                                          float (&acc)[NT][4], float& s0, float& s1, uint32_t& z0, uint32_t& z1,
                                          int ntiles = NT) {
-  const uint4 wa = *reinterpret_cast<const uint4*>(sb + r0 * 64 + tig * 16);
-  const uint4 wb = *reinterpret_cast<const uint4*>(sb + (r0 + 8) * 64 + tig * 16);
+  // chunk tig of rows r0 and r0+8 (both rotated by (r0/2)%4 in the layout)
+  const int pos = ((tig + (r0 >> 1)) & 3) * 16;
+  const uint4 wa = *reinterpret_cast<const uint4*>(sb + r0 * 64 + pos);
+  const uint4 wb = *reinterpret_cast<const uint4*>(sb + (r0 + 8) * 64 + pos);
   const __half* sc = reinterpret_cast<const __half*>(sb + kSbNib);
   s0 = __half2float(sc[r0]);
   s1 = __half2float(sc[r0 + 8]);

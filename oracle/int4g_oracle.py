@@ -262,20 +262,24 @@ def tiled_bytes(N, K, group=GROUP):
     return (Np // ROW_TILE) * (K // group) * SB_BYTES
 
 
-def _nibble_address(kk):
-    """Position of logical column kk (0..127 inside a group) in a 64-byte
-    row of a super-block: returns (byte offset, nibble half).
+def _nibble_address(kk, r):
+    """Position of logical column kk (0..127 inside a group) of row r (0..127
+    inside a row tile) in the row's 64 bytes: returns (byte offset, nibble half).
 
     The 16 32-bit words of a row hold 8 columns each; word slot p holds
     logical word 4*(p%4) + p//4, and inside a word, nibble e holds column
     offset 2*(e%4) + e//4.  Inverted: logical word wl -> p = 4*(wl%4) +
-    wl//4, offset o -> e = 4*(o%2) + o//2.
+    wl//4, offset o -> e = 4*(o%2) + o//2.  The four 16-byte chunks of row r
+    (slots 4c..4c+3 form chunk c) are rotated by (r//2)%4: chunk c sits at
+    16-byte position (c + (r//2)%4) % 4.
     """
     kk = np.asarray(kk)
+    r = np.asarray(r)
     wl, o = kk // 8, kk % 8
     p = 4 * (wl % 4) + wl // 4
     e = 4 * (o % 2) + o // 2
-    return 4 * p + e // 2, e % 2
+    pos = (p // 4 + (r // 2) % 4) % 4
+    return 16 * pos + 4 * (p % 4) + e // 2, e % 2
 
 
 def repack(Q, S, Z, N, K, group=GROUP):
@@ -283,7 +287,7 @@ def repack(Q, S, Z, N, K, group=GROUP):
 
     Super-block (T, g) -- rows 128T..128T+127, group g -- starts at byte
     (T * G + g) * 8512 and holds: 128 rows x 64 B of codes (row r at r*64,
-    columns placed by _nibble_address), then 128 fp16 scales (row r at
+    columns placed by _nibble_address(kk, r)), then 128 fp16 scales (row r at
     8192 + 2r, little endian), then 128 zero points (row r in byte
     8448 + r//2, low nibble = even r).  Rows past N are zero.
     """
@@ -298,15 +302,15 @@ def repack(Q, S, Z, N, K, group=GROUP):
     z = np.zeros((Np, G), np.uint8)
     z[:N] = unpack_zeros(Z, G)
     out = np.zeros(tiled_bytes(N, K, group), np.uint8)
-    boff, half = _nibble_address(np.arange(GROUP))
     rows = np.arange(ROW_TILE)
+    boff, half = _nibble_address(np.arange(GROUP)[None, :], rows[:, None])   # [128 rows, 128 columns]
     for T in range(Np // ROW_TILE):
         for g in range(G):
             base = (T * G + g) * SB_BYTES
             blk = q[T * ROW_TILE:(T + 1) * ROW_TILE, g * group:(g + 1) * group]
             nib = np.zeros((ROW_TILE, 64), np.uint8)
             for kk in range(GROUP):
-                nib[:, boff[kk]] |= (blk[:, kk] << (4 * half[kk])).astype(np.uint8)
+                nib[rows, boff[:, kk]] |= (blk[:, kk] << (4 * half[:, kk])).astype(np.uint8)
             out[base:base + SB_NIB] = nib.reshape(-1)
             sc = s[T * ROW_TILE:(T + 1) * ROW_TILE, g]
             out[base + SB_NIB:base + SB_NIB + SB_SCALE] = sc.astype('<u2').view(np.uint8)
@@ -326,14 +330,14 @@ def unrepack(buf, N, K, group=GROUP):
     q = np.zeros((Np, K), np.uint8)
     s = np.zeros((Np, G), np.uint16)
     z = np.zeros((Np, G), np.uint8)
-    boff, half = _nibble_address(np.arange(GROUP))
     rows = np.arange(ROW_TILE)
+    boff, half = _nibble_address(np.arange(GROUP)[None, :], rows[:, None])
     for T in range(Np // ROW_TILE):
         for g in range(G):
             base = (T * G + g) * SB_BYTES
             nib = buf[base:base + SB_NIB].reshape(ROW_TILE, 64)
             for kk in range(GROUP):
-                q[T * ROW_TILE:(T + 1) * ROW_TILE, g * group + kk] = (nib[:, boff[kk]] >> (4 * half[kk])) & 0xF
+                q[T * ROW_TILE:(T + 1) * ROW_TILE, g * group + kk] = (nib[rows, boff[:, kk]] >> (4 * half[:, kk])) & 0xF
             s[T * ROW_TILE:(T + 1) * ROW_TILE, g] = buf[base + SB_NIB:base + SB_NIB + SB_SCALE].view('<u2')
             zb = buf[base + SB_NIB + SB_SCALE:base + SB_BYTES]
             z[T * ROW_TILE:(T + 1) * ROW_TILE, g] = (zb[rows // 2] >> (4 * (rows % 2))) & 0xF

@@ -206,17 +206,18 @@ def test_linear_columns_equals_full():
 def test_repack_hand_bytes():
     """Byte addresses worked by hand from the layout definition:
     super-block (T, g) at (T*G+g)*8512; row r codes at r*64; column kk ->
-    word wl=kk//8, offset o=kk%8, slot p=4*(wl%4)+wl//4, nibble e=4*(o%2)+o//2,
-    byte 4p+e//2, high nibble iff e odd; scales at 8192+2r; zeros at
-    8448+r//2 (high nibble iff r odd)."""
+    word wl=kk//8, offset o=kk%8, slot p=4*(wl%4)+wl//4, nibble e=4*(o%2)+o//2;
+    slot p is word p%4 of chunk p//4, and chunk c of row r sits at 16-byte
+    position (c + (r//2)%4) % 4: byte 16*pos + 4*(p%4) + e//2, high nibble
+    iff e odd; scales at 8192+2r; zeros at 8448+r//2 (high nibble iff r odd)."""
     N, K = 130, 256
     G = 2
     q = np.zeros((N, K), np.uint8)
     q[0, 0] = 5        # T0 g0 r0 kk0: p0 e0 -> byte 0 low
     q[0, 1] = 7        # kk1: o1 -> e4 -> byte 2 low
     q[1, 8] = 9        # kk8: wl1 -> p4 -> byte 64+16 low
-    q[2, 127] = 3      # kk127: wl15 o7 -> p15 e7 -> byte 128+60+3 high
-    q[127, 130] = 15   # g1 kk2: p0, o2 -> e1 -> byte 0 high, row 127
+    q[2, 127] = 3      # kk127: wl15 o7 -> p15 (chunk 3, word 3) e7; row 2 rotates by 1 -> pos 0 -> byte 128+12+3 high
+    q[127, 130] = 15   # g1 kk2: p0, o2 -> e1; row 127 rotates by 3 -> pos 3 -> byte 127*64+48 high
     q[129, 0] = 1      # T1 g0 r1
     S = np.zeros((N, G), np.uint16)
     S[3, 1] = 0x1234
@@ -224,8 +225,8 @@ def test_repack_hand_bytes():
     z[5, 0] = 11
     buf = O.repack(O.pack_codes(q), S, O.pack_zeros(z), N, K)
     assert buf.size == 2 * 2 * 8512
-    expect = {0: 0x05, 2: 0x07, 80: 0x09, 191: 0x30,
-              8512 + 8128: 0xF0,
+    expect = {0: 0x05, 2: 0x07, 80: 0x09, 143: 0x30,
+              8512 + 8176: 0xF0,
               8512 + 8192 + 6: 0x34, 8512 + 8192 + 7: 0x12,
               8450: 0xB0,
               2 * 8512 + 64: 0x01}
@@ -247,7 +248,8 @@ def _brute_tiled_dequant(buf, N, K):
             wl, o = divmod(kk, 8)
             p = 4 * (wl % 4) + wl // 4
             e = 4 * (o % 2) + o // 2
-            b = int(buf[base + r * 64 + 4 * p + e // 2])
+            pos = (p // 4 + (r // 2) % 4) % 4
+            b = int(buf[base + r * 64 + 16 * pos + 4 * (p % 4) + e // 2])
             qv = (b >> 4) if e % 2 else (b & 15)
             sv = float(np.frombuffer(bytes(buf[base + 8192 + 2 * r: base + 8194 + 2 * r]), '<f2')[0])
             zb = int(buf[base + 8448 + r // 2])
