@@ -35,11 +35,12 @@ constexpr int kABytes = 128 * 128 * 2;  // A tile of one group: 128 rows x 128 k
 template <int BN>
 struct TcCfg {
   static constexpr int kBBytes = BN * 128 * 2;          // B tile of one group: BN rows x 128 k bf16
-  static constexpr int kStages = BN == 256 ? 2 : 3;
-  static constexpr int kStageBytes = kABytes + kBBytes + kSbBytes + 64;   // + padding to keep 1 KB alignment
+  static constexpr int kStageBytes = kBBytes + kSbBytes;
   static constexpr int kStageStride = (kStageBytes + 1023) / 1024 * 1024;
+  static constexpr int kStages = BN == 256 ? 3 : 5;
   static constexpr int kSmem = kStages * kStageStride + 1024 /*align slack*/ + 256 /*barriers*/;
-  static constexpr uint32_t kTmemCols = BN;             // fp32 accumulator columns (power of 2)
+  static constexpr int kARing = 2;                      // dequantized A tiles in tensor memory (64 columns each)
+  static constexpr uint32_t kTmemCols = BN == 256 ? 512 : 256;   // accumulator (BN) + A ring (128)
 };
 
 struct TcParams {
@@ -160,30 +161,32 @@ __device__ __forceinline__ uint32_t bfma2(uint32_t a, uint32_t b, uint32_t c) {
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   using C = TcCfg<BN>;
+  constexpr int RA = C::kARing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* bars = smem + C::kStages * C::kStageStride;
   uint64_t* full = reinterpret_cast<uint64_t*>(bars);          // B + super-block landed
-  uint64_t* afull = full + C::kStages;                         // A dequantized
-  uint64_t* empty = afull + C::kStages;                        // MMAs of the stage done
-  uint64_t* dfull = empty + C::kStages;                        // accumulator final
+  uint64_t* empty = full + C::kStages;                         // MMAs of the stage done
+  uint64_t* afull = empty + C::kStages;                        // A slot dequantized (tensor memory)
+  uint64_t* aempty = afull + RA;                               // MMAs reading the A slot done
+  uint64_t* dfull = aempty + RA;                               // accumulator final
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfull + 1);
-  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = blockIdx.x / p.mtiles, mt = blockIdx.x % p.mtiles;
-  auto stage_a = [&](int s) { return smem + s * C::kStageStride; };
-  auto stage_b = [&](int s) { return smem + s * C::kStageStride + kABytes; };
-  auto stage_sb = [&](int s) { return smem + s * C::kStageStride + kABytes + C::kBBytes; };
+  auto stage_b = [&](int s) { return smem + s * C::kStageStride; };
+  auto stage_sb = [&](int s) { return smem + s * C::kStageStride + C::kBBytes; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&afull[s], 8);
       mbar_init(&empty[s], 1);
     }
+    for (int a = 0; a < RA; ++a) {
+      mbar_init(&afull[a], 8);
+      mbar_init(&aempty[a], 1);
+    }
     mbar_init(dfull, 1);
-    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -193,7 +196,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_d = *tmem_slot;
+  const uint32_t tmem_d = *tmem_slot;          // accumulator: columns [0, BN)
+  const uint32_t tmem_a = tmem_d + BN;         // A ring: columns [BN, BN + 64 * RA)
   pdl_launch_dependents();
 
   if (warp == 0) {
@@ -206,8 +210,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       for (int g = 0; g < p.G; ++g) {
         if (g >= C::kStages && !mbar_wait(&empty[s], ph ^ 1u)) {
           set_status(p.status, FL_ERR_TIMEOUT, 21);
-          atomicExch(abort_flag, 1);
-          // let the copies already issued land before the CTA retires
           for (int j = 0; j < C::kStages; ++j) {
             const int nf = g / C::kStages + (j < g % C::kStages ? 1 : 0);
             if (nf > 0) mbar_wait(&full[j], static_cast<uint32_t>(nf - 1) & 1u);
@@ -222,45 +224,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: A from tensor memory, B from shared memory
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16<BN>();
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
       for (int g = 0; g < p.G; ++g) {
-        if (!mbar_wait(&afull[s], ph)) {
+        const int a = g % RA;
+        if (!mbar_wait(&full[s], ph) || !mbar_wait(&afull[a], (g / RA) & 1u)) {
           set_status(p.status, FL_ERR_TIMEOUT, 22);
-          atomicExch(abort_flag, 1);
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(stage_a(s)), b0 = smem_u32(stage_b(s));
+        const uint32_t b0 = smem_u32(stage_b(s));
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem_d, sw128_desc(a0 + h * 16384 + kk * 32), sw128_desc(b0 + h * BN * 128 + kk * 32), idesc,
-                      (g | h | kk) != 0);
+            umma_bf16_ta(tmem_d, tmem_a + a * 64 + h * 32 + kk * 8, sw128_desc(b0 + h * BN * 128 + kk * 32), idesc,
+                         (g | h | kk) != 0);
         umma_commit(&empty[s]);
+        umma_commit(&aempty[a]);
         if (++s == C::kStages) s = 0, ph ^= 1u;
       }
       if (ok) umma_commit(dfull);
     }
   } else if (warp >= kDeqWarp0) {
-    // ---------------- dequant: thread = weight row r, chunk pair kh of the row's codes
-    const int q = warp & 3, kh = (warp - kDeqWarp0) >> 2;
+    // ---------------- dequant: thread = (weight row r = TMEM lane, K half h);
+    // each weight becomes the correctly rounded bf16 of s16 * (q - z)
+    const int q = warp & 3, h = (warp - kDeqWarp0) >> 2;
     const int r = q * 32 + lane;
+    const uint32_t trow = static_cast<uint32_t>(q * 32) << 16;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
     for (int g = 0; g < p.G; ++g) {
-      if (!mbar_wait(&full[s], ph)) {
+      const int a = g % RA;
+      if (!mbar_wait(&full[s], ph) || (g >= RA && !mbar_wait(&aempty[a], ((g / RA) - 1) & 1u))) {
         set_status(p.status, FL_ERR_TIMEOUT, 23);
         ok = false;
         break;
       }
+      tc_fence_after();
       const uint8_t* sb = stage_sb(s);
       const float sf = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
       const __nv_bfloat16 shi = __float2bfloat16_rn(sf);
@@ -269,29 +276,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       const uint32_t lo2 = static_cast<uint32_t>(__bfloat16_as_ushort(slo)) * 0x00010001u;
       const uint32_t z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
       const uint32_t zz = bf16_bias_pair(z);
-      uint8_t* a = stage_a(s);
+      uint4 cv[4];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int cidx = 2 * kh + cc;
-        const uint4 wv = *reinterpret_cast<const uint4*>(sb + r * 64 + ((cidx + (r >> 1)) & 3) * 16);
+      for (int t = 0; t < 4; ++t) cv[t] = *reinterpret_cast<const uint4*>(sb + r * 64 + ((t + (r >> 1)) & 3) * 16);
+      uint32_t o[32];
+      auto unpack = [&](auto H) {
+        constexpr int hh = decltype(H)::value;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t word = (&wv.x)[j];
-          uint32_t o[4];
+        for (int t = 0; t < 8; ++t) {
+          const int wl = 8 * hh + t;
+          const uint32_t word = (&cv[wl & 3].x)[wl >> 2];
 #pragma unroll
           for (int pi = 0; pi < 4; ++pi) {
             const uint32_t qz = bf16x2_sub(nib_pair_bf16(word, pi), zz);
-            o[pi] = bfma2(hi2, qz, bmul2(lo2, qz));
+            o[4 * t + pi] = bfma2(hi2, qz, bmul2(lo2, qz));
           }
-          const int wl = cidx + 4 * j;                      // logical 8-column chunk 0..15
-          const int half = wl >> 3, c = wl & 7;
-          *reinterpret_cast<uint4*>(a + half * 16384 + r * 128 + ((c ^ (r & 7)) << 4)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
         }
-      }
-      fence_proxy_async();
+      };
+      if (h == 0)
+        unpack(std::integral_constant<int, 0>());
+      else
+        unpack(std::integral_constant<int, 1>());
+      tmem_st32(tmem_a + trow + a * 64 + h * 32, o);
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&afull[s]);
+      if (lane == 0) mbar_arrive(&afull[a]);
       if (++s == C::kStages) s = 0, ph ^= 1u;
     }
     if (warp < kDeqWarp0 + 4) {
@@ -302,7 +312,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
 #pragma unroll 1
         for (int j = 0; j < BN; j += 32) {
           float v[32];
-          tmem_ld32(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + j, v);
+          tmem_ld32(tmem_d + trow + j, v);
           if (n < p.N) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
