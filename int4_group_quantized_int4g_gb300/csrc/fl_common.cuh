@@ -18,6 +18,14 @@ constexpr int kSbScale = 256;   // 128 fp16 scales
 constexpr int kSbZero = 64;     // 128 4-bit zero points
 constexpr int kSbBytes = kSbNib + kSbScale + kSbZero;  // 8512
 constexpr int kStatusBytes = 16;
+// Workspace layout shared by every split kernel of the linear: the status
+// block, then ticket counters for up to kTicketTiles tiles x 8 warps at a fixed
+// offset (a workspace reused across shapes always finds them zero: each last
+// arriver resets its counter), then scratch from kScratchOff.
+constexpr int kTicketTiles = 8192;
+constexpr int kTicketWarps = 8;
+constexpr size_t kTicketOff = kStatusBytes;
+constexpr size_t kScratchOff = (kTicketOff + static_cast<size_t>(kTicketTiles) * kTicketWarps * 4 + 255) / 256 * 256;
 
 // Upper bound for any device-side wait (ns).  A wait that runs out records
 // FL_ERR_TIMEOUT in the status block and the kernel winds down.
@@ -117,6 +125,11 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
 // GPU-scope acquire/release fence (lighter than the sequentially consistent
 // fence behind __threadfence) for ticket hand-offs between CTAs.
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // Programmatic dependent launch: let the next kernel in the stream start its
 // CTAs now / wait until the previous kernel has completed and its memory

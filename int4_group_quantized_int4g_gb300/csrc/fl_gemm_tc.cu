@@ -4,17 +4,25 @@
 // int4g linear (FastLLM page, section 3.1: 4-bit codes dequantized inside the
 // matmul; fastllm README section 2: --dtype int4g applies to every linear).
 //
-// One CTA computes a 128 (weight rows n) x BN (tokens m) tile of y^T with
-// tcgen05.mma kind::f16 (bf16 in, fp32 accumulate in tensor memory):
-//   warp 0        producer: per group of 128 along K, the tile's token block
-//                 of x by TMA (two 64-column boxes, 128-byte swizzle) and the
-//                 weight super-block (8512 B) by a 1-D bulk copy;
-//   warp 1        allocates tensor memory; lane 0 issues the 8 MMAs of a group
-//                 (K = 16 each) and commits them to mbarriers;
-//   warps 4..11   dequantize the super-block into the A operand in shared
-//                 memory (K-major, 128-byte swizzle): each weight becomes the
-//                 correctly rounded bf16 of s16 * (q - z);
-//   warps 4..7    epilogue: tcgen05.ld of the accumulator, bf16 store of y.
+// Work unit = (tile, group): a tile is 128 weight rows n x BN tokens m of y^T,
+// a group the 128 k of one super-block.  The grid is persistent (one CTA per
+// SM); CTA c owns the contiguous units [c*U/P, (c+1)*U/P) in tile-major order
+// (stream-K), so every SM gets the same number of MMAs whatever the tile count.
+// A tile whose groups are spread over several CTAs is finished by the last of
+// them to take its ticket, the fp32 partials summed in CTA order
+// (deterministic).  Roles inside a CTA (tcgen05.mma kind::f16, bf16 in, fp32
+// accumulate in tensor memory):
+//   warp 0        x producer: per group, two TMA boxes of BN tokens x 64 k
+//                 (128-byte swizzle) into a ring of half-group stages
+//   warp 2        weight producer: the super-block (8512 B) by a 1-D bulk copy
+//                 into its own ring, so the dequantization runs ahead of x
+//   warp 1        allocates tensor memory; lane 0 issues 8 MMAs per group
+//                 (K = 16 each) with A read from tensor memory
+//   warps 4..11   dequantize the super-block into an A ring in tensor memory:
+//                 each weight becomes the correctly rounded bf16 of s16*(q-z)
+//   warps 12..19  epilogue: tcgen05.ld of the accumulator, bf16 store of y (or
+//                 an fp32 partial and a ticket), then hand the accumulator
+//                 back so the next tile's MMAs overlap the stores.
 // The dequantized value bf16(s16*(q-z)) is computed exactly: s16 = s_hi +
 // s_lo with s_hi = bf16(s16) and s_lo exact in bf16 (<= 3 bits), t =
 // s_lo*(q-z) is exact, and fma(s_hi, q-z, t) rounds once.
@@ -28,26 +36,32 @@ using namespace fl;
 
 namespace {
 
-constexpr int kTcThreads = 12 * 32;
-constexpr int kDeqWarp0 = 4;            // warps 4..11 dequantize; 4..7 also run the epilogue
-constexpr int kABytes = 128 * 128 * 2;  // A tile of one group: 128 rows x 128 k bf16 (two 16 KB halves)
+constexpr int kPfThreads = 20 * 32;
+constexpr int kPfDeq0 = 4;    // warps 4..11 dequantize
+constexpr int kPfEpi0 = 12;   // warps 12..19 epilogue
 
 template <int BN>
-struct TcCfg {
-  static constexpr int kBBytes = BN * 128 * 2;          // B tile of one group: BN rows x 128 k bf16
-  static constexpr int kStageBytes = kBBytes + kSbBytes;
-  static constexpr int kStageStride = (kStageBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = BN == 256 ? 3 : 5;
-  static constexpr int kSmem = kStages * kStageStride + 1024 /*align slack*/ + 256 /*barriers*/;
-  static constexpr int kARing = 2;                      // dequantized A tiles in tensor memory (64 columns each)
-  static constexpr uint32_t kTmemCols = BN == 256 ? 512 : 256;   // accumulator (BN) + A ring (128)
+struct PfCfg {
+  static constexpr int kBBox = BN * 64 * 2;                  // one x box: BN tokens x 64 k bf16
+  static constexpr int kBStages = BN == 256 ? 5 : 8;         // half-group x stages
+  static constexpr int kSStages = BN == 256 ? 7 : 8;         // super-block stages
+  static constexpr int kARing = 4;                           // dequantized A tiles (64 TMEM columns each)
+  static constexpr int kSOff = kBStages * kBBox;             // 1 KB aligned
+  static constexpr int kBarOff = kSOff + kSStages * kSbBytes;
+  static constexpr int kNumBars = 2 * kBStages + 2 * kSStages + 2 * kARing + 2;
+  static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024 /*align slack*/;
+  static constexpr uint32_t kTmemCols = 512;                 // accumulator [0, BN), A ring [BN, BN + 256)
+  static_assert(BN + 64 * kARing <= 512, "tensor memory");
+  static_assert(kSmem <= 232448, "shared memory");
 };
 
-struct TcParams {
-  const uint8_t* w;
-  __nv_bfloat16* y;
+struct PfParams {
+  const uint8_t* w;    // interleaved weights, first row tile of this launch
+  __nv_bfloat16* y;    // y + n0 (first row of this launch)
+  float* part;         // 2P partial slots of 128 x BN floats, [column][row]
+  int32_t* cnt;        // ticket counters [tile][8]
   int32_t* status;
-  int M, N, K, G, mtiles;
+  int M, N, ldy, G, mtiles, U, P;
 };
 
 // ------------------------------------------------------------ tcgen05 helpers
@@ -64,15 +78,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -92,6 +97,56 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Issue a load of 16 consecutive fp32 columns (no wait).
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+// Wait for this thread's outstanding tensor-memory loads; the registers of
+// `r` are tied to the wait so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+// Read NC chunks of 16 columns starting at taddr, keeping the next chunk's
+// load in flight while the current one is consumed; `release` runs as soon as
+// the last load has completed (the accumulator may then be overwritten).
+template <int NC, typename Rel, typename Use>
+__device__ __forceinline__ void pf_drain(uint32_t taddr, Rel&& release, Use&& use) {
+  static_assert(NC % 2 == 0, "chunks come in pairs");
+  uint32_t ra[16], rb[16];
+  tmem_ld16_issue(taddr, ra);
+  tmem_ld_wait(ra);
+#pragma unroll
+  for (int k = 0; k < NC; k += 2) {
+    tmem_ld16_issue(taddr + 16 * (k + 1), rb);
+    {
+      float v[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(ra[t]);
+      use(k, v);
+    }
+    tmem_ld_wait(rb);
+    if (k + 2 < NC)
+      tmem_ld16_issue(taddr + 16 * (k + 2), ra);
+    else
+      release();
+    {
+      float v[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(rb[t]);
+      use(k + 1, v);
+    }
+    if (k + 2 < NC) tmem_ld_wait(ra);
+  }
 }
 
 // 32 consecutive 32-bit columns of the calling warp's 32 TMEM lanes.
@@ -147,6 +202,15 @@ __device__ __forceinline__ uint32_t idesc_bf16() {
          (static_cast<uint32_t>(128 >> 4) << 24);
 }
 
+// CTA c of P owns units [unit_begin(c), unit_begin(c + 1)) of U; cta_of_unit
+// inverts it.
+__host__ __device__ __forceinline__ int td_unit_begin(int c, int U, int P) {
+  return static_cast<int>(static_cast<long long>(c) * U / P);
+}
+__host__ __device__ __forceinline__ int td_cta_of_unit(int u, int U, int P) {
+  return static_cast<int>((static_cast<long long>(u + 1) * P - 1) / U);
+}
+
 // bf16x2 helpers with a single rounding
 __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
   __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
@@ -158,35 +222,71 @@ __device__ __forceinline__ uint32_t bfma2(uint32_t a, uint32_t b, uint32_t c) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// 16 columns (tokens m0..m0+15) of one accumulator row n per lane -> bf16 y.
+// With an even row stride, lanes 2i and 2i+1 (rows n, n+1) swap halves so
+// that each lane writes one aligned pair of adjacent rows.
+__device__ __forceinline__ void pf_store_cols(const PfParams& p, int n, int m0, const float (&v)[16], int lane) {
+  if ((p.ldy & 1) == 0) {
+    const bool odd = lane & 1;
+    const int ne = n & ~1;
+#pragma unroll
+    for (int t = 0; t < 16; t += 2) {
+      const float send = odd ? v[t] : v[t + 1];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+      const int m = m0 + t + (odd ? 1 : 0);
+      const float lo = odd ? recv : v[t];
+      const float hi = odd ? v[t + 1] : recv;
+      if (m < p.M && ne < p.N) {
+        __nv_bfloat16* dst = p.y + static_cast<size_t>(m) * p.ldy + ne;
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+        if (ne + 1 < p.N)
+          *reinterpret_cast<__nv_bfloat162*>(dst) = pr;
+        else
+          *dst = pr.x;
+      }
+    }
+  } else if (n < p.N) {
+#pragma unroll
+    for (int t = 0; t < 16; ++t)
+      if (m0 + t < p.M) p.y[static_cast<size_t>(m0 + t) * p.ldy + n] = __float2bfloat16_rn(v[t]);
+  }
+}
+
 template <int BN>
-__global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
-  using C = TcCfg<BN>;
-  constexpr int RA = C::kARing;
+__global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const PfParams p) {
+  using C = PfCfg<BN>;
+  constexpr int RA = C::kARing, NBS = C::kBStages, NSS = C::kSStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* bars = smem + C::kStages * C::kStageStride;
-  uint64_t* full = reinterpret_cast<uint64_t*>(bars);          // B + super-block landed
-  uint64_t* empty = full + C::kStages;                         // MMAs of the stage done
-  uint64_t* afull = empty + C::kStages;                        // A slot dequantized (tensor memory)
-  uint64_t* aempty = afull + RA;                               // MMAs reading the A slot done
-  uint64_t* dfull = aempty + RA;                               // accumulator final
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dfull + 1);
+  uint64_t* bfull = reinterpret_cast<uint64_t*>(smem + C::kBarOff);   // x stage landed
+  uint64_t* bempty = bfull + NBS;                                     // MMAs reading the x stage done
+  uint64_t* sfull = bempty + NBS;                                     // super-block landed
+  uint64_t* sempty = sfull + NSS;                                     // super-block read by the 8 dequant warps
+  uint64_t* afull = sempty + NSS;                                     // A slot written (8 dequant warps)
+  uint64_t* aempty = afull + RA;                                      // MMAs reading the A slot done
+  uint64_t* dfull = aempty + RA;                                      // accumulator of a tile final
+  uint64_t* dempty = dfull + 1;                                       // accumulator read out (8 epilogue warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = blockIdx.x / p.mtiles, mt = blockIdx.x % p.mtiles;
-  auto stage_b = [&](int s) { return smem + s * C::kStageStride; };
-  auto stage_sb = [&](int s) { return smem + s * C::kStageStride + C::kBBytes; };
+  const int c = blockIdx.x;
+  const int u0 = td_unit_begin(c, p.U, p.P), nu = td_unit_begin(c + 1, p.U, p.P) - u0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int i = 0; i < NBS; ++i) {
+      mbar_init(&bfull[i], 1);
+      mbar_init(&bempty[i], 1);
     }
-    for (int a = 0; a < RA; ++a) {
-      mbar_init(&afull[a], 8);
-      mbar_init(&aempty[a], 1);
+    for (int i = 0; i < NSS; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sempty[i], 8);
+    }
+    for (int i = 0; i < RA; ++i) {
+      mbar_init(&afull[i], 8);
+      mbar_init(&aempty[i], 1);
     }
     mbar_init(dfull, 1);
+    mbar_init(dempty, 8);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -201,84 +301,114 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   pdl_launch_dependents();
 
   if (warp == 0) {
-    // ---------------- producer
+    // ---------------- x producer
+    if (lane == 0) {
+      pdl_wait();
+      int j = 0;
+      bool ok = true;
+      for (int i = 0; i < nu && ok; ++i) {
+        const int u = u0 + i, T = u / p.G, g = u - T * p.G, mt = T % p.mtiles;
+        for (int h = 0; h < 2; ++h, ++j) {
+          const int b = j % NBS;
+          if (j >= NBS && !mbar_wait(&bempty[b], static_cast<uint32_t>(j / NBS - 1) & 1u)) {
+            set_status(p.status, FL_ERR_TIMEOUT, 31);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bfull[b], C::kBBox);
+          tma_load_2d(smem + b * C::kBBox, &xmap, g * kGroup + 64 * h, mt * BN, &bfull[b]);
+        }
+      }
+      if (!ok)   // let the copies in flight land before the CTA can exit
+        for (int jj = j > NBS ? j - NBS : 0; jj < j; ++jj) mbar_wait(&bfull[jj % NBS], static_cast<uint32_t>(jj / NBS) & 1u);
+    }
+  } else if (warp == 2) {
+    // ---------------- weight producer
     if (lane == 0) {
       pdl_wait();
       const uint64_t pol = policy_evict_first();
-      int s = 0;
-      uint32_t ph = 0;
-      for (int g = 0; g < p.G; ++g) {
-        if (g >= C::kStages && !mbar_wait(&empty[s], ph ^ 1u)) {
-          set_status(p.status, FL_ERR_TIMEOUT, 21);
-          for (int j = 0; j < C::kStages; ++j) {
-            const int nf = g / C::kStages + (j < g % C::kStages ? 1 : 0);
-            if (nf > 0) mbar_wait(&full[j], static_cast<uint32_t>(nf - 1) & 1u);
-          }
-          break;
-        }
-        mbar_arrive_expect_tx(&full[s], C::kBBytes + kSbBytes);
-        tma_load_2d(stage_b(s), &xmap, g * kGroup, mt * BN, &full[s]);
-        tma_load_2d(stage_b(s) + BN * 128, &xmap, g * kGroup + 64, mt * BN, &full[s]);
-        bulk_g2s_hint(stage_sb(s), p.w + (static_cast<size_t>(nt) * p.G + g) * kSbBytes, kSbBytes, &full[s], pol);
-        if (++s == C::kStages) s = 0, ph ^= 1u;
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer: A from tensor memory, B from shared memory
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16<BN>();
-      int s = 0;
-      uint32_t ph = 0;
+      int i = 0;
       bool ok = true;
-      for (int g = 0; g < p.G; ++g) {
-        const int a = g % RA;
-        if (!mbar_wait(&full[s], ph) || !mbar_wait(&afull[a], (g / RA) & 1u)) {
-          set_status(p.status, FL_ERR_TIMEOUT, 22);
+      for (; i < nu; ++i) {
+        const int u = u0 + i, T = u / p.G, g = u - T * p.G, nt = T / p.mtiles;
+        const int sI = i % NSS;
+        if (i >= NSS && !mbar_wait(&sempty[sI], static_cast<uint32_t>(i / NSS - 1) & 1u)) {
+          set_status(p.status, FL_ERR_TIMEOUT, 32);
           ok = false;
           break;
         }
+        mbar_arrive_expect_tx(&sfull[sI], kSbBytes);
+        bulk_g2s_hint(smem + C::kSOff + sI * kSbBytes, p.w + (static_cast<size_t>(nt) * p.G + g) * kSbBytes, kSbBytes,
+                      &sfull[sI], pol);
+      }
+      if (!ok)
+        for (int ii = i > NSS ? i - NSS : 0; ii < i; ++ii) mbar_wait(&sfull[ii % NSS], static_cast<uint32_t>(ii / NSS) & 1u);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: A from tensor memory, B (x) from shared memory
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16<BN>();
+      int jt = 0, j = 0;
+      for (int i = 0; i < nu; ++i) {
+        const int u = u0 + i, g = u % p.G;
+        const bool first = i == 0 || g == 0, last = i == nu - 1 || g == p.G - 1;
+        const int a = i % RA;
+        if ((first && jt > 0 && !mbar_wait(dempty, static_cast<uint32_t>(jt - 1) & 1u)) ||
+            !mbar_wait(&afull[a], static_cast<uint32_t>(i / RA) & 1u)) {
+          set_status(p.status, FL_ERR_TIMEOUT, 33);
+          break;
+        }
         tc_fence_after();
-        const uint32_t b0 = smem_u32(stage_b(s));
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
+        bool ok = true;
+        for (int h = 0; h < 2; ++h, ++j) {
+          const int b = j % NBS;
+          if (!mbar_wait(&bfull[b], static_cast<uint32_t>(j / NBS) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b0 = smem_u32(smem + b * C::kBBox);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ta(tmem_d, tmem_a + a * 64 + h * 32 + kk * 8, sw128_desc(b0 + h * BN * 128 + kk * 32), idesc,
-                         (g | h | kk) != 0);
-        umma_commit(&empty[s]);
+            umma_bf16_ta(tmem_d, tmem_a + a * 64 + h * 32 + kk * 8, sw128_desc(b0 + kk * 32), idesc,
+                         (!first || h != 0 || kk != 0) ? 1u : 0u);
+          umma_commit(&bempty[b]);
+        }
+        if (!ok) {
+          set_status(p.status, FL_ERR_TIMEOUT, 34);
+          break;
+        }
         umma_commit(&aempty[a]);
-        if (++s == C::kStages) s = 0, ph ^= 1u;
+        if (last) {
+          umma_commit(dfull);
+          ++jt;
+        }
       }
-      if (ok) umma_commit(dfull);
     }
-  } else if (warp >= kDeqWarp0) {
-    // ---------------- dequant: thread = (weight row r = TMEM lane, K half h);
-    // each weight becomes the correctly rounded bf16 of s16 * (q - z)
-    const int q = warp & 3, h = (warp - kDeqWarp0) >> 2;
+  } else if (warp >= kPfDeq0 && warp < kPfEpi0) {
+    // ---------------- dequant: thread = (weight row r = TMEM lane, K half h)
+    const int q = warp & 3, h = (warp - kPfDeq0) >> 2;
     const int r = q * 32 + lane;
     const uint32_t trow = static_cast<uint32_t>(q * 32) << 16;
-    int s = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    for (int g = 0; g < p.G; ++g) {
-      const int a = g % RA;
-      if (!mbar_wait(&full[s], ph) || (g >= RA && !mbar_wait(&aempty[a], ((g / RA) - 1) & 1u))) {
-        set_status(p.status, FL_ERR_TIMEOUT, 23);
-        ok = false;
+    for (int i = 0; i < nu; ++i) {
+      const int sI = i % NSS, a = i % RA;
+      if (!mbar_wait(&sfull[sI], static_cast<uint32_t>(i / NSS) & 1u)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 35);
         break;
       }
-      tc_fence_after();
-      const uint8_t* sb = stage_sb(s);
+      const uint8_t* sb = smem + C::kSOff + sI * kSbBytes;
       const float sf = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
+      const uint32_t z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
+      uint4 cv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) cv[t] = *reinterpret_cast<const uint4*>(sb + r * 64 + ((t + (r >> 1)) & 3) * 16);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[sI]);
       const __nv_bfloat16 shi = __float2bfloat16_rn(sf);
       const __nv_bfloat16 slo = __float2bfloat16_rn(sf - __bfloat162float(shi));   // exact remainder
       const uint32_t hi2 = static_cast<uint32_t>(__bfloat16_as_ushort(shi)) * 0x00010001u;
       const uint32_t lo2 = static_cast<uint32_t>(__bfloat16_as_ushort(slo)) * 0x00010001u;
-      const uint32_t z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
       const uint32_t zz = bf16_bias_pair(z);
-      uint4 cv[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) cv[t] = *reinterpret_cast<const uint4*>(sb + r * 64 + ((t + (r >> 1)) & 3) * 16);
       uint32_t o[32];
       auto unpack = [&](auto H) {
         constexpr int hh = decltype(H)::value;
@@ -297,33 +427,108 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
         unpack(std::integral_constant<int, 0>());
       else
         unpack(std::integral_constant<int, 1>());
+      if (i >= RA && !mbar_wait(&aempty[a], static_cast<uint32_t>(i / RA - 1) & 1u)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 36);
+        break;
+      }
+      tc_fence_after();
       tmem_st32(tmem_a + trow + a * 64 + h * 32, o);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[a]);
-      if (++s == C::kStages) s = 0, ph ^= 1u;
     }
-    if (warp < kDeqWarp0 + 4) {
-      // ---------------- epilogue: rows q*32+lane, tokens of the tile
-      if (ok && mbar_wait(dfull, 0)) {
-        tc_fence_after();
-        const int n = nt * kRowTile + r;
-#pragma unroll 1
-        for (int j = 0; j < BN; j += 32) {
-          float v[32];
-          tmem_ld32(tmem_d + trow + j, v);
-          if (n < p.N) {
+  } else if (warp >= kPfEpi0) {
+    // ---------------- epilogue: rows q*32+lane, one half of the tile's tokens
+    const int e = warp - kPfEpi0, q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t tcol = tmem_d + (static_cast<uint32_t>(q * 32) << 16) + (e >> 2) * (BN / 2);
+    const int col0 = (e >> 2) * (BN / 2);
+    auto release_d = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty);
+    };
+    int jt = 0;
+    for (int i = 0; i < nu; ++jt) {
+      const int u = u0 + i, T = u / p.G, g = u - T * p.G;
+      const int len = min(p.G - g, nu - i);
+      const bool whole = g == 0 && len == p.G, first_of_cta = i == 0;
+      i += len;
+      const bool last_of_cta = i == nu;
+      if (!mbar_wait(dfull, static_cast<uint32_t>(jt) & 1u)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 37);
+        break;
+      }
+      tc_fence_after();
+      const int nt = T / p.mtiles, mt = T % p.mtiles;
+      const int n = nt * kRowTile + r, m0 = mt * BN + col0;
+      if (whole) {
+        pf_drain<BN / 32>(tcol, release_d, [&](int k, const float (&v)[16]) { pf_store_cols(p, n, m0 + 16 * k, v, lane); });
+        continue;
+      }
+      // partial tile: contributors cf..cl, summed in CTA order by the last one
+      const int cf = td_cta_of_unit(T * p.G, p.U, p.P), cl = td_cta_of_unit((T + 1) * p.G - 1, p.U, p.P);
+      int32_t* cnt = p.cnt + T * 8 + e;
+      auto slot_of = [&](int cc) {
+        return p.part + static_cast<size_t>(2 * cc + (td_unit_begin(cc, p.U, p.P) / p.G == T ? 0 : 1)) * kRowTile * BN;
+      };
+      int done = 0;
+      if (last_of_cta) {   // the accumulator is not needed afterwards: combine in place if all others are in
+        if (lane == 0) done = ld_acquire_gpu(cnt) == cl - cf;
+        done = __shfl_sync(0xffffffffu, done, 0);
+        __syncwarp();   // orders every lane's reads after lane 0's acquire
+      }
+      if (done) {
+        pf_drain<BN / 32>(tcol, release_d, [&](int k, const float (&v)[16]) {
+          float acc[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int m = mt * BN + j + i;
-              if (m < p.M) p.y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(v[i]);
+          for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+          for (int cc = cf; cc <= cl; ++cc) {   // CTA order: deterministic
+            if (cc == c) {
+#pragma unroll
+              for (int t = 0; t < 16; ++t) acc[t] += v[t];
+            } else {
+              const float* src = slot_of(cc) + static_cast<size_t>(col0 + 16 * k) * kRowTile + r;
+#pragma unroll
+              for (int t = 0; t < 16; ++t) acc[t] += __ldcg(src + t * kRowTile);
             }
           }
-        }
-      } else if (ok) {
-        set_status(p.status, FL_ERR_TIMEOUT, 24);
+          pf_store_cols(p, n, m0 + 16 * k, acc, lane);
+        });
+        __syncwarp();
+        if (lane == 0) *cnt = 0;
+        continue;
       }
+      float* slot = p.part + static_cast<size_t>(2 * c + (first_of_cta ? 0 : 1)) * kRowTile * BN;
+      pf_drain<BN / 32>(tcol, release_d, [&](int k, const float (&v)[16]) {
+        float* dst = slot + static_cast<size_t>(col0 + 16 * k) * kRowTile + r;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) __stcg(dst + t * kRowTile, v[t]);
+      });
+      int lastw = 0;
+      if (lane == 0) {
+        fence_acq_rel_gpu();
+        lastw = atomicAdd(cnt, 1) == cl - cf;
+        if (lastw) fence_acq_rel_gpu();
+      }
+      lastw = __shfl_sync(0xffffffffu, lastw, 0);
+      if (!lastw) continue;
+      __syncwarp();
+#pragma unroll 1
+      for (int k = 0; k < BN / 32; ++k) {
+        float acc[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+        for (int cc = cf; cc <= cl; ++cc) {   // CTA order: deterministic
+          const float* src = slot_of(cc) + static_cast<size_t>(col0 + 16 * k) * kRowTile + r;
+#pragma unroll
+          for (int t = 0; t < 16; ++t) acc[t] += __ldcg(src + t * kRowTile);
+        }
+        pf_store_cols(p, n, m0 + 16 * k, acc, lane);
+      }
+      __syncwarp();
+      if (lane == 0) *cnt = 0;
     }
   }
   tc_fence_before();
@@ -348,9 +553,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Prefill workspace: status block, ticket counters at kTicketOff, 2P
+// partial slots of 128 x BN floats at kScratchOff.
+int pf_bn(int M) { return M > 128 ? 256 : 128; }
+
+size_t pf_workspace(int M) {
+  const size_t P = static_cast<size_t>(flh::sm_count());
+  return kScratchOff + 2 * P * kRowTile * pf_bn(M) * 4;
+}
+
 template <int BN>
-int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_t* status, cudaStream_t s) {
-  using C = TcCfg<BN>;
+int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, void* ws, cudaStream_t s) {
+  using C = PfCfg<BN>;
   auto enc = encode_fn();
   if (!enc) return FL_ERR_CUDA;
   CUtensorMap map;
@@ -362,16 +576,6 @@ int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return FL_ERR_CUDA;
-  TcParams p;
-  p.w = static_cast<const uint8_t*>(w);
-  p.y = static_cast<__nv_bfloat16*>(y);
-  p.status = status;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.G = K / kGroup;
-  p.mtiles = (M + BN - 1) / BN;
-  const int ntiles = (N + kRowTile - 1) / kRowTile;
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -380,17 +584,42 @@ int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_
       return FL_ERR_CUDA;
     attr_done[dev] = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ntiles * p.mtiles));
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, k_gemm_tc<BN>, map, p) != cudaSuccess) return FL_ERR_CUDA;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const int G = K / kGroup, mtiles = (M + BN - 1) / BN, ntiles = (N + kRowTile - 1) / kRowTile;
+  const int sms = flh::sm_count();
+  // the ticket counters cover kTicketTiles tiles: larger problems run as
+  // several launches over row-tile ranges, serialized on the stream
+  const int nt_chunk = kTicketTiles / mtiles;
+  if (nt_chunk < 1) return FL_ERR_UNSUPPORTED;
+  for (int nt0 = 0; nt0 < ntiles; nt0 += nt_chunk) {
+    const int nts = ntiles - nt0 < nt_chunk ? ntiles - nt0 : nt_chunk;
+    PfParams p;
+    p.w = static_cast<const uint8_t*>(w) + static_cast<size_t>(nt0) * G * kSbBytes;
+    p.y = static_cast<__nv_bfloat16*>(y) + static_cast<size_t>(nt0) * kRowTile;
+    p.part = reinterpret_cast<float*>(wsb + kScratchOff);
+    p.cnt = reinterpret_cast<int32_t*>(wsb + kTicketOff);
+    p.status = reinterpret_cast<int32_t*>(wsb);
+    p.M = M;
+    p.N = N - nt0 * kRowTile < nts * kRowTile ? N - nt0 * kRowTile : nts * kRowTile;
+    p.ldy = N;
+    p.G = G;
+    p.mtiles = mtiles;
+    const long long U = static_cast<long long>(nts) * mtiles * G;
+    if (U > 0x7fffffffLL / (sms + 1)) return FL_ERR_UNSUPPORTED;
+    p.U = static_cast<int>(U);
+    p.P = p.U < sms ? p.U : sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.P));
+    cfg.blockDim = dim3(kPfThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = nt0 == 0 ? 1 : 0;   // chunks after the first reuse the counters: no overlap
+    if (cudaLaunchKernelEx(&cfg, k_gemm_tc<BN>, map, p) != cudaSuccess) return FL_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
@@ -431,12 +660,6 @@ struct TdCfg {
 constexpr int kTdThreads = 16 * 32;
 constexpr int kTdDeq0 = 4, kTdEpi0 = 12;
 
-__host__ __device__ __forceinline__ int td_unit_begin(int c, int U, int P) {
-  return static_cast<int>(static_cast<long long>(c) * U / P);
-}
-__host__ __device__ __forceinline__ int td_cta_of_unit(int u, int U, int P) {
-  return static_cast<int>((static_cast<long long>(u + 1) * P - 1) / U);
-}
 
 // Final sums of row tile T for this epilogue thread's row: write them or hand
 // them off (returns true when a ticket is owed).
@@ -767,10 +990,12 @@ int launch_tcdec(const void* x, int M, int K, const void* w, int N, void* y, voi
 
 }  // namespace
 
-// Prefill path of fl_int4g_linear (M >= 64): one tcgen05 kernel launch.
-int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_t* status, cudaStream_t s) {
-  if (M >= 1024) return launch_tc<256>(x, M, K, w, N, y, status, s);
-  return launch_tc<128>(x, M, K, w, N, y, status, s);
+// Prefill path of fl_int4g_linear (M > 32): persistent stream-K tcgen05 GEMM.
+size_t fl_linear_tc_workspace(int M) { return pf_workspace(M); }
+
+int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, void* ws, cudaStream_t s) {
+  if (pf_bn(M) == 256) return launch_tc<256>(x, M, K, w, N, y, ws, s);
+  return launch_tc<128>(x, M, K, w, N, y, ws, s);
 }
 
 // Decode path of fl_int4g_linear on tcgen05 (M <= 32); the workspace layout is

@@ -32,6 +32,8 @@ constexpr int kMaxTokens = 32;
 // so that a workspace reused across shapes never finds another shape's
 // scratch partial sums where its counters are (they must be zero on entry).
 constexpr int kMaxRowTiles = 8192;  // N <= 1,048,576
+static_assert(kMaxRowTiles == kTicketTiles && kConsumerWarps == kTicketWarps,
+              "the decode counters are the shared ticket region");
 
 struct RowsParams {
   const uint8_t* w;
@@ -348,8 +350,8 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl) {
   const int nslot = units_max < pl->G ? units_max : pl->G;
   pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes + 2 * pl->stages * sizeof(uint64_t) +
              static_cast<size_t>(nslot) * 8 * pl->NT * sizeof(float);
-  pl->cnt_off = kStatusBytes;
-  pl->part_off = align_up(pl->cnt_off + static_cast<size_t>(kMaxRowTiles) * kConsumerWarps * 4, 256);
+  pl->cnt_off = kTicketOff;
+  pl->part_off = kScratchOff;
   pl->ws_bytes = pl->part_off + static_cast<size_t>(pl->P + pl->T) * kRowTile * (8 * pl->NT) * 4;
   return true;
 }
@@ -424,7 +426,8 @@ static bool linear_args_ok(const void* x, int M, int K, const void* w, int N, co
   return flh::aligned16(x) && flh::aligned16(w) && flh::aligned16(y) && flh::aligned16(ws);
 }
 
-int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, int32_t* status, cudaStream_t s);
+size_t fl_linear_tc_workspace(int M);
+int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, void* ws, cudaStream_t s);
 int fl_linear_tcdec(const void* x, int M, int K, const void* w, int N, void* y, void* ws, size_t cnt_off,
                     size_t part_off, cudaStream_t s);
 
@@ -447,7 +450,7 @@ static bool tcdec_plan(int M, int N, int K, size_t* cnt_off, size_t* part_off, s
 extern "C" int fl_int4g_linear_workspace(int M, int N, int K, size_t* out) {
   if (!out || M < 1 || N < 1 || K < kGroup || K % kGroup) return FL_ERR_ARG;
   if (M > kMaxTokens) {
-    *out = kStatusBytes;   // the prefill kernel needs only the status block
+    *out = fl_linear_tc_workspace(M);
     return FL_OK;
   }
   size_t a, b;
@@ -459,8 +462,8 @@ extern "C" int fl_int4g_linear(const void* x, int M, int K, const void* w, int N
   if (!linear_args_ok(x, M, K, w, N, y, ws)) return FL_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (M > kMaxTokens) {
-    if (ws_bytes < kStatusBytes) return FL_ERR_WORKSPACE;
-    return fl_linear_tc(x, M, K, w, N, y, static_cast<int32_t*>(ws), s);
+    if (ws_bytes < fl_linear_tc_workspace(M)) return FL_ERR_WORKSPACE;
+    return fl_linear_tc(x, M, K, w, N, y, ws, s);
   }
   size_t cnt_off, part_off, need;
   if (!tcdec_plan(M, N, K, &cnt_off, &part_off, &need)) return FL_ERR_ARG;
