@@ -44,9 +44,11 @@ template <int BN>
 struct PfCfg {
   static constexpr int kBBox = BN * 64 * 2;                  // one x box: BN tokens x 64 k bf16
   static constexpr int kBStages = BN == 256 ? 5 : 8;         // half-group x stages
-  static constexpr int kSStages = BN == 256 ? 7 : 8;         // super-block stages
+  static constexpr int kSStages = BN == 256 ? 4 : 8;         // super-block stages
   static constexpr int kARing = 4;                           // dequantized A tiles (64 TMEM columns each)
-  static constexpr int kSOff = kBStages * kBBox;             // 1 KB aligned
+  static constexpr int kStgBytes = BN / 2 * kRowTile * 2;    // y staging: BN/2 tokens x 128 rows bf16
+  static constexpr int kStgOff = kBStages * kBBox;           // 1 KB aligned
+  static constexpr int kSOff = kStgOff + kStgBytes;
   static constexpr int kBarOff = kSOff + kSStages * kSbBytes;
   static constexpr int kNumBars = 2 * kBStages + 2 * kSStages + 2 * kARing + 2;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024 /*align slack*/;
@@ -62,6 +64,7 @@ struct PfParams {
   int32_t* cnt;        // ticket counters [tile][8]
   int32_t* status;
   int M, N, ldy, G, mtiles, U, P;
+  int tma_y;           // y written by TMA stores through a staging tile (row stride a multiple of 16 B)
 };
 
 // ------------------------------------------------------------ tcgen05 helpers
@@ -183,6 +186,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// TMA 2-D tile store shared -> global (bulk group); rows/columns outside the
+// tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(c0),
+               "r"(c1), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 B apart (SBO), descriptor version 1.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -252,8 +266,35 @@ __device__ __forceinline__ void pf_store_cols(const PfParams& p, int n, int m0, 
   }
 }
 
+// Order in which a CTA takes its units [u0, u1): first the units of its two
+// split tiles (the head tile it shares with CTA c-1, the tail tile it shares
+// with CTA c+1), then its whole tiles.  Both sharers of a tile then reach it
+// early, so its ticketed reduction overlaps the MMAs of the whole tiles
+// instead of trailing the kernel.  Three contiguous segments of units.
+struct PfSeq {
+  int ha, hb, ta, tb;   // head [ha, hb), tail [ta, tb), whole tiles [hb, ta)
+  __device__ static PfSeq make(int u0, int u1, int G) {
+    PfSeq q;
+    q.ha = u0;
+    q.hb = u0 % G ? min(u1, (u0 / G + 1) * G) : u0;
+    q.tb = u1;
+    q.ta = u1 % G ? max(u1 / G * G, q.hb) : u1;
+    return q;
+  }
+  __device__ int nh() const { return hb - ha; }
+  __device__ int nt() const { return tb - ta; }
+  __device__ int at(int i) const {
+    if (i < nh()) return ha + i;
+    if (i < nh() + nt()) return ta + (i - nh());
+    return hb + (i - nh() - nt());
+  }
+  __device__ int seg_begin(int i) const { return i < nh() ? 0 : i < nh() + nt() ? nh() : nh() + nt(); }
+  __device__ int seg_end(int i, int n) const { return i < nh() ? nh() : i < nh() + nt() ? nh() + nt() : n; }
+};
+
 template <int BN>
-__global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const PfParams p) {
+__global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
+                                                    const PfParams p) {
   using C = PfCfg<BN>;
   constexpr int RA = C::kARing, NBS = C::kBStages, NSS = C::kSStages;
   extern __shared__ uint8_t smem_raw[];
@@ -267,10 +308,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
   uint64_t* dfull = aempty + RA;                                      // accumulator of a tile final
   uint64_t* dempty = dfull + 1;                                       // accumulator read out (8 epilogue warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + 1);
+  int* epi_abort = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   const int u0 = td_unit_begin(c, p.U, p.P), nu = td_unit_begin(c + 1, p.U, p.P) - u0;
+  const PfSeq sq = PfSeq::make(u0, u0 + nu, p.G);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBS; ++i) {
@@ -287,6 +330,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
     }
     mbar_init(dfull, 1);
     mbar_init(dempty, 8);
+    *epi_abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -307,7 +351,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
       int j = 0;
       bool ok = true;
       for (int i = 0; i < nu && ok; ++i) {
-        const int u = u0 + i, T = u / p.G, g = u - T * p.G, mt = T % p.mtiles;
+        const int u = sq.at(i), T = u / p.G, g = u - T * p.G, mt = T % p.mtiles;
         for (int h = 0; h < 2; ++h, ++j) {
           const int b = j % NBS;
           if (j >= NBS && !mbar_wait(&bempty[b], static_cast<uint32_t>(j / NBS - 1) & 1u)) {
@@ -330,7 +374,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
       int i = 0;
       bool ok = true;
       for (; i < nu; ++i) {
-        const int u = u0 + i, T = u / p.G, g = u - T * p.G, nt = T / p.mtiles;
+        const int u = sq.at(i), T = u / p.G, g = u - T * p.G, nt = T / p.mtiles;
         const int sI = i % NSS;
         if (i >= NSS && !mbar_wait(&sempty[sI], static_cast<uint32_t>(i / NSS - 1) & 1u)) {
           set_status(p.status, FL_ERR_TIMEOUT, 32);
@@ -345,43 +389,49 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
         for (int ii = i > NSS ? i - NSS : 0; ii < i; ++ii) mbar_wait(&sfull[ii % NSS], static_cast<uint32_t>(ii / NSS) & 1u);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: A from tensor memory, B (x) from shared memory
+    // ---------------- MMA issuer: A from tensor memory, B (x) from shared memory.
+    // The tensor pipe queues only a few MMAs, so the per-unit bookkeeping is
+    // kept to counters (no divisions) to stay inside that slack.
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16<BN>();
-      int jt = 0, j = 0;
-      for (int i = 0; i < nu; ++i) {
-        const int u = u0 + i, g = u % p.G;
-        const bool first = i == 0 || g == 0, last = i == nu - 1 || g == p.G - 1;
-        const int a = i % RA;
-        if ((first && jt > 0 && !mbar_wait(dempty, static_cast<uint32_t>(jt - 1) & 1u)) ||
-            !mbar_wait(&afull[a], static_cast<uint32_t>(i / RA) & 1u)) {
-          set_status(p.status, FL_ERR_TIMEOUT, 33);
-          break;
-        }
-        tc_fence_after();
-        bool ok = true;
-        for (int h = 0; h < 2; ++h, ++j) {
-          const int b = j % NBS;
-          if (!mbar_wait(&bfull[b], static_cast<uint32_t>(j / NBS) & 1u)) {
+      int jt = 0, a = 0, b = 0;
+      uint32_t aph = 0, bph = 0;
+      bool ok = true;
+      for (int seg = 0; seg < 3 && ok; ++seg) {
+        const int ub = seg == 0 ? sq.ha : seg == 1 ? sq.ta : sq.hb;
+        const int ue = seg == 0 ? sq.hb : seg == 1 ? sq.tb : sq.ta;
+        int g = ub % p.G;
+        for (int u = ub; u < ue; ++u) {
+          const bool first = g == 0 || u == ub, last = g == p.G - 1 || u == ue - 1;
+          if ((first && jt > 0 && !mbar_wait(dempty, static_cast<uint32_t>(jt - 1) & 1u)) || !mbar_wait(&afull[a], aph)) {
+            set_status(p.status, FL_ERR_TIMEOUT, 33);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t b0 = smem_u32(smem + b * C::kBBox);
+          for (int h = 0; h < 2; ++h) {
+            if (!mbar_wait(&bfull[b], bph)) {
+              set_status(p.status, FL_ERR_TIMEOUT, 34);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t b0 = smem_u32(smem + b * C::kBBox);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ta(tmem_d, tmem_a + a * 64 + h * 32 + kk * 8, sw128_desc(b0 + kk * 32), idesc,
-                         (!first || h != 0 || kk != 0) ? 1u : 0u);
-          umma_commit(&bempty[b]);
-        }
-        if (!ok) {
-          set_status(p.status, FL_ERR_TIMEOUT, 34);
-          break;
-        }
-        umma_commit(&aempty[a]);
-        if (last) {
-          umma_commit(dfull);
-          ++jt;
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_ta(tmem_d, tmem_a + a * 64 + h * 32 + kk * 8, sw128_desc(b0 + kk * 32), idesc,
+                           (!first || h != 0 || kk != 0) ? 1u : 0u);
+            umma_commit(&bempty[b]);
+            if (++b == NBS) b = 0, bph ^= 1u;
+          }
+          if (!ok) break;
+          umma_commit(&aempty[a]);
+          if (++a == RA) a = 0, aph ^= 1u;
+          if (last) {
+            umma_commit(dfull);
+            ++jt;
+          }
+          if (++g == p.G) g = 0;
         }
       }
     }
@@ -451,18 +501,49 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
     };
     int jt = 0;
     for (int i = 0; i < nu; ++jt) {
-      const int u = u0 + i, T = u / p.G, g = u - T * p.G;
-      const int len = min(p.G - g, nu - i);
-      const bool whole = g == 0 && len == p.G, first_of_cta = i == 0;
+      const int u = sq.at(i), T = u / p.G, g = u - T * p.G;
+      const int len = min(p.G - g, sq.seg_end(i, nu) - i);
+      const bool whole = g == 0 && len == p.G, head = T == u0 / p.G;
       i += len;
       const bool last_of_cta = i == nu;
-      if (!mbar_wait(dfull, static_cast<uint32_t>(jt) & 1u)) {
+      // all epilogue warps take the same exit decision (they share named barriers)
+      if (!mbar_wait(dfull, static_cast<uint32_t>(jt) & 1u)) *epi_abort = 1;
+      named_bar(1, 256);
+      if (*reinterpret_cast<volatile int*>(epi_abort)) {
         set_status(p.status, FL_ERR_TIMEOUT, 37);
         break;
       }
       tc_fence_after();
       const int nt = T / p.mtiles, mt = T % p.mtiles;
       const int n = nt * kRowTile + r, m0 = mt * BN + col0;
+      if (whole && p.tma_y) {
+        // two rounds of BN/2 tokens through the staging tile: TMEM -> bf16 in
+        // shared memory -> one TMA store of 128 rows x BN/2 tokens
+        __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem + C::kStgOff);
+#pragma unroll 1
+        for (int rho = 0; rho < 2; ++rho) {
+          const int lt0 = (e >> 2) * (BN / 4);
+          pf_drain<BN / 64>(
+              tmem_d + (static_cast<uint32_t>(q * 32) << 16) + rho * (BN / 2) + lt0,
+              [&]() {
+                if (rho == 1) release_d();
+              },
+              [&](int k, const float (&v)[16]) {
+                __nv_bfloat16* dst = stg + static_cast<size_t>(lt0 + 16 * k) * kRowTile + r;
+#pragma unroll
+                for (int t = 0; t < 16; ++t) dst[t * kRowTile] = __float2bfloat16_rn(v[t]);
+              });
+          fence_proxy_async();
+          named_bar(1, 256);
+          if (e == 0 && lane == 0) {
+            tma_store_2d(&ymap, stg, nt * kRowTile, mt * BN + rho * (BN / 2));
+            bulk_commit();
+            bulk_wait_read0();   // the staging tile has been read
+          }
+          named_bar(1, 256);
+        }
+        continue;
+      }
       if (whole) {
         pf_drain<BN / 32>(tcol, release_d, [&](int k, const float (&v)[16]) { pf_store_cols(p, n, m0 + 16 * k, v, lane); });
         continue;
@@ -500,7 +581,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
         if (lane == 0) *cnt = 0;
         continue;
       }
-      float* slot = p.part + static_cast<size_t>(2 * c + (first_of_cta ? 0 : 1)) * kRowTile * BN;
+      float* slot = p.part + static_cast<size_t>(2 * c + (head ? 0 : 1)) * kRowTile * BN;
       pf_drain<BN / 32>(tcol, release_d, [&](int k, const float (&v)[16]) {
         float* dst = slot + static_cast<size_t>(col0 + 16 * k) * kRowTile + r;
 #pragma unroll
@@ -530,6 +611,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
       __syncwarp();
       if (lane == 0) *cnt = 0;
     }
+    if (e == 0 && lane == 0) bulk_wait0();   // y stores complete before the CTA exits
   }
   tc_fence_before();
   __syncthreads();
@@ -584,6 +666,8 @@ int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, void* 
       return FL_ERR_CUDA;
     attr_done[dev] = true;
   }
+  // y through TMA stores when its row stride is a multiple of 16 bytes
+  const int tma_y = N % 8 == 0 ? 1 : 0;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   const int G = K / kGroup, mtiles = (M + BN - 1) / BN, ntiles = (N + kRowTile - 1) / kRowTile;
   const int sms = flh::sm_count();
@@ -608,6 +692,18 @@ int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, void* 
     if (U > 0x7fffffffLL / (sms + 1)) return FL_ERR_UNSUPPORTED;
     p.U = static_cast<int>(U);
     p.P = p.U < sms ? p.U : sms;
+    p.tma_y = tma_y;
+    CUtensorMap ymap;
+    memset(&ymap, 0, sizeof(ymap));
+    if (tma_y) {
+      const cuuint64_t ydims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(M)};
+      const cuuint64_t ystrides[1] = {static_cast<cuuint64_t>(N) * 2};
+      const cuuint32_t ybox[2] = {static_cast<cuuint32_t>(kRowTile), static_cast<cuuint32_t>(BN / 2)};
+      if (enc(&ymap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.y, ydims, ystrides, ybox, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return FL_ERR_CUDA;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.P));
     cfg.blockDim = dim3(kPfThreads);
@@ -618,7 +714,7 @@ int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, void* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = nt0 == 0 ? 1 : 0;   // chunks after the first reuse the counters: no overlap
-    if (cudaLaunchKernelEx(&cfg, k_gemm_tc<BN>, map, p) != cudaSuccess) return FL_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, k_gemm_tc<BN>, map, ymap, p) != cudaSuccess) return FL_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
