@@ -390,12 +390,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: A from tensor memory, B (x) from shared memory.
-    // The tensor pipe queues only a few MMAs, so the per-unit bookkeeping is
-    // kept to counters (no divisions) to stay inside that slack.
+    // The tensor pipe queues only a few MMAs, so the per-unit work of this
+    // thread is kept small: counters instead of divisions, and one barrier
+    // probe per unit (afull also certifies the unit's x stages: the dequant
+    // warps wait for them before arriving).
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16<BN>();
       int jt = 0, a = 0, b = 0;
-      uint32_t aph = 0, bph = 0;
+      uint32_t aph = 0;
       bool ok = true;
       for (int seg = 0; seg < 3 && ok; ++seg) {
         const int ub = seg == 0 ? sq.ha : seg == 1 ? sq.ta : sq.hb;
@@ -409,22 +411,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
             break;
           }
           tc_fence_after();
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
-            if (!mbar_wait(&bfull[b], bph)) {
-              set_status(p.status, FL_ERR_TIMEOUT, 34);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
             const uint32_t b0 = smem_u32(smem + b * C::kBBox);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16_ta(tmem_d, tmem_a + a * 64 + h * 32 + kk * 8, sw128_desc(b0 + kk * 32), idesc,
                            (!first || h != 0 || kk != 0) ? 1u : 0u);
             umma_commit(&bempty[b]);
-            if (++b == NBS) b = 0, bph ^= 1u;
+            if (++b == NBS) b = 0;
           }
-          if (!ok) break;
           umma_commit(&aempty[a]);
           if (++a == RA) a = 0, aph ^= 1u;
           if (last) {
@@ -484,6 +480,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
       tc_fence_after();
       tmem_st32(tmem_a + trow + a * 64 + h * 32, o);
       tmem_wait_st();
+      // the unit's two x stages must have landed before afull is signalled
+      if (!mbar_wait(&bfull[(2 * i) % NBS], static_cast<uint32_t>((2 * i) / NBS) & 1u) ||
+          !mbar_wait(&bfull[(2 * i + 1) % NBS], static_cast<uint32_t>((2 * i + 1) / NBS) & 1u)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 34);
+        break;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[a]);
