@@ -772,9 +772,10 @@ __device__ __forceinline__ bool td_store(const TdParams& p, int T, int c, int u0
     }
     return false;
   }
-  float* pp = p.part + (static_cast<size_t>(c + T) * kRowTile + r) * NB;
+  // slot layout [token m][row r]: a warp's 32 rows are one 128-byte line per token
+  float* pp = p.part + static_cast<size_t>(c + T) * kRowTile * NB + r;
 #pragma unroll
-  for (int m = 0; m < NB; m += 4) __stcg(reinterpret_cast<float4*>(pp + m), make_float4(tot[m], tot[m + 1], tot[m + 2], tot[m + 3]));
+  for (int m = 0; m < NB; ++m) __stcg(pp + m * kRowTile, tot[m]);
   return true;
 }
 
@@ -790,18 +791,19 @@ __device__ __forceinline__ void td_ticket(const TdParams& p, int T, int q, int l
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
+  __syncwarp();
   const int r = q * 32 + lane;
   const int n = T * kRowTile + r;
   float acc[NB];
 #pragma unroll
   for (int m = 0; m < NB; ++m) acc[m] = 0.f;
   for (int cc = cf; cc <= cl; ++cc) {   // CTA order: deterministic
-    const float* pp = p.part + (static_cast<size_t>(cc + T) * kRowTile + r) * NB;
+    const float* pp = p.part + static_cast<size_t>(cc + T) * kRowTile * NB + r;
+    float v[NB];
 #pragma unroll
-    for (int m = 0; m < NB; m += 4) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(pp + m));
-      acc[m] += v.x, acc[m + 1] += v.y, acc[m + 2] += v.z, acc[m + 3] += v.w;
-    }
+    for (int m = 0; m < NB; ++m) v[m] = __ldcg(pp + m * kRowTile);
+#pragma unroll
+    for (int m = 0; m < NB; ++m) acc[m] += v[m];
   }
   if (n < p.N) {
 #pragma unroll
@@ -903,11 +905,12 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16<NB>();
+      // one probe per super-block in the common case: a_full also certifies
+      // the x tile (the dequant warps wait for it before arriving)
+      int a = 0, b = 0;
+      uint32_t pa = 0, pd = 1;   // the D ring starts free (parity of the phase before the first)
       for (int i = 0; i < nu; ++i) {
-        const int a = i % RA, b = i % RD;
-        const uint32_t pa = (i / RA) & 1u;
-        if (!mbar_wait(&a_full[a], pa) || !mbar_wait(&x_full[a], pa) ||
-            (i >= RD && !mbar_wait(&dempty[b], ((i / RD) - 1) & 1u))) {
+        if (!mbar_wait(&a_full[a], pa) || (i >= RD && !mbar_wait(&dempty[b], pd))) {
           set_status(p.status, FL_ERR_TIMEOUT, 32);
           break;
         }
@@ -921,6 +924,8 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
                          sw128_desc(x0 + h * NB * 128 + kk * 32), idesc, (h | kk) != 0);
         umma_commit(&a_empty[a]);
         umma_commit(&dfull[b]);
+        if (++a == RA) a = 0, pa ^= 1u;
+        if (++b == RD) b = 0, pd ^= 1u;
       }
     }
   } else if (warp >= kTdDeq0 && warp < kTdEpi0) {
@@ -965,6 +970,11 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
         unpack(std::integral_constant<int, 1>());
       if (prev >= 0) {
         tmem_wait_st();
+        if (!mbar_wait(&x_full[prev % RA], static_cast<uint32_t>(prev / RA) & 1u)) {
+          set_status(p.status, FL_ERR_TIMEOUT, 36);
+          prev = -1;
+          break;
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -977,9 +987,11 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
     }
     if (prev >= 0) {
       tmem_wait_st();
+      const bool xok = mbar_wait(&x_full[prev % RA], static_cast<uint32_t>(prev / RA) & 1u);
+      if (!xok) set_status(p.status, FL_ERR_TIMEOUT, 36);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && xok) {
         mbar_arrive(&a_full[prev % RA]);
         mbar_arrive(&sb_empty[prev % RS]);
       }
