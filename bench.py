@@ -36,12 +36,12 @@ BYTES_PER_WEIGHT = 0.51953125          # 0.5 B code + 2 B scale / 128 + 0.5 B ze
 LLAMA = [("qkv", 4096, 12288), ("gate", 4096, 11008), ("up", 4096, 11008), ("down", 11008, 4096)]
 DECODE_M = [1, 8, 32]
 # DRAM traffic / algorithmic bytes of k_linear_rows, from one ncu capture of
-# the M=1 fused-QKV launch (profiles/k_linear_rows_m1_qkv_full.md):
-# 26.204672 MB read, 0 written, for 26.181632 MB of weights + x + y.
-# Traffic grows in proportion to the super-blocks a launch streams, so the
-# per-launch traffic of the step is scaled from it.  Reset to None whenever the
-# kernel changes after that capture.
-TRAFFIC_RATIO = 26.204672 / 26.181632
+# the M=1 fused-QKV launch (profiles/k_linear_rows_m1_qkv.md): 26,205,952 B
+# read, 0 written, for 26,181,632 algorithmic bytes.  Traffic grows in
+# proportion to the super-blocks a launch streams, so the per-launch traffic
+# is scaled from it.  Reset to None whenever the kernel changes after that
+# capture.
+TRAFFIC_RATIO = 26205952 / 26181632
 WORKLOAD = "llama7b-decode-linears int4g g128: (K,N) in {(4096,12288),(4096,11008)x2,(11008,4096)} x M in {1,8,32}"
 
 
@@ -250,7 +250,6 @@ def run_gpu(args):
             ws = torch.zeros(fl.fl_int4g_linear_workspace(M, N, K), dtype=torch.uint8, device=dev)
             calls.append((M, K, N, x, w, y, ws))
     wbytes = sum(BYTES_PER_WEIGHT * N * K for (M, K, N, *_r) in calls)
-    algo_bytes = sum(BYTES_PER_WEIGHT * N * K + 2 * M * K + 2 * M * N for (M, K, N, *_r) in calls)
 
     stream = torch.cuda.Stream(device=dev)
 
@@ -292,7 +291,6 @@ def run_gpu(args):
     ms_total = t0.elapsed_time(t1)
     ms_step = ms_total / args.steps
     value = wbytes / (ms_step * 1e-3) / 1e9
-    achieved = algo_bytes / (ms_step * 1e-3) / 1e9
 
     # per-M breakdown (outside the timed region): a graph of each M's 4 launches, repeated
     per_m = {}
@@ -312,6 +310,27 @@ def run_gpu(args):
         torch.cuda.synchronize()
         b = 15 * sum(BYTES_PER_WEIGHT * N * K for (_m, K, N, *_r) in sub)
         per_m[M] = round(b / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+
+    # roofline of the dominant kernel, k_linear_rows (the M <= 16 calls): a
+    # graph of just those launches (8 distinct matrices, 192 MB > L2, so every
+    # launch streams from HBM), timed with CUDA events on the launching stream
+    rows_calls = [c for c in calls if c[0] <= 16]
+    g_rows = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_rows, stream=stream):
+        launch_all(rows_calls)
+    reps_rows = 200
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g_rows.replay()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(reps_rows):
+            g_rows.replay()
+        r1.record(stream)
+    torch.cuda.synchronize()
+    rows_launch_s = r0.elapsed_time(r1) * 1e-3 / (reps_rows * len(rows_calls))
+    rows_algo = sum(BYTES_PER_WEIGHT * N * K + 2 * M * K + 2 * M * N for (M, K, N, *_r) in rows_calls) / len(rows_calls)
+    achieved = rows_algo / rows_launch_s / 1e9
 
     for (M, K, N, x, w, y, ws) in calls:
         assert torch.isfinite(y.float()).all(), "non-finite output"
@@ -375,16 +394,19 @@ def run_gpu(args):
             "per_M_weight_GBps_untimed": {str(M): v for M, v in per_m.items()},
         },
         "roofline": {
-            "kernel": "k_linear_rows (decode int4g linear, M<=32): all launches of the step",
-            "duration": "timed region / launches (back-to-back, PDL-overlapped)",
+            "kernel": "k_linear_rows (decode int4g linear, M <= 16): the 8 launches of the step at M in {1, 8}",
+            "duration": "events around 200 replays of a graph of those 8 launches / launches (PDL-chained)",
+            "launch_us": round(rows_launch_s * 1e6, 3),
+            "bytes_per_launch": round(rows_algo),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": pk["hbm_gbs"],
             "peak_source": pk["source"] + " burst copy",
             "unit": "GB/s",
             "frac": round(achieved / pk["hbm_gbs"], 4),
-            "traffic": (round(algo_bytes / len(calls) * TRAFFIC_RATIO / 1e6, 3) if TRAFFIC_RATIO else None),
-            "traffic_unit": "MB per launch (scaled from the ncu capture of the M=1 fused-QKV launch)",
+            "traffic": (round(rows_algo * TRAFFIC_RATIO / 1e6, 3) if TRAFFIC_RATIO else None),
+            "traffic_unit": "MB per launch (DRAM read + write of the ncu capture of the M=1 fused-QKV launch, "
+                            "scaled by algorithmic bytes)",
         },
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": len(calls) * args.steps,
