@@ -1098,6 +1098,277 @@ int launch_tcdec(const void* x, int M, int K, const void* w, int N, void* y, voi
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
+// ======================================================================
+// Grouped expert GEMM of the MoE layer on tcgen05 (token segments of up to
+// 128 positions of one expert, in expert order).  A tile is (segment s, 128
+// output rows nt); tiles are split over the CTAs as whole tiles (no split-K),
+// so every output element is one fp32 sum written once.  The roles are those
+// of k_gemm_tc with BN = 128: x producer (TMA boxes of the segment's 128
+// position rows, rows past the segment are computed and not stored), weight
+// producer (the segment's expert), MMA issuer, 8 dequant warps, 8 epilogue
+// warps.  Output: fp32 rows of the segment's positions, times wpos[pos] when
+// given (the down projection), else as they are (gate/up).
+struct MgParams {
+  const uint8_t* w;          // routed experts back to back
+  const uint8_t* w_shared;   // shared expert (expert index E) or null
+  size_t wbytes;             // bytes of one expert's interleaved matrix
+  const int32_t* seg_e;
+  const int32_t* seg_pos;
+  const int32_t* seg_n;
+  const int32_t* nseg;       // device: number of segments (written by the permute kernel)
+  const float* wpos;         // per-position scale or null
+  float* out;                // [positions][ldo]
+  int ldo, G, TT, E, P;
+  int32_t* status;
+};
+
+constexpr int kMgThreads = 20 * 32;
+
+struct MgCfg {
+  static constexpr int BN = 128;
+  static constexpr int kBBox = BN * 64 * 2;     // 16 KB
+  static constexpr int kBStages = 8;
+  static constexpr int kSStages = 8;
+  static constexpr int kARing = 4;
+  static constexpr int kSOff = kBStages * kBBox;
+  static constexpr int kBarOff = kSOff + kSStages * kSbBytes;
+  static constexpr int kNumBars = 2 * kBStages + 2 * kSStages + 2 * kARing + 2;
+  static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kSmem <= 232448, "shared memory");
+};
+
+__global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constant__ CUtensorMap xmap, const MgParams p) {
+  using C = MgCfg;
+  constexpr int BN = C::BN, RA = C::kARing, NBS = C::kBStages, NSS = C::kSStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bfull = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* bempty = bfull + NBS;
+  uint64_t* sfull = bempty + NBS;
+  uint64_t* sempty = sfull + NSS;
+  uint64_t* afull = sempty + NSS;
+  uint64_t* aempty = afull + RA;
+  uint64_t* dfull = aempty + RA;
+  uint64_t* dempty = dfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NBS; ++i) {
+      mbar_init(&bfull[i], 1);
+      mbar_init(&bempty[i], 1);
+    }
+    for (int i = 0; i < NSS; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sempty[i], 8);
+    }
+    for (int i = 0; i < RA; ++i) {
+      mbar_init(&afull[i], 8);
+      mbar_init(&aempty[i], 1);
+    }
+    mbar_init(dfull, 1);
+    mbar_init(dempty, 8);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_d = *tmem_slot;
+  const uint32_t tmem_a = tmem_d + BN;
+  pdl_launch_dependents();
+  // the segment plan, the weights' selection and x come from earlier kernels
+  pdl_wait();
+  const int ntiles = *p.nseg * p.TT;
+  const int t0 = static_cast<int>(static_cast<long long>(c) * ntiles / p.P);
+  const int t1 = static_cast<int>(static_cast<long long>(c + 1) * ntiles / p.P);
+  const int nu = (t1 - t0) * p.G;   // units of this CTA, tile-major
+
+  if (warp == 0) {
+    // ---------------- x producer
+    if (lane == 0) {
+      int j = 0;
+      bool ok = true;
+      for (int t = t0; t < t1 && ok; ++t) {
+        const int pos0 = p.seg_pos[t / p.TT];
+        for (int g = 0; g < p.G && ok; ++g) {
+          for (int h = 0; h < 2; ++h, ++j) {
+            const int b = j % NBS;
+            if (j >= NBS && !mbar_wait(&bempty[b], static_cast<uint32_t>(j / NBS - 1) & 1u)) {
+              set_status(p.status, FL_ERR_TIMEOUT, 41);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bfull[b], C::kBBox);
+            tma_load_2d(smem + b * C::kBBox, &xmap, g * kGroup + 64 * h, pos0, &bfull[b]);
+          }
+        }
+      }
+      if (!ok)
+        for (int jj = j > NBS ? j - NBS : 0; jj < j; ++jj) mbar_wait(&bfull[jj % NBS], static_cast<uint32_t>(jj / NBS) & 1u);
+    }
+  } else if (warp == 2) {
+    // ---------------- weight producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int i = 0;
+      bool ok = true;
+      for (int t = t0; t < t1 && ok; ++t) {
+        const int sg = t / p.TT, nt = t - sg * p.TT, e = p.seg_e[sg];
+        const uint8_t* base = e == p.E ? p.w_shared : p.w + static_cast<size_t>(e) * p.wbytes;
+        for (int g = 0; g < p.G; ++g, ++i) {
+          const int sI = i % NSS;
+          if (i >= NSS && !mbar_wait(&sempty[sI], static_cast<uint32_t>(i / NSS - 1) & 1u)) {
+            set_status(p.status, FL_ERR_TIMEOUT, 42);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sfull[sI], kSbBytes);
+          bulk_g2s_hint(smem + C::kSOff + sI * kSbBytes, base + (static_cast<size_t>(nt) * p.G + g) * kSbBytes,
+                        kSbBytes, &sfull[sI], pol);
+        }
+      }
+      if (!ok)
+        for (int ii = i > NSS ? i - NSS : 0; ii < i; ++ii) mbar_wait(&sfull[ii % NSS], static_cast<uint32_t>(ii / NSS) & 1u);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (one barrier probe per unit: afull certifies the x stages too)
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16<BN>();
+      int jt = 0, a = 0, b = 0;
+      uint32_t aph = 0;
+      for (int i = 0, g = 0; i < nu; ++i) {
+        const bool first = g == 0, last = g == p.G - 1;
+        if ((first && jt > 0 && !mbar_wait(dempty, static_cast<uint32_t>(jt - 1) & 1u)) || !mbar_wait(&afull[a], aph)) {
+          set_status(p.status, FL_ERR_TIMEOUT, 43);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t b0 = smem_u32(smem + b * C::kBBox);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16_ta(tmem_d, tmem_a + a * 64 + h * 32 + kk * 8, sw128_desc(b0 + kk * 32), idesc,
+                         (!first || h != 0 || kk != 0) ? 1u : 0u);
+          umma_commit(&bempty[b]);
+          if (++b == NBS) b = 0;
+        }
+        umma_commit(&aempty[a]);
+        if (++a == RA) a = 0, aph ^= 1u;
+        if (last) {
+          umma_commit(dfull);
+          ++jt;
+        }
+        if (++g == p.G) g = 0;
+      }
+    }
+  } else if (warp >= kPfDeq0 && warp < kPfEpi0) {
+    // ---------------- dequant (as k_gemm_tc): exact bf16(s16 * (q - z)) into the A ring
+    const int q = warp & 3, h = (warp - kPfDeq0) >> 2;
+    const int r = q * 32 + lane;
+    const uint32_t trow = static_cast<uint32_t>(q * 32) << 16;
+    for (int i = 0; i < nu; ++i) {
+      const int sI = i % NSS, a = i % RA;
+      if (!mbar_wait(&sfull[sI], static_cast<uint32_t>(i / NSS) & 1u)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 44);
+        break;
+      }
+      const uint8_t* sb = smem + C::kSOff + sI * kSbBytes;
+      const float sf = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
+      const uint32_t z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
+      uint4 cv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) cv[t] = *reinterpret_cast<const uint4*>(sb + r * 64 + ((t + (r >> 1)) & 3) * 16);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[sI]);
+      const __nv_bfloat16 shi = __float2bfloat16_rn(sf);
+      const __nv_bfloat16 slo = __float2bfloat16_rn(sf - __bfloat162float(shi));
+      const uint32_t hi2 = static_cast<uint32_t>(__bfloat16_as_ushort(shi)) * 0x00010001u;
+      const uint32_t lo2 = static_cast<uint32_t>(__bfloat16_as_ushort(slo)) * 0x00010001u;
+      const uint32_t zz = bf16_bias_pair(z);
+      uint32_t o[32];
+      auto unpack = [&](auto H) {
+        constexpr int hh = decltype(H)::value;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int wl = 8 * hh + t;
+          const uint32_t word = (&cv[wl & 3].x)[wl >> 2];
+#pragma unroll
+          for (int pi = 0; pi < 4; ++pi) {
+            const uint32_t qz = bf16x2_sub(nib_pair_bf16(word, pi), zz);
+            o[4 * t + pi] = bfma2(hi2, qz, bmul2(lo2, qz));
+          }
+        }
+      };
+      if (h == 0)
+        unpack(std::integral_constant<int, 0>());
+      else
+        unpack(std::integral_constant<int, 1>());
+      if (i >= RA && !mbar_wait(&aempty[a], static_cast<uint32_t>(i / RA - 1) & 1u)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 45);
+        break;
+      }
+      tc_fence_after();
+      tmem_st32(tmem_a + trow + a * 64 + h * 32, o);
+      tmem_wait_st();
+      if (!mbar_wait(&bfull[(2 * i) % NBS], static_cast<uint32_t>((2 * i) / NBS) & 1u) ||
+          !mbar_wait(&bfull[(2 * i + 1) % NBS], static_cast<uint32_t>((2 * i + 1) / NBS) & 1u)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 46);
+        break;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[a]);
+    }
+  } else if (warp >= kPfEpi0) {
+    // ---------------- epilogue: rows q*32+lane of the tile, one half of its 128 positions
+    const int e = warp - kPfEpi0, q = warp & 3;
+    const int r = q * 32 + lane;
+    const int col0 = (e >> 2) * (BN / 2);
+    const uint32_t tcol = tmem_d + (static_cast<uint32_t>(q * 32) << 16) + col0;
+    auto release_d = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty);
+    };
+    int jt = 0;
+    for (int t = t0; t < t1; ++t, ++jt) {
+      if (!mbar_wait(dfull, static_cast<uint32_t>(jt) & 1u)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 47);
+        break;
+      }
+      tc_fence_after();
+      const int sg = t / p.TT, nt = t - sg * p.TT;
+      const int pos0 = p.seg_pos[sg], n = p.seg_n[sg];
+      const int col = nt * kRowTile + r;
+      pf_drain<BN / 32>(tcol, release_d, [&](int k, const float (&v)[16]) {
+#pragma unroll
+        for (int tt = 0; tt < 16; ++tt) {
+          const int m = col0 + 16 * k + tt;
+          if (m < n) {
+            const int pos = pos0 + m;
+            const float sc = p.wpos ? p.wpos[pos] : 1.f;
+            p.out[static_cast<size_t>(pos) * p.ldo + col] = sc * v[tt];
+          }
+        }
+      });
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_d, C::kTmemCols);
+  }
+}
+
 }  // namespace
 
 // Prefill path of fl_int4g_linear (M > 32): persistent stream-K tcgen05 GEMM.
@@ -1115,4 +1386,59 @@ int fl_linear_tcdec(const void* x, int M, int K, const void* w, int N, void* y, 
                     size_t part_off, cudaStream_t s) {
   if (M <= 16) return launch_tcdec<16>(x, M, K, w, N, y, ws, cnt_off, part_off, s);
   return launch_tcdec<32>(x, M, K, w, N, y, ws, cnt_off, part_off, s);
+}
+
+// Grouped expert GEMM of the MoE layer (see k_moe_gemm).  x: [npos, K] bf16
+// rows in position order; out: [npos, ldo] fp32.  nseg, seg_* and wpos are
+// device arrays written by earlier kernels on the same stream.
+int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* w_shared, size_t wbytes, int E, int Nout,
+                const int32_t* seg_e, const int32_t* seg_pos, const int32_t* seg_n, const int32_t* nseg,
+                const float* wpos, float* out, int32_t* status, cudaStream_t s) {
+  auto enc = encode_fn();
+  if (!enc) return FL_ERR_CUDA;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(npos)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(MgCfg::BN)};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return FL_ERR_CUDA;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(k_moe_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, MgCfg::kSmem) != cudaSuccess)
+      return FL_ERR_CUDA;
+    attr_done[dev] = true;
+  }
+  MgParams p;
+  p.w = static_cast<const uint8_t*>(w);
+  p.w_shared = static_cast<const uint8_t*>(w_shared);
+  p.wbytes = wbytes;
+  p.seg_e = seg_e;
+  p.seg_pos = seg_pos;
+  p.seg_n = seg_n;
+  p.nseg = nseg;
+  p.wpos = wpos;
+  p.out = out;
+  p.ldo = Nout;
+  p.G = K / kGroup;
+  p.TT = Nout / kRowTile;
+  p.E = E;
+  p.P = flh::sm_count();
+  p.status = status;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.P));
+  cfg.blockDim = dim3(kMgThreads);
+  cfg.dynamicSmemBytes = MgCfg::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k_moe_gemm, map, p) != cudaSuccess) return FL_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }

@@ -17,6 +17,13 @@
 // The grouped kernels stream each active expert's super-blocks once per
 // 32-token segment, with the same register-dequant mma.sync consumer as the
 // decode linear, split over K across all SMs with a ticket hand-off.
+//
+// With many tokens per expert (see moe_uses_gemm) the two grouped steps run on the
+// tensor-memory GEMM instead (fl_moe_gemm, segments of up to 128 positions):
+//   k_moe_gather   x rows in position order, bf16 [pos, H]
+//   fl_moe_gemm    gate/up rows, fp32 [pos, 2I]
+//   k_moe_swiglu   h = silu(gate) * up, bf16 [pos, I]
+//   fl_moe_gemm    out = w_pos * (W2 h), fp32 [pos, H]
 #include "fl_common.cuh"
 #include "fl_rows.cuh"
 
@@ -119,6 +126,7 @@ struct PermuteArgs {
   int M, E, k, TT13, TT2;       // TT: row tiles of the grouped kernels' outputs
   int G13, G2;                  // groups along K of the two grouped kernels
   int has_shared;
+  int seg_rows;                 // positions per segment (32: grouped rows kernels, 128: grouped GEMM)
   int32_t* offsets;             // [E+1]
   int32_t* perm;                // [M*k]
   int32_t* inv;                 // [M*k]
@@ -178,11 +186,11 @@ __global__ void __launch_bounds__(1024, 1) k_moe_permute(const PermuteArgs a) {
       tot[e] = run;                              // exclusive scan -> offsets
       nch[e] = seg;                              // first segment of expert e
       run += c;
-      seg += (c + kSegRows - 1) / kSegRows;
+      seg += (c + a.seg_rows - 1) / a.seg_rows;
     }
     tot[E] = run;
     nch[E] = seg;
-    const int nshared = a.has_shared ? (a.M + kSegRows - 1) / kSegRows : 0;
+    const int nshared = a.has_shared ? (a.M + a.seg_rows - 1) / a.seg_rows : 0;
     a.plan->nseg = seg + nshared;
     a.plan->U = (seg + nshared) * a.TT13 * a.G13;   // == (seg + nshared) * TT2 * G2
   }
@@ -218,24 +226,24 @@ __global__ void __launch_bounds__(1024, 1) k_moe_permute(const PermuteArgs a) {
   // segments
   for (int e = tid; e < E; e += blockDim.x) {
     const int c = tot[e + 1] - tot[e];
-    for (int s = 0; s * kSegRows < c; ++s) {
+    for (int s = 0; s * a.seg_rows < c; ++s) {
       const int si = nch[e] + s;
       a.seg_e[si] = e;
-      a.seg_pos[si] = tot[e] + s * kSegRows;
-      a.seg_n[si] = min(kSegRows, c - s * kSegRows);
+      a.seg_pos[si] = tot[e] + s * a.seg_rows;
+      a.seg_n[si] = min(a.seg_rows, c - s * a.seg_rows);
     }
   }
   if (a.has_shared) {
-    const int ns = (a.M + kSegRows - 1) / kSegRows;
+    const int ns = (a.M + a.seg_rows - 1) / a.seg_rows;
     for (int s = tid; s < ns; s += blockDim.x) {
       const int si = nch[E] + s;
       a.seg_e[si] = E;   // E denotes the shared expert
-      a.seg_pos[si] = n + s * kSegRows;
-      a.seg_n[si] = min(kSegRows, a.M - s * kSegRows);
+      a.seg_pos[si] = n + s * a.seg_rows;
+      a.seg_n[si] = min(a.seg_rows, a.M - s * a.seg_rows);
     }
   }
   // zero the ticket counters the grouped kernels will use
-  const int nseg = nch[E] + (a.has_shared ? (a.M + kSegRows - 1) / kSegRows : 0);
+  const int nseg = nch[E] + (a.has_shared ? (a.M + a.seg_rows - 1) / a.seg_rows : 0);
   for (int i = tid; i < nseg * a.TT13 * kConsumerWarps; i += blockDim.x) a.cnt13[i] = 0;
   for (int i = tid; i < nseg * a.TT2 * kConsumerWarps; i += blockDim.x) a.cnt2[i] = 0;
 }
@@ -508,14 +516,51 @@ __global__ void k_moe_combine(const float* __restrict__ out, const int32_t* __re
   y[static_cast<size_t>(t) * H + n] = __float2bfloat16_rn(acc);
 }
 
+// ------------------------------------------------------------------ gather / SwiGLU (grouped-GEMM path)
+// xp[pos] = x[token of pos], 16 bytes per thread.
+__global__ void k_moe_gather(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ tok_of_pos, int npos,
+                             int H, __nv_bfloat16* __restrict__ xp) {
+  pdl_wait();
+  const int per_row = H / 8;
+  const long long total = static_cast<long long>(npos) * per_row;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int pos = static_cast<int>(i / per_row), c = static_cast<int>(i - static_cast<long long>(pos) * per_row);
+    const int t = tok_of_pos[pos];
+    reinterpret_cast<uint4*>(xp + static_cast<size_t>(pos) * H)[c] =
+        reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H)[c];
+  }
+}
+
+// h[pos, i] = bf16(silu(gu[pos, i]) * gu[pos, I + i]), gate rows first.
+__global__ void k_moe_swiglu(const float* __restrict__ gu, int npos, int I, __nv_bfloat16* __restrict__ h) {
+  pdl_wait();
+  const long long total = static_cast<long long>(npos) * I;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int pos = static_cast<int>(i / I), c = static_cast<int>(i - static_cast<long long>(pos) * I);
+    const float g = gu[static_cast<size_t>(pos) * 2 * I + c], u = gu[static_cast<size_t>(pos) * 2 * I + I + c];
+    h[i] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
+  }
+}
+
 // ------------------------------------------------------------------ host plan
 size_t al(size_t v) { return (v + 255) / 256 * 256; }
 
 struct MoeLayout {
-  size_t plan, ids, wts, offsets, perm, inv, tok, wpos, sege, segp, segn, h, out, cnt13, cnt2, part13, part2, total;
-  int nseg_max, P, stages13, stages2;
+  size_t plan, ids, wts, offsets, perm, inv, tok, wpos, sege, segp, segn, h, out, cnt13, cnt2, part13, part2, xp, gu,
+      total;
+  int nseg_max, P, stages13, stages2, gemm;
   uint32_t stage13, stage2;
 };
+
+// Many tokens per expert: the grouped steps run on the tensor-memory GEMM
+// (from 8 tokens per expert on average, or from 2 with large experts, where
+// the GEMM's per-super-block cost wins over its extra launches).
+bool moe_uses_gemm(int M, int E, int k, int H) {
+  const long long n = static_cast<long long>(M) * k;
+  return n >= 8LL * E || (n >= 2LL * E && H >= 4096);
+}
 
 bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeLayout* L) {
   if (M < 1 || E < 1 || E > kMaxE || k < 1 || k > E || k > 32 || H < kGroup || I < kGroup || H % kGroup ||
@@ -544,6 +589,9 @@ bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeL
   L->cnt2 = o; o = al(o + 4ull * L->nseg_max * TT2 * kConsumerWarps);
   L->part13 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * kNT * 2);
   L->part2 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * kNT);
+  L->gemm = moe_uses_gemm(M, E, k, H) ? 1 : 0;
+  L->xp = o; o = al(o + (L->gemm ? 2ull * npos * H : 0));
+  L->gu = o; o = al(o + (L->gemm ? 4ull * npos * 2 * I : 0));
   L->total = o;
   L->stage13 = static_cast<uint32_t>((2 * kSbBytes + kSegRows * kXRowStride + 127) / 128 * 128);
   L->stage2 = static_cast<uint32_t>((kSbBytes + kSegRows * kXRowStride + 127) / 128 * 128);
@@ -571,6 +619,10 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 }
 
 }  // namespace
+
+int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* w_shared, size_t wbytes, int E, int Nout,
+                const int32_t* seg_e, const int32_t* seg_pos, const int32_t* seg_n, const int32_t* nseg,
+                const float* wpos, float* out, int32_t* status, cudaStream_t s);
 
 extern "C" int fl_moe_int4g_workspace(int M, int E, int k, int H, int I, int has_shared, size_t* out) {
   if (!out) return FL_ERR_ARG;
@@ -625,6 +677,7 @@ extern "C" int fl_moe_int4g(const void* x, const float* logits, int M, int H, in
     a.G13 = H / kGroup;
     a.G2 = I / kGroup;
     a.has_shared = has_shared;
+    a.seg_rows = L.gemm ? 128 : kSegRows;
     a.offsets = reinterpret_cast<int32_t*>(W + L.offsets);
     a.perm = reinterpret_cast<int32_t*>(W + L.perm);
     a.inv = reinterpret_cast<int32_t*>(W + L.inv);
@@ -651,8 +704,30 @@ extern "C" int fl_moe_int4g(const void* x, const float* logits, int M, int H, in
     if (smem > 227 * 1024) return FL_ERR_UNSUPPORTED;
     if (launch_pdl(k_moe_permute, dim3(1), dim3(1024), smem, s, a) != cudaSuccess) return FL_ERR_CUDA;
   }
+  const int n = M * k, npos = n + (has_shared ? M : 0);
+  if (L.gemm) {
+    const int32_t* sege = reinterpret_cast<const int32_t*>(W + L.sege);
+    const int32_t* segp = reinterpret_cast<const int32_t*>(W + L.segp);
+    const int32_t* segn = reinterpret_cast<const int32_t*>(W + L.segn);
+    const int32_t* nseg = reinterpret_cast<const int32_t*>(W + L.plan);   // MoePlan::nseg
+    __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(W + L.xp);
+    float* gu = reinterpret_cast<float*>(W + L.gu);
+    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(W + L.h);
+    const int sms = flh::sm_count();
+    if (launch_pdl(k_moe_gather, dim3(4 * sms), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(x),
+                   reinterpret_cast<const int32_t*>(W + L.tok), npos, H, xp) != cudaSuccess)
+      return FL_ERR_CUDA;
+    int rc = fl_moe_gemm(xp, npos, H, w13, shared_w13, b13, E, 2 * I, sege, segp, segn, nseg, nullptr, gu, status, s);
+    if (rc != FL_OK) return rc;
+    if (launch_pdl(k_moe_swiglu, dim3(4 * sms), dim3(256), 0, s, static_cast<const float*>(gu), npos, I, h) !=
+        cudaSuccess)
+      return FL_ERR_CUDA;
+    rc = fl_moe_gemm(h, npos, I, w2, shared_w2, b2, E, H, sege, segp, segn, nseg,
+                     reinterpret_cast<const float*>(W + L.wpos), reinterpret_cast<float*>(W + L.out), status, s);
+    if (rc != FL_OK) return rc;
+  }
   // grouped gate/up + SwiGLU, then grouped down
-  for (int mode = 0; mode < 2; ++mode) {
+  for (int mode = 0; mode < 2 && !L.gemm; ++mode) {
     MoeRowsParams p;
     p.w = static_cast<const uint8_t*>(mode == 0 ? w13 : w2);
     p.w_shared = static_cast<const uint8_t*>(mode == 0 ? shared_w13 : shared_w2);

@@ -203,9 +203,10 @@ def test_moe_qwen3_shaped():
 
 def test_moe_deepseek_shaped():
     """256 routed experts + 1 shared, hidden 7168, intermediate 2048, top-8
-    sigmoid renormalised, skewed logits; M in {1, 16} (sampled tokens)."""
+    sigmoid renormalised, skewed logits; M in {1, 16, 512} (sampled tokens;
+    M = 512 runs the grouped tensor-memory GEMM path)."""
     ex = DeviceExperts(256, 7168, 2048, layer=800, shared=True)
-    for M in (1, 16):
+    for M in (1, 16, 512):
         xb = inputs.activations(M, 7168, stream=800 + M)
         logits = inputs.router_logits(M, 256, stream=800 + M, hot=51)
         y, ids, wts, offs, perm = run_moe(xb, logits, 8, 2048, ex.w13, ex.w2, fl.FL_SIGMOID, True, ex.sw13, ex.sw2)
