@@ -152,6 +152,49 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Thread-block clusters: full barrier of every thread of the cluster (all
+// CTAs of a cluster are resident together, so it cannot wait on a CTA that
+// has not started).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Generic address of the same shared-memory object in cluster rank 0.
+template <typename T>
+__device__ __forceinline__ T* cluster_map_rank0(T* p) {
+  uint64_t out;
+  asm volatile("mapa.u64 %0, %1, 0;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(p)));
+  return reinterpret_cast<T*>(out);
+}
+// Bounded wait, acquire at cluster scope (for arrivals made by other CTAs of
+// the cluster with release.cluster); false when the limit ran out.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+// Arrive (release, cluster scope) on the same mbarrier in cluster rank 0.
+__device__ __forceinline__ void mbar_arrive_remote_rank0(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\t"
+      "mapa.shared::cluster.u32 ra, %0, 0;\n\t"
+      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
 // Named barrier over `nthreads` threads (multiple of 32).
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

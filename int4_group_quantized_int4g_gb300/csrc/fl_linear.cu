@@ -46,6 +46,8 @@ struct RowsParams {
   int M, K, N, T, G, P;
   int stages;
   uint32_t stage_bytes;
+  int csize;         // > 1: clusters of csize CTAs split one row tile over K (DSMEM reduction)
+  uint32_t red_off;  // shared-memory offset of the cluster reduction barrier and buffer
 };
 
 // CTA c owns units [unit_begin(c), unit_begin(c+1)); cta_of_unit inverts it.
@@ -143,6 +145,53 @@ __device__ __forceinline__ void ticket_tile(const RowsParams& p, int T, int warp
   if (lane == 0) p.cnt[T * kConsumerWarps + warp] = 0;
 }
 
+// Cluster reduction of row tile T: ranks 1..csize-1 write their warps' sums
+// into rank 0's shared memory (distributed shared memory) and arrive on its
+// barrier; rank 0 adds them to its own in rank order (= K order,
+// deterministic) and writes y.  No global round trip, no ticket.
+template <int NT>
+__device__ __forceinline__ void cluster_reduce(const RowsParams& p, int T, int rank, int warp, int lane,
+                                               const float (&tot)[NT][4], uint64_t* red_bar, float* red_buf) {
+  constexpr int V = 4 * NT;   // values per lane
+  if (rank > 0) {
+    float* dst = cluster_map_rank0(red_buf) + ((static_cast<size_t>(rank - 1) * kConsumerWarps + warp) * 32 + lane) * V;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      *reinterpret_cast<float4*>(dst + 4 * nt) = make_float4(tot[nt][0], tot[nt][1], tot[nt][2], tot[nt][3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_remote_rank0(red_bar);
+    return;
+  }
+  if (!mbar_wait_cluster(red_bar, 0)) {
+    if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 4);
+    return;
+  }
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = tot[nt][e];
+  for (int rr = 1; rr < p.csize; ++rr) {
+    const float* src = red_buf + ((static_cast<size_t>(rr - 1) * kConsumerWarps + warp) * 32 + lane) * V;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float4 v = *reinterpret_cast<const float4*>(src + 4 * nt);
+      acc[nt][0] += v.x, acc[nt][1] += v.y, acc[nt][2] += v.z, acc[nt][3] += v.w;
+    }
+  }
+  const int gid = lane >> 2, tig = lane & 3;
+  const int rbase = T * kRowTile + warp * 16;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int n = rbase + gid + (e >> 1) * 8;
+      const int m = nt * 8 + 2 * tig + (e & 1);
+      if (n < p.N && m < p.M) p.y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(acc[nt][e]);
+    }
+  }
+}
+
 // NT token tiles of 8; UPS super-blocks per pipeline stage (2 gives each
 // warp two independent MMA chains and 17 KB bulk copies).  One CTA per SM,
 // sized to leave room for the next kernel's CTA (programmatic launch), which
@@ -157,7 +206,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) k_linear_rows(const
   float* xsum = reinterpret_cast<float*>(empty + p.stages);   // [group slot][Mp]: sum_k x over each group
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
-  const int u0 = unit_begin(c, p.U, p.P), u1 = unit_begin(c + 1, p.U, p.P);
+  // stream-K ranges, or (clusters) K slice `rank` of row tile c / csize
+  const int rank = p.csize > 1 ? c % p.csize : 0;
+  int u0, u1;
+  if (p.csize > 1) {
+    const int t = c / p.csize;
+    u0 = t * p.G + rank * p.G / p.csize;
+    u1 = t * p.G + (rank + 1) * p.G / p.csize;
+  } else {
+    u0 = unit_begin(c, p.U, p.P);
+    u1 = unit_begin(c + 1, p.U, p.P);
+  }
+  uint64_t* red_bar = reinterpret_cast<uint64_t*>(smem + p.red_off);
+  float* red_buf = reinterpret_cast<float*>(smem + p.red_off + 16);   // [csize-1][warp][lane][4*NT]
   const int nstage = (u1 - u0 + UPS - 1) / UPS;   // stages this CTA fills, in order
   const uint32_t xoff = UPS * kSbBytes;           // x slices follow the super-blocks
   const int g0 = u0 % p.G;
@@ -168,9 +229,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) k_linear_rows(const
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
+    if (p.csize > 1) mbar_init(red_bar, (p.csize - 1) * kConsumerWarps);
     fence_mbar_init();
   }
   __syncthreads();
+  // rank 0's reduction barrier is initialised before any peer can arrive on it
+  if (p.csize > 1) cluster_sync_all();
   // the next kernel in the stream may start prefetching its weights now
   pdl_launch_dependents();
 
@@ -265,6 +329,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) k_linear_rows(const
     const int ua = u0 + k * UPS, n = min(UPS, u1 - ua);
     if (!mbar_wait(&full[s], ph)) {
       if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 2);
+      // rank 0 of a cluster stays until its peers' DSMEM writes have landed
+      if (p.csize > 1 && rank == 0) mbar_wait_cluster(red_bar, 0);
       return;
     }
     const uint8_t* sb = smem + static_cast<size_t>(s) * p.stage_bytes;
@@ -313,6 +379,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) k_linear_rows(const
     }
     if (++s == p.stages) s = 0, ph ^= 1u;
   }
+  if (p.csize > 1) {
+    cluster_reduce<NT>(p, curT, rank, warp, lane, tot, red_bar, red_buf);
+    return;
+  }
   const bool owed1 = store_tile<NT>(p, curT, c, u0, u1, warp, lane, tot);
   // only the first and the last row tile of a CTA's range can be partial
   if (owed0 >= 0) ticket_tile<NT>(p, owed0, warp, lane);
@@ -321,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) k_linear_rows(const
 
 // ------------------------------------------------------------------ plan
 struct RowsPlan {
-  int T, G, P, NT, ups, stages, U;
-  uint32_t stage_bytes;
+  int T, G, P, NT, ups, stages, U, csize;
+  uint32_t stage_bytes, red_off;
   size_t smem, cnt_off, part_off, ws_bytes;
 };
 
@@ -340,16 +410,33 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl) {
   pl->ups = pl->NT <= 2 ? 2 : 1;
   // M <= 8: two CTAs per SM (four consumer warps per scheduler)
   const long long slots = static_cast<long long>(sms) * (pl->NT == 1 ? 2 : 1);
-  pl->P = static_cast<int>(U < slots ? U : slots);
+  // Few row tiles: clusters of csize CTAs share each tile, split over K, and
+  // reduce through distributed shared memory.  Otherwise contiguous unit
+  // ranges over all tiles (stream-K) with the global ticket hand-off.
+  pl->csize = 1;
+  if (2LL * pl->T <= slots) {
+    long long cs = slots / pl->T;
+    if (cs > 8) cs = 8;
+    if (cs > pl->G) cs = pl->G;
+    pl->csize = static_cast<int>(cs);
+  }
+  if (pl->csize > 1)
+    pl->P = pl->T * pl->csize;
+  else
+    pl->P = static_cast<int>(U < slots ? U : slots);
+  const size_t red_bytes =
+      pl->csize > 1 ? 16 + static_cast<size_t>(pl->csize - 1) * kConsumerWarps * 32 * 4 * pl->NT * sizeof(float) : 0;
   pl->stage_bytes = static_cast<uint32_t>(
       align_up(static_cast<size_t>(pl->ups) * (kSbBytes + static_cast<size_t>(M) * kXRowStride), 128));
-  const size_t budget = pl->NT == 1 ? 100u * 1024u : 200u * 1024u;
+  const size_t budget = (pl->NT == 1 ? 100u * 1024u : 200u * 1024u) - red_bytes;
   int stages = static_cast<int>(budget / pl->stage_bytes);
   pl->stages = stages > 12 ? 12 : (stages < 2 ? 2 : stages);
-  const int units_max = (pl->U + pl->P - 1) / pl->P;
+  const int units_max = pl->csize > 1 ? (pl->G + pl->csize - 1) / pl->csize : (pl->U + pl->P - 1) / pl->P;
   const int nslot = units_max < pl->G ? units_max : pl->G;
   pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes + 2 * pl->stages * sizeof(uint64_t) +
              static_cast<size_t>(nslot) * 8 * pl->NT * sizeof(float);
+  pl->red_off = static_cast<uint32_t>(align_up(pl->smem, 16));
+  if (red_bytes) pl->smem = pl->red_off + red_bytes;
   pl->cnt_off = kTicketOff;
   pl->part_off = kScratchOff;
   pl->ws_bytes = pl->part_off + static_cast<size_t>(pl->P + pl->T) * kRowTile * (8 * pl->NT) * 4;
@@ -372,11 +459,15 @@ int launch_rows(const RowsPlan& pl, const RowsParams& prm, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(pl.csize);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pl.csize > 1 ? 2 : 1;
   if (cudaLaunchKernelEx(&cfg, k_linear_rows<NT, UPS>, prm) != cudaSuccess) return FL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
@@ -412,6 +503,8 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   prm.P = pl.P;
   prm.stages = pl.stages;
   prm.stage_bytes = pl.stage_bytes;
+  prm.csize = pl.csize;
+  prm.red_off = pl.red_off;
   switch (pl.NT) {
     case 1: return launch_rows<1, 2>(pl, prm, stream);
     case 2: return launch_rows<2, 2>(pl, prm, stream);
