@@ -901,16 +901,19 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
         tma_load_2d(xbuf + a * C::kXBytes + NB * 128, &xmap, g * kGroup + 64, 0, &x_full[a]);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer
+  } else if (warp == 1 || warp == 3) {
+    // ---------------- MMA issuers: warp 1 takes the even super-blocks, warp 3
+    // the odd ones.  One thread issues tcgen05.mma at only about one per 65
+    // cycles, and at N = NB the tensor pipe is far from full, so two issuers
+    // double the rate (each commit tracks only its own thread's MMAs).
+    // One probe per super-block in the common case: a_full also certifies
+    // the x tile (the dequant warps wait for it before arriving).
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16<NB>();
-      // one probe per super-block in the common case: a_full also certifies
-      // the x tile (the dequant warps wait for it before arriving)
-      int a = 0, b = 0;
-      uint32_t pa = 0, pd = 1;   // the D ring starts free (parity of the phase before the first)
-      for (int i = 0; i < nu; ++i) {
-        if (!mbar_wait(&a_full[a], pa) || (i >= RD && !mbar_wait(&dempty[b], pd))) {
+      for (int i = warp == 1 ? 0 : 1; i < nu; i += 2) {
+        const int a = i % RA, b = i % RD;
+        if (!mbar_wait(&a_full[a], static_cast<uint32_t>(i / RA) & 1u) ||
+            (i >= RD && !mbar_wait(&dempty[b], static_cast<uint32_t>(i / RD - 1) & 1u))) {
           set_status(p.status, FL_ERR_TIMEOUT, 32);
           break;
         }
@@ -924,8 +927,6 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
                          sw128_desc(x0 + h * NB * 128 + kk * 32), idesc, (h | kk) != 0);
         umma_commit(&a_empty[a]);
         umma_commit(&dfull[b]);
-        if (++a == RA) a = 0, pa ^= 1u;
-        if (++b == RD) b = 0, pd ^= 1u;
       }
     }
   } else if (warp >= kTdDeq0 && warp < kTdEpi0) {
