@@ -748,10 +748,13 @@ struct TdParams {
 template <int NB>
 struct TdCfg {
   static constexpr int kXBytes = NB * 256;                        // NB rows x 128 k bf16 (two swizzled halves)
-  static constexpr int kSbRing = 20;                              // super-blocks in flight per CTA
-  static constexpr int kARing = 4;                                // dequantized A tiles (tensor memory) + x tiles
+  static constexpr int kSbRing = 16;                              // super-blocks in flight per CTA
+  static constexpr int kARing = 4;                                // dequantized A tiles (tensor memory)
+  static constexpr int kXRing = 8;                                // x tiles (one per super-block's group)
   static constexpr int kDRing = 8;                                // accumulators in tensor memory
-  static constexpr int kSmem = kARing * kXBytes + kSbRing * kSbBytes + 1024 + 512;
+  static constexpr int kSmem = kXRing * kXBytes + kSbRing * kSbBytes + 1024 /*align slack*/ + 1024 /*barriers*/;
+  static_assert((2 * kSbRing + 2 * kXRing + 2 * kARing + 2 * kDRing) * 8 + 8 <= 1024, "barrier area");
+  static_assert(kSmem <= 232448, "shared memory");
   static constexpr uint32_t kTmemCols = 512;                      // A ring 4 x 64 columns, D ring 8 x NB
 };
 
@@ -817,16 +820,17 @@ __device__ __forceinline__ void td_ticket(const TdParams& p, int T, int q, int l
 template <int NB>
 __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_constant__ CUtensorMap xmap, const TdParams p) {
   using C = TdCfg<NB>;
-  constexpr int RS = C::kSbRing, RA = C::kARing;
+  constexpr int RS = C::kSbRing, RA = C::kARing, RX = C::kXRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* xbuf = smem;                                    // [RA][NB*256] (1 KB aligned)
-  uint8_t* sbuf = xbuf + RA * C::kXBytes;                  // [RS][8512]
+  uint8_t* xbuf = smem;                                    // [RX][NB*256] (1 KB aligned)
+  uint8_t* sbuf = xbuf + RX * C::kXBytes;                  // [RS][8512]
   uint64_t* sb_full = reinterpret_cast<uint64_t*>(sbuf + RS * kSbBytes);
   uint64_t* sb_empty = sb_full + RS;   // dequant (8 warps) + epilogue (4 warps)
-  uint64_t* x_full = sb_empty + RS;    // x tile landed
-  uint64_t* a_full = x_full + RA;      // A tile dequantized (8 warps)
-  uint64_t* a_empty = a_full + RA;     // MMAs on the A/x slot done
+  uint64_t* x_full = sb_empty + RS;    // [RX] x tile landed
+  uint64_t* x_empty = x_full + RX;     // [RX] MMAs reading the x tile done
+  uint64_t* a_full = x_empty + RX;     // A tile dequantized (8 warps)
+  uint64_t* a_empty = a_full + RA;     // MMAs on the A slot done
   constexpr int RD = C::kDRing;
   uint64_t* dfull = a_empty + RA;      // [RD]
   uint64_t* dempty = dfull + RD;       // [RD]
@@ -842,8 +846,11 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
       mbar_init(&sb_full[j], 1);
       mbar_init(&sb_empty[j], 8 + 4);
     }
+    for (int xs = 0; xs < RX; ++xs) {
+      mbar_init(&x_full[xs], 1);
+      mbar_init(&x_empty[xs], 1);
+    }
     for (int a = 0; a < RA; ++a) {
-      mbar_init(&x_full[a], 1);
       mbar_init(&a_full[a], 8);
       mbar_init(&a_empty[a], 1);
     }
@@ -886,19 +893,16 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
     if (lane == 0) {
       pdl_wait();
       for (int i = 0; i < nu; ++i) {
-        const int a = i % RA;
-        if (i >= RA && !mbar_wait(&a_empty[a], ((i / RA) - 1) & 1u)) {
+        const int xs = i % RX;
+        if (i >= RX && !mbar_wait(&x_empty[xs], static_cast<uint32_t>(i / RX - 1) & 1u)) {
           set_status(p.status, FL_ERR_TIMEOUT, 35);
-          for (int aa = 0; aa < RA; ++aa) {
-            const int nf = i / RA + (aa < i % RA ? 1 : 0);
-            if (nf > 0) mbar_wait(&x_full[aa], static_cast<uint32_t>(nf - 1) & 1u);
-          }
+          for (int jj = i > RX ? i - RX : 0; jj < i; ++jj) mbar_wait(&x_full[jj % RX], static_cast<uint32_t>(jj / RX) & 1u);
           break;
         }
         const int g = (u0 + i) % p.G;
-        mbar_arrive_expect_tx(&x_full[a], C::kXBytes);
-        tma_load_2d(xbuf + a * C::kXBytes, &xmap, g * kGroup, 0, &x_full[a]);
-        tma_load_2d(xbuf + a * C::kXBytes + NB * 128, &xmap, g * kGroup + 64, 0, &x_full[a]);
+        mbar_arrive_expect_tx(&x_full[xs], C::kXBytes);
+        tma_load_2d(xbuf + xs * C::kXBytes, &xmap, g * kGroup, 0, &x_full[xs]);
+        tma_load_2d(xbuf + xs * C::kXBytes + NB * 128, &xmap, g * kGroup + 64, 0, &x_full[xs]);
       }
     }
   } else if (warp == 1 || warp == 3) {
@@ -918,13 +922,15 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
           break;
         }
         tc_fence_after();
-        const uint32_t x0 = smem_u32(xbuf + a * C::kXBytes);
+        const int xs = i % RX;
+        const uint32_t x0 = smem_u32(xbuf + xs * C::kXBytes);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16_ta(tmem_d + 256 + b * NB, tmem_d + a * 64 + h * 32 + kk * 8,
                          sw128_desc(x0 + h * NB * 128 + kk * 32), idesc, (h | kk) != 0);
+        umma_commit(&x_empty[xs]);
         umma_commit(&a_empty[a]);
         umma_commit(&dfull[b]);
       }
@@ -971,7 +977,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
         unpack(std::integral_constant<int, 1>());
       if (prev >= 0) {
         tmem_wait_st();
-        if (!mbar_wait(&x_full[prev % RA], static_cast<uint32_t>(prev / RA) & 1u)) {
+        if (!mbar_wait(&x_full[prev % RX], static_cast<uint32_t>(prev / RX) & 1u)) {
           set_status(p.status, FL_ERR_TIMEOUT, 36);
           prev = -1;
           break;
@@ -988,7 +994,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
     }
     if (prev >= 0) {
       tmem_wait_st();
-      const bool xok = mbar_wait(&x_full[prev % RA], static_cast<uint32_t>(prev / RA) & 1u);
+      const bool xok = mbar_wait(&x_full[prev % RX], static_cast<uint32_t>(prev / RX) & 1u);
       if (!xok) set_status(p.status, FL_ERR_TIMEOUT, 36);
       tc_fence_before();
       __syncwarp();
