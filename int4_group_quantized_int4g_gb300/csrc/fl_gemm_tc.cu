@@ -910,19 +910,19 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
     // the odd ones.  One thread issues tcgen05.mma at only about one per 65
     // cycles, and at N = NB the tensor pipe is far from full, so two issuers
     // double the rate (each commit tracks only its own thread's MMAs).
-    // One probe per super-block in the common case: a_full also certifies
-    // the x tile (the dequant warps wait for it before arriving).
+    // Each issuer probes its super-block's A slot, x tile and accumulator.
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16<NB>();
       for (int i = warp == 1 ? 0 : 1; i < nu; i += 2) {
         const int a = i % RA, b = i % RD;
+        const int xs = i % RX;
         if (!mbar_wait(&a_full[a], static_cast<uint32_t>(i / RA) & 1u) ||
+            !mbar_wait(&x_full[xs], static_cast<uint32_t>(i / RX) & 1u) ||
             (i >= RD && !mbar_wait(&dempty[b], static_cast<uint32_t>(i / RD - 1) & 1u))) {
           set_status(p.status, FL_ERR_TIMEOUT, 32);
           break;
         }
         tc_fence_after();
-        const int xs = i % RX;
         const uint32_t x0 = smem_u32(xbuf + xs * C::kXBytes);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
@@ -977,11 +977,6 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
         unpack(std::integral_constant<int, 1>());
       if (prev >= 0) {
         tmem_wait_st();
-        if (!mbar_wait(&x_full[prev % RX], static_cast<uint32_t>(prev / RX) & 1u)) {
-          set_status(p.status, FL_ERR_TIMEOUT, 36);
-          prev = -1;
-          break;
-        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -994,11 +989,9 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
     }
     if (prev >= 0) {
       tmem_wait_st();
-      const bool xok = mbar_wait(&x_full[prev % RX], static_cast<uint32_t>(prev / RX) & 1u);
-      if (!xok) set_status(p.status, FL_ERR_TIMEOUT, 36);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && xok) {
+      if (lane == 0) {
         mbar_arrive(&a_full[prev % RA]);
         mbar_arrive(&sb_empty[prev % RS]);
       }
