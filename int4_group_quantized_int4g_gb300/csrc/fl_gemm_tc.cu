@@ -941,16 +941,14 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
     const int q = warp & 3, h = (warp - kTdDeq0) >> 2;
     const int r = q * 32 + lane;
     const uint32_t trow = static_cast<uint32_t>(q * 32) << 16;
-    // software pipeline: the tensor-memory store of super-block i completes
-    // while super-block i+1 is dequantized; i is signalled after that
-    int prev = -1;
+    // the super-block is read into registers and released, unpacked, then
+    // stored to its A slot once the MMAs of the slot's previous use are done
     for (int i = 0; i < nu; ++i) {
       const int j = i % RS, a = i % RA;
-      if (!mbar_wait(&sb_full[j], (i / RS) & 1u) || (i >= RA && !mbar_wait(&a_empty[a], ((i / RA) - 1) & 1u))) {
+      if (!mbar_wait(&sb_full[j], (i / RS) & 1u)) {
         set_status(p.status, FL_ERR_TIMEOUT, 33);
         break;
       }
-      tc_fence_after();
       const uint8_t* sb = sbuf + j * kSbBytes;
       const uint32_t z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
       const uint32_t zz = bf16_bias_pair(z);
@@ -959,6 +957,8 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
       uint4 cv[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) cv[t] = *reinterpret_cast<const uint4*>(sb + r * 64 + ((t + (r >> 1)) & 3) * 16);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb_empty[j]);
       uint32_t o[32];
       // h is uniform across the warp: two static copies keep cv in registers
       auto unpack = [&](auto H) {
@@ -975,26 +975,16 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
         unpack(std::integral_constant<int, 0>());
       else
         unpack(std::integral_constant<int, 1>());
-      if (prev >= 0) {
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&a_full[prev % RA]);
-          mbar_arrive(&sb_empty[prev % RS]);
-        }
+      if (i >= RA && !mbar_wait(&a_empty[a], ((i / RA) - 1) & 1u)) {
+        set_status(p.status, FL_ERR_TIMEOUT, 36);
+        break;
       }
+      tc_fence_after();
       tmem_st32(tmem_d + trow + a * 64 + h * 32, o);
-      prev = i;
-    }
-    if (prev >= 0) {
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&a_full[prev % RA]);
-        mbar_arrive(&sb_empty[prev % RS]);
-      }
+      if (lane == 0) mbar_arrive(&a_full[a]);
     }
   } else if (warp >= kTdEpi0) {
     // ---------------- epilogue: row r of every super-block, all tokens
