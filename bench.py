@@ -36,12 +36,10 @@ BYTES_PER_WEIGHT = 0.51953125          # 0.5 B code + 2 B scale / 128 + 0.5 B ze
 LLAMA = [("qkv", 4096, 12288), ("gate", 4096, 11008), ("up", 4096, 11008), ("down", 11008, 4096)]
 DECODE_M = [1, 8, 32]
 # DRAM traffic / algorithmic bytes of k_linear_rows, from one ncu capture of
-# the M=1 fused-QKV launch (profiles/k_linear_rows_m1_qkv.md): 26,205,952 B
-# read, 0 written, for 26,181,632 algorithmic bytes.  Traffic grows in
-# proportion to the super-blocks a launch streams, so the per-launch traffic
-# is scaled from it.  Reset to None whenever the kernel changes after that
-# capture.
-TRAFFIC_RATIO = 26205952 / 26181632
+# the M=1 fused-QKV launch (profiles/k_linear_rows_m1_qkv.md).  Traffic grows
+# in proportion to the super-blocks a launch streams, so the per-launch
+# traffic is scaled from it.  None until the current kernel is captured.
+TRAFFIC_RATIO = None
 WORKLOAD = "llama7b-decode-linears int4g g128: (K,N) in {(4096,12288),(4096,11008)x2,(11008,4096)} x M in {1,8,32}"
 
 
@@ -311,10 +309,10 @@ def run_gpu(args):
         b = 15 * sum(BYTES_PER_WEIGHT * N * K for (_m, K, N, *_r) in sub)
         per_m[M] = round(b / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
 
-    # roofline of the dominant kernel, k_linear_rows (the M <= 16 calls): a
+    # roofline of the dominant kernel, k_linear_rows (the M <= 8 calls): a
     # graph of just those launches (8 distinct matrices, 192 MB > L2, so every
     # launch streams from HBM), timed with CUDA events on the launching stream
-    rows_calls = [c for c in calls if c[0] <= 16]
+    rows_calls = [c for c in calls if c[0] <= 8]
     g_rows = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_rows, stream=stream):
         launch_all(rows_calls)
@@ -394,7 +392,7 @@ def run_gpu(args):
             "per_M_weight_GBps_untimed": {str(M): v for M, v in per_m.items()},
         },
         "roofline": {
-            "kernel": "k_linear_rows (decode int4g linear, M <= 16): the 8 launches of the step at M in {1, 8}",
+            "kernel": "k_linear_rows (decode int4g linear, M <= 8): the 8 launches of the step at M in {1, 8}",
             "duration": "events around 200 replays of a graph of those 8 launches / launches (PDL-chained)",
             "launch_us": round(rows_launch_s * 1e6, 3),
             "bytes_per_launch": round(rows_algo),

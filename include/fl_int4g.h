@@ -132,13 +132,16 @@ int fl_int4g_unrepack(const void* w, size_t w_bytes, int N, int K, int group,
 int fl_int4g_linear_workspace(int M, int N, int K, size_t* out);
 
 /* y[m, n] = sum_g s16[n,g] * sum_{k in g} x[m,k] * (q[n,k] - z[n,g]),
- * fp32 accumulation, bf16 output (FastLLM page, section 3.1: "read 4-bit
- * weight -> dequantize -> matmul" in one pass).
+ * fp32 accumulation, bf16 output (FastLLM page, section 3.1: the 4-bit
+ * weights are read, dequantized and multiplied in one pass).
  *   x  bf16 [M, K] device, row-major     w  interleaved layout of W [N, K]
  *   y  bf16 [M, N] device, row-major     ws workspace (see conventions)
- * M >= 1.  M <= 32 runs the decode kernel (HBM-streaming, register-level
- * dequantization, split over K across all SMs); larger M runs the prefill
- * kernel.  Reduction order is fixed, so results are deterministic. */
+ * M >= 1.  M <= 8: mma.sync decode kernel (HBM streaming, register-level
+ * dequantization, split over K across the SMs, or per row tile across a
+ * thread-block cluster reduced in distributed shared memory when the row
+ * tiles are few); 8 < M <= 32: tcgen05 decode kernel (dequantized weights in
+ * tensor memory); larger M: persistent tcgen05 prefill GEMM.  Reduction
+ * order is fixed, so results are deterministic. */
 int fl_int4g_linear(const void* x, int M, int K, const void* w, int N,
                     void* y, void* ws, size_t ws_bytes, fl_stream_t stream);
 

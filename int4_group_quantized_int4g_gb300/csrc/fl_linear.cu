@@ -561,8 +561,8 @@ extern "C" int fl_int4g_linear(const void* x, int M, int K, const void* w, int N
   size_t cnt_off, part_off, need;
   if (!tcdec_plan(M, N, K, &cnt_off, &part_off, &need)) return FL_ERR_ARG;
   if (ws_bytes < need) return FL_ERR_WORKSPACE;
-  // M <= 16: the register-dequant mma.sync stream is faster (one warp hand-off
-  // per two super-blocks); 16 < M <= 32: tcgen05 (mma.sync issue-bound there)
-  if (M <= 16) return fl_linear_rows(x, M, K, w, N, y, ws, ws_bytes, s);
+  // M <= 8: the register-dequant mma.sync stream is faster (one warp hand-off
+  // per two super-blocks); 8 < M <= 32: tcgen05 (mma.sync issue-bound there)
+  if (M <= 8) return fl_linear_rows(x, M, K, w, N, y, ws, ws_bytes, s);
   return fl_linear_tcdec(x, M, K, w, N, y, ws, cnt_off, part_off, s);
 }
