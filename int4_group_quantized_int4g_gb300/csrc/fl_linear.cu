@@ -48,6 +48,7 @@ struct RowsParams {
   uint32_t stage_bytes;
   int csize;         // > 1: clusters of csize CTAs split one row tile over K (DSMEM reduction)
   uint32_t red_off;  // shared-memory offset of the cluster reduction barrier and buffer
+  uint32_t zrow_off; // shared-memory offset of 256 zero bytes (x rows of absent tokens)
 };
 
 // CTA c owns units [unit_begin(c), unit_begin(c+1)); cta_of_unit inverts it.
@@ -192,6 +193,96 @@ __device__ __forceinline__ void cluster_reduce(const RowsParams& p, int T, int r
   }
 }
 
+// The consumer warps' stream over their stages.  CL: the CTA is one rank of
+// a cluster sharing a row tile (its range lies inside that tile, group slot
+// = unit index in the range, no tile boundaries); otherwise a stream-K range
+// that may cross row tiles, finished through the ticket hand-off.
+template <int NT, int UPS, bool CL>
+__device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                             const float* xsum, int u0, int u1, int g0, int nslot, int nstage,
+                                             int c, int rank, int warp, int lane, uint64_t* red_bar,
+                                             float* red_buf) {
+  constexpr bool FOLD = NT <= 2;
+  constexpr int Mp = 8 * NT;
+  const uint32_t xoff = UPS * kSbBytes;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int r0 = warp * 16 + gid;
+  const uint8_t* xzero = smem + p.zrow_off;
+  float tot[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) tot[nt][e] = 0.f;
+  int curT = u0 / p.G, g = g0, slot = 0, s = 0, owed0 = -1;
+  uint32_t ph = 0;
+  for (int k = 0; k < nstage; ++k) {
+    const int ua = u0 + k * UPS, n = min(UPS, u1 - ua);
+    if (!mbar_wait(&full[s], ph)) {
+      if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 2);
+      // rank 0 of a cluster stays until its peers' DSMEM writes have landed
+      if (CL && rank == 0) mbar_wait_cluster(red_bar, 0);
+      return;
+    }
+    const uint8_t* sb = smem + static_cast<size_t>(s) * p.stage_bytes;
+    float acc[UPS][NT][4];
+    float sc[UPS][2];
+    uint32_t zr[UPS][2];
+    // Every slot of the stage is computed, in one basic block so that the
+    // compiler interleaves the independent MMA chains; a slot past the end
+    // of the range holds stale shared memory and its result is dropped.
+#pragma unroll
+    for (int i = 0; i < UPS; ++i)
+      unit_dot<NT, FOLD, true>(sb + i * kSbBytes, sb + xoff + i * p.M * kXRowStride, p.M, r0, gid, tig, acc[i],
+                               sc[i][0], sc[i][1], zr[i][0], zr[i][1], NT, xzero);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+    for (int i = 0; i < UPS; ++i) {
+      if (i < n) {
+        const int sl = CL ? k * UPS + i : (slot < nslot ? slot : 0);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float2 xs = make_float2(0.f, 0.f);
+          if (FOLD) xs = *reinterpret_cast<const float2*>(xsum + sl * Mp + nt * 8 + 2 * tig);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float v = acc[i][nt][e];
+            // 128 + z as a float without a conversion: z in the mantissa of 128.0
+            if (FOLD) v = fmaf(-__uint_as_float(0x43000000u + (zr[i][e >> 1] << 16)), (e & 1) ? xs.y : xs.x, v);
+            tot[nt][e] = fmaf(sc[i][e >> 1], v, tot[nt][e]);
+          }
+        }
+        if (!CL) {
+          ++slot;
+          if (++g == p.G) {
+            g = 0;
+            if (ua + i + 1 < u1) {
+              // row tile finished inside this CTA's range: store it now,
+              // take its ticket after the stream
+              if (store_tile<NT>(p, curT, c, u0, u1, warp, lane, tot)) owed0 = curT;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) tot[nt][e] = 0.f;
+              ++curT;
+            }
+          }
+          if (slot == nslot) slot = 0;
+        }
+      }
+    }
+    if (++s == p.stages) s = 0, ph ^= 1u;
+  }
+  if (CL) {
+    cluster_reduce<NT>(p, curT, rank, warp, lane, tot, red_bar, red_buf);
+    return;
+  }
+  const bool owed1 = store_tile<NT>(p, curT, c, u0, u1, warp, lane, tot);
+  // only the first and the last row tile of a CTA's range can be partial
+  if (owed0 >= 0) ticket_tile<NT>(p, owed0, warp, lane);
+  if (owed1) ticket_tile<NT>(p, curT, warp, lane);
+}
+
 // NT token tiles of 8; UPS super-blocks per pipeline stage (2 gives each
 // warp two independent MMA chains and 17 KB bulk copies).  One CTA per SM,
 // sized to leave room for the next kernel's CTA (programmatic launch), which
@@ -232,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) k_linear_rows(const
     if (p.csize > 1) mbar_init(red_bar, (p.csize - 1) * kConsumerWarps);
     fence_mbar_init();
   }
+  if (threadIdx.x < 16) reinterpret_cast<uint4*>(smem + p.zrow_off)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
   // rank 0's reduction barrier is initialised before any peer can arrive on it
   if (p.csize > 1) cluster_sync_all();
@@ -290,109 +382,59 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) k_linear_rows(const
   // (they read x and write y and the workspace: only once the previous kernel is done)
   pdl_wait();
   if (FOLD) {
-    // per-group token sums of x for this CTA's groups: one thread per
-    // (group slot, token), its 16 loads in flight at once, summed in k order
-    for (int idx = threadIdx.x; idx < nslot * Mp; idx += kConsumerWarps * 32) {
-      const int i = idx / Mp, m = idx - i * Mp;
+    // Per-group token sums of x for this CTA's groups, [slot][Mp]: four
+    // neighbouring threads per (group slot, token < M), 32 values each in
+    // four independent chains, then two shuffles (a fixed order:
+    // deterministic).  The thread count is rounded up to whole warps so
+    // that every lane of a warp runs the shuffles; tokens M..Mp-1 get 0.
+    const int items = nslot * p.M;
+    const int nthr = (items * 4 + 31) & ~31;
+    for (int idx = threadIdx.x; idx < nthr; idx += kConsumerWarps * 32) {
+      const int it = idx >> 2, part = idx & 3;
       float v = 0.f;
-      if (m < p.M) {
+      if (it < items) {
+        const int i = it / p.M, m = it - i * p.M;
         int g = g0 + i;
         if (g >= p.G) g -= p.G;
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K + g * kGroup);
-        uint4 q[16];
+        const uint4* src =
+            reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K + g * kGroup) + part * 4;
+        uint4 q[4];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) q[t] = __ldg(src + t);
+        for (int t = 0; t < 4; ++t) q[t] = __ldg(src + t);
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
+        for (int t = 0; t < 4; ++t) {
           const uint32_t w4[4] = {q[t].x, q[t].y, q[t].z, q[t].w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            v += __uint_as_float(w4[h] << 16);
-            v += __uint_as_float(w4[h] & 0xffff0000u);
+            a[h] += __uint_as_float(w4[h] << 16);
+            a[h] += __uint_as_float(w4[h] & 0xffff0000u);
           }
         }
+        v = (a[0] + a[1]) + (a[2] + a[3]);
       }
-      xsum[idx] = v;
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if (part == 0 && it < items) xsum[(it / p.M) * Mp + it % p.M] = v;
+    }
+    for (int idx = threadIdx.x; idx < nslot * (Mp - p.M); idx += kConsumerWarps * 32) {
+      const int i = idx / (Mp - p.M), m = p.M + idx - i * (Mp - p.M);
+      xsum[i * Mp + m] = 0.f;
     }
     named_bar(1, kConsumerWarps * 32);
   }
-  const int gid = lane >> 2, tig = lane & 3;
-  const int r0 = warp * 16 + gid;
-  float tot[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) tot[nt][e] = 0.f;
-  int curT = u0 / p.G, g = g0, slot = 0, s = 0, owed0 = -1;
-  uint32_t ph = 0;
-  for (int k = 0; k < nstage; ++k) {
-    const int ua = u0 + k * UPS, n = min(UPS, u1 - ua);
-    if (!mbar_wait(&full[s], ph)) {
-      if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 2);
-      // rank 0 of a cluster stays until its peers' DSMEM writes have landed
-      if (p.csize > 1 && rank == 0) mbar_wait_cluster(red_bar, 0);
-      return;
-    }
-    const uint8_t* sb = smem + static_cast<size_t>(s) * p.stage_bytes;
-    float acc[UPS][NT][4];
-    float sc[UPS][2];
-    uint32_t zr[UPS][2];
-    // Every slot of the stage is computed, in one basic block so that the
-    // compiler interleaves the independent MMA chains; a slot past the end
-    // of the range holds stale shared memory and its result is dropped.
-#pragma unroll
-    for (int i = 0; i < UPS; ++i)
-      unit_dot<NT, FOLD>(sb + i * kSbBytes, sb + xoff + i * p.M * kXRowStride, p.M, r0, gid, tig, acc[i],
-                         sc[i][0], sc[i][1], zr[i][0], zr[i][1]);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-    for (int i = 0; i < UPS; ++i) {
-      if (i < n) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float2 xs = make_float2(0.f, 0.f);
-          if (FOLD) xs = *reinterpret_cast<const float2*>(xsum + (slot < nslot ? slot : 0) * Mp + nt * 8 + 2 * tig);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float v = acc[i][nt][e];
-            if (FOLD) v = fmaf(-static_cast<float>(128u + zr[i][e >> 1]), (e & 1) ? xs.y : xs.x, v);
-            tot[nt][e] = fmaf(sc[i][e >> 1], v, tot[nt][e]);
-          }
-        }
-        ++slot;
-        if (++g == p.G) {
-          g = 0;
-          if (ua + i + 1 < u1) {
-            // row tile finished inside this CTA's range: store it now,
-            // take its ticket after the stream
-            if (store_tile<NT>(p, curT, c, u0, u1, warp, lane, tot)) owed0 = curT;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) tot[nt][e] = 0.f;
-            ++curT;
-          }
-        }
-        if (slot == nslot) slot = 0;
-      }
-    }
-    if (++s == p.stages) s = 0, ph ^= 1u;
-  }
-  if (p.csize > 1) {
-    cluster_reduce<NT>(p, curT, rank, warp, lane, tot, red_bar, red_buf);
-    return;
-  }
-  const bool owed1 = store_tile<NT>(p, curT, c, u0, u1, warp, lane, tot);
-  // only the first and the last row tile of a CTA's range can be partial
-  if (owed0 >= 0) ticket_tile<NT>(p, owed0, warp, lane);
-  if (owed1) ticket_tile<NT>(p, curT, warp, lane);
+  if (p.csize > 1)
+    rows_consume<NT, UPS, true>(p, smem, full, empty, xsum, u0, u1, g0, nslot, nstage, c, rank, warp, lane,
+                                red_bar, red_buf);
+  else
+    rows_consume<NT, UPS, false>(p, smem, full, empty, xsum, u0, u1, g0, nslot, nstage, c, rank, warp, lane,
+                                 red_bar, red_buf);
 }
 
 // ------------------------------------------------------------------ plan
 struct RowsPlan {
   int T, G, P, NT, ups, stages, U, csize;
-  uint32_t stage_bytes, red_off;
+  uint32_t stage_bytes, red_off, zrow_off;
   size_t smem, cnt_off, part_off, ws_bytes;
 };
 
@@ -435,6 +477,8 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl) {
   const int nslot = units_max < pl->G ? units_max : pl->G;
   pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes + 2 * pl->stages * sizeof(uint64_t) +
              static_cast<size_t>(nslot) * 8 * pl->NT * sizeof(float);
+  pl->zrow_off = static_cast<uint32_t>(align_up(pl->smem, 16));
+  pl->smem = pl->zrow_off + 256;
   pl->red_off = static_cast<uint32_t>(align_up(pl->smem, 16));
   if (red_bytes) pl->smem = pl->red_off + red_bytes;
   pl->cnt_off = kTicketOff;
@@ -505,6 +549,7 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   prm.stage_bytes = pl.stage_bytes;
   prm.csize = pl.csize;
   prm.red_off = pl.red_off;
+  prm.zrow_off = pl.zrow_off;
   switch (pl.NT) {
     case 1: return launch_rows<1, 2>(pl, prm, stream);
     case 2: return launch_rows<2, 2>(pl, prm, stream);

@@ -21,11 +21,15 @@ constexpr int kXRowStride = 320;  // 256 B of x per staged row + 64 B pad: confl
 //
 // FOLD: the (128+q) codes go to the MMA as they are; the caller removes
 // (128+z) * sum_k x[m,k] per row and token, instead of a bf16 subtract per
-// pair on the ALU.  Two accumulator chains halve the dependent-MMA latency.
-template <int NT, bool FOLD>
+// pair on the ALU.  One accumulator chain per super-block: the callers keep
+// two super-blocks in flight per warp, which covers the MMA latency, and a
+// second chain would cost a merge and its own zeroing per super-block.
+// ZROW: lanes whose token m >= M read their B fragment from `xzero` (256
+// zero bytes in shared memory) instead of zero-filling registers per step.
+template <int NT, bool FOLD, bool ZROW = false>
 __device__ __forceinline__ void unit_dot(const uint8_t* sb, const uint8_t* sx, int M, int r0, int gid, int tig,
                                          float (&acc)[NT][4], float& s0, float& s1, uint32_t& z0, uint32_t& z1,
-                                         int ntiles = NT) {
+                                         int ntiles = NT, const uint8_t* xzero = nullptr) {
   // chunk tig of rows r0 and r0+8 (both rotated by (r0/2)%4 in the layout)
   const int pos = ((tig + (r0 >> 1)) & 3) * 16;
   const uint4 wa = *reinterpret_cast<const uint4*>(sb + r0 * 64 + pos);
@@ -37,11 +41,16 @@ __device__ __forceinline__ void unit_dot(const uint8_t* sb, const uint8_t* sx, i
   z0 = (sb[kSbNib + kSbScale + (r0 >> 1)] >> zsh) & 15u;
   z1 = (sb[kSbNib + kSbScale + (r0 >> 1) + 4] >> zsh) & 15u;
   const uint32_t zz0 = bf16_bias_pair(z0), zz1 = bf16_bias_pair(z1);
-  float acc2[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f, acc2[nt][e] = 0.f;
+    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+  const uint8_t* xrow[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int m = nt * 8 + gid;
+    xrow[nt] = (!ZROW || m < M) ? sx + m * kXRowStride : xzero;
+  }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t qa = (&wa.x)[j], qb = (&wb.x)[j];
@@ -59,21 +68,17 @@ __device__ __forceinline__ void unit_dot(const uint8_t* sb, const uint8_t* sx, i
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int m = nt * 8 + gid;
-      xv[nt] = m < M ? *reinterpret_cast<const uint4*>(sx + m * kXRowStride + (4 * j + tig) * 16)
-                     : make_uint4(0u, 0u, 0u, 0u);
+      xv[nt] = (ZROW || m < M) ? *reinterpret_cast<const uint4*>(xrow[nt] + (4 * j + tig) * 16)
+                               : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       if (nt == 0 || nt < ntiles) {   // token tiles past the last token are all zero: skipped
         mma_bf16_16816(acc[nt], a[0], b[0], a[1], b[1], xv[nt].x, xv[nt].y);
-        mma_bf16_16816(acc2[nt], a[2], b[2], a[3], b[3], xv[nt].z, xv[nt].w);
+        mma_bf16_16816(acc[nt], a[2], b[2], a[3], b[3], xv[nt].z, xv[nt].w);
       }
     }
   }
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
 }
 
 }  // namespace fl
