@@ -18,6 +18,8 @@
 //  * a row tile split across CTAs is reduced by the last CTA to finish it
 //    (atomic ticket, no waiting), summing the partials in CTA order so the
 //    result is deterministic.
+#include <mutex>
+
 #include "fl_common.cuh"
 #include "fl_rows.cuh"
 
@@ -284,11 +286,12 @@ __device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem,
 }
 
 // NT token tiles of 8; UPS super-blocks per pipeline stage (2 gives each
-// warp two independent MMA chains and 17 KB bulk copies).  One CTA per SM,
-// sized to leave room for the next kernel's CTA (programmatic launch), which
-// prefetches its weights while this one computes.
-template <int NT, int UPS>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) k_linear_rows(const RowsParams p) {
+// warp two independent MMA chains and 17 KB bulk copies).  MINB CTAs per SM:
+// 2 (M <= 8, ~100 KB of stages each), 3 (M <= 8 when the row tiles' clusters
+// would fill the GPU's cluster capacity at 2: smaller stages, fewer
+// registers, so that every cluster is resident in one wave) or 1 (M > 8).
+template <int NT, int UPS, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams p) {
   constexpr bool FOLD = NT <= 2;
   constexpr int Mp = 8 * NT;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -433,14 +436,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) k_linear_rows(const
 
 // ------------------------------------------------------------------ plan
 struct RowsPlan {
-  int T, G, P, NT, ups, stages, U, csize;
+  int T, G, P, NT, ups, stages, U, csize, minb;
   uint32_t stage_bytes, red_off, zrow_off;
   size_t smem, cnt_off, part_off, ws_bytes;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl) {
+// minb: CTAs per SM the kernel is built for (0 = the default for M).
+bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0) {
   if (M < 1 || M > kMaxTokens || N < 1 || K < kGroup || K % kGroup || sms < 1) return false;
   if ((N + kRowTile - 1) / kRowTile > kMaxRowTiles) return false;
   pl->T = (N + kRowTile - 1) / kRowTile;
@@ -450,6 +454,8 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl) {
   pl->U = static_cast<int>(U);
   pl->NT = (M + 7) / 8;
   pl->ups = pl->NT <= 2 ? 2 : 1;
+  pl->minb = minb > 0 ? minb : (pl->NT == 1 ? 2 : 1);
+  if (pl->NT > 1) pl->minb = 1;
   // M <= 8: two CTAs per SM (four consumer warps per scheduler)
   const long long slots = static_cast<long long>(sms) * (pl->NT == 1 ? 2 : 1);
   // Few row tiles: clusters of csize CTAs share each tile, split over K, and
@@ -470,7 +476,7 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl) {
       pl->csize > 1 ? 16 + static_cast<size_t>(pl->csize - 1) * kConsumerWarps * 32 * 4 * pl->NT * sizeof(float) : 0;
   pl->stage_bytes = static_cast<uint32_t>(
       align_up(static_cast<size_t>(pl->ups) * (kSbBytes + static_cast<size_t>(M) * kXRowStride), 128));
-  const size_t budget = (pl->NT == 1 ? 100u * 1024u : 200u * 1024u) - red_bytes;
+  const size_t budget = (pl->minb == 3 ? 66u * 1024u : pl->minb == 2 ? 100u * 1024u : 200u * 1024u) - red_bytes;
   int stages = static_cast<int>(budget / pl->stage_bytes);
   pl->stages = stages > 12 ? 12 : (stages < 2 ? 2 : stages);
   const int units_max = pl->csize > 1 ? (pl->G + pl->csize - 1) / pl->csize : (pl->U + pl->P - 1) / pl->P;
@@ -487,17 +493,58 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl) {
   return true;
 }
 
-template <int NT, int UPS>
-int launch_rows(const RowsPlan& pl, const RowsParams& prm, cudaStream_t s) {
+template <int NT, int UPS, int MINB>
+bool rows_attr(int dev) {
   static bool attr_done[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(k_linear_rows<NT, UPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (dev < 0 || dev >= 64) return false;
+  if (!attr_done[dev]) {
+    if (cudaFuncSetAttribute(k_linear_rows<NT, UPS, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              227 * 1024) != cudaSuccess)
-      return FL_ERR_CUDA;
+      return false;
     attr_done[dev] = true;
   }
+  return true;
+}
+
+// How many clusters of pl.csize CTAs of the two-per-SM kernel (with pl.smem
+// bytes each) the GPU holds at once; cached per device, cluster size and
+// shared-memory size.  -1 when the query fails.
+int rows_cluster_capacity(const RowsPlan& pl) {
+  struct Entry { int dev, csize; size_t smem; int cap; };
+  static Entry cache[64];
+  static int n = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (cache[i].dev == dev && cache[i].csize == pl.csize && cache[i].smem == pl.smem) return cache[i].cap;
+  if (!rows_attr<1, 2, 2>(dev)) return -1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.P);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(pl.csize);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int cap = -1;
+  if (cudaOccupancyMaxActiveClusters(&cap, k_linear_rows<1, 2, 2>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    cap = -1;
+  }
+  if (n < 64) cache[n++] = Entry{dev, pl.csize, pl.smem, cap};
+  return cap;
+}
+
+template <int NT, int UPS, int MINB>
+int launch_rows(const RowsPlan& pl, const RowsParams& prm, cudaStream_t s) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!rows_attr<NT, UPS, MINB>(dev)) return FL_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.P);
   cfg.blockDim = dim3(kThreads);
@@ -512,7 +559,7 @@ int launch_rows(const RowsPlan& pl, const RowsParams& prm, cudaStream_t s) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pl.csize > 1 ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, k_linear_rows<NT, UPS>, prm) != cudaSuccess) return FL_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, k_linear_rows<NT, UPS, MINB>, prm) != cudaSuccess) return FL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
@@ -531,6 +578,14 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   RowsPlan pl;
   if (!make_rows_plan(M, N, K, flh::sm_count(), &pl)) return FL_ERR_ARG;
   if (ws_bytes < pl.ws_bytes) return FL_ERR_WORKSPACE;
+  // Clusters that would fill the GPU's cluster capacity leave some of them
+  // waiting for a second wave whenever the previous kernel's exits fragment
+  // the free slots: such shapes run three smaller CTAs per SM instead (same
+  // grid, same workspace), which has capacity to spare.
+  if (pl.NT == 1 && pl.csize > 1) {
+    const int cap = rows_cluster_capacity(pl);
+    if (cap > 0 && pl.T > cap - 2 && !make_rows_plan(M, N, K, flh::sm_count(), &pl, 3)) return FL_ERR_ARG;
+  }
   RowsParams prm;
   prm.w = static_cast<const uint8_t*>(w);
   prm.x = static_cast<const __nv_bfloat16*>(x);
@@ -551,10 +606,10 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   prm.red_off = pl.red_off;
   prm.zrow_off = pl.zrow_off;
   switch (pl.NT) {
-    case 1: return launch_rows<1, 2>(pl, prm, stream);
-    case 2: return launch_rows<2, 2>(pl, prm, stream);
-    case 3: return launch_rows<3, 1>(pl, prm, stream);
-    default: return launch_rows<4, 1>(pl, prm, stream);
+    case 1: return pl.minb == 3 ? launch_rows<1, 2, 3>(pl, prm, stream) : launch_rows<1, 2, 2>(pl, prm, stream);
+    case 2: return launch_rows<2, 2, 1>(pl, prm, stream);
+    case 3: return launch_rows<3, 1, 1>(pl, prm, stream);
+    default: return launch_rows<4, 1, 1>(pl, prm, stream);
   }
 }
 
