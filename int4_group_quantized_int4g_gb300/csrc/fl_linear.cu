@@ -4,20 +4,22 @@
 // x one group) stream from HBM once.  FastLLM page, section 3.1: decode is
 // memory-bound, so the 4-bit codes are read once and dequantized on the fly
 // inside the matmul.  GB300 design:
-//  * work = the T*G super-blocks in layout order, split into P contiguous
-//    ranges, one per CTA (P = number of SMs), so every SM streams the same
-//    number of bytes whatever N and K are (split over K inside a row tile);
+//  * work = the T*G super-blocks.  Few row tiles: one thread-block cluster
+//    per tile, its CTAs splitting the tile's groups (K), partial sums added
+//    in rank 0's shared memory through distributed shared memory.  Many row
+//    tiles: equal contiguous ranges of super-blocks, one per CTA (stream-K),
+//    a tile shared by several CTAs finished by the last one to take its
+//    ticket (no waiting; partials summed in CTA order, deterministic);
 //  * one producer warp moves super-blocks and the matching 256-byte slices of
 //    every token row of x into a ring of shared-memory stages with 1-D bulk
-//    copies completing on mbarriers;
+//    copies completing on mbarriers; the weights of the first stages are
+//    requested before the wait on the previous kernel (programmatic launch);
 //  * 8 consumer warps each own 16 rows: 16 bytes of codes per lane and row
-//    become 8 exact (q - z) bf16 pairs with one LOP3 + one bf16x2 subtract per
-//    pair, feeding mma.sync m16n8k16 as the A operand (the K order inside a
-//    group is permuted consistently for A and B, which leaves the dot product
-//    unchanged); the per-group fp16 scale is applied to the fp32 group sum;
-//  * a row tile split across CTAs is reduced by the last CTA to finish it
-//    (atomic ticket, no waiting), summing the partials in CTA order so the
-//    result is deterministic.
+//    become 8 bf16 pairs (128 + q) with one LOP3 each, the A operand of
+//    mma.sync m16n8k16 (the K order inside a group is permuted consistently
+//    for A and B, which leaves the dot product unchanged); (128 + z) times
+//    the group's sum of x is subtracted afterwards and the fp16 scale
+//    applied to the fp32 group sum (M <= 16; larger M subtracts z per pair).
 #include <mutex>
 
 #include "fl_common.cuh"
