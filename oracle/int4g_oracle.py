@@ -25,6 +25,10 @@ What it computes, and where it comes from:
   |y| > 0.51 * sum_k |x||w'|).
 * the tile-interleaved weight layout ("按组重排 ... 连续内存", same section):
   an invertible byte/nibble permutation, restated here from its definition.
+  Its super-blocks always span 128 columns.  Groups of 256 (same page,
+  section 4.2 "模型转换与格式说明": --group-size defaults to 128 and may be
+  raised to 256) are stored as two consecutive super-blocks that carry the
+  same scale and zero point; the dequantized weights are unchanged.
 * the routed MoE expert FFN with int4g experts -- fastllm README (gittoolsai
   mirror), "2. 如何设定推理精度" (--moe_dtype int4g) and "5. 其它参数"
   (--moe_experts = top-k, --cuda_se = shared expert): top-k routing,
@@ -43,6 +47,7 @@ from __future__ import annotations
 import numpy as np
 
 GROUP = 128          # weights per group along K (FastLLM page, section 3.1)
+GROUPS = (128, 256)  # group sizes of the layout (section 4.2: 128 by default, 256 allowed)
 QMAX = 15            # 4-bit codes 0..15
 ROW_TILE = 128       # rows per super-block of the interleaved layout
 SB_NIB = 8192        # nibble bytes per super-block: 128 rows x 64 B
@@ -258,8 +263,23 @@ def linear_columns(x, Q, S, Z, cols, group=GROUP):
 # --------------------------------------------------------------------------
 
 def tiled_bytes(N, K, group=GROUP):
+    """Bytes of the interleaved layout: one 8512-byte super-block per 128
+    rows x 128 columns, whatever the group size."""
+    if group not in GROUPS or K % group:
+        raise ValueError("the interleaved layout takes groups of 128 or 256 and K % group == 0")
     Np = -(-N // ROW_TILE) * ROW_TILE
-    return (Np // ROW_TILE) * (K // group) * SB_BYTES
+    return (Np // ROW_TILE) * (K // GROUP) * SB_BYTES
+
+
+def expand_groups(S, Z, group):
+    """Scales and zero points of a triple with `group` columns per group,
+    restated per 128 columns: each group's entry repeated group/128 times
+    (the dequantized weights are the same, dequantize() of both agree)."""
+    r = group // GROUP
+    G = S.shape[1]
+    S128 = np.repeat(np.asarray(S, np.uint16), r, axis=1)
+    Z128 = pack_zeros(np.repeat(unpack_zeros(Z, G), r, axis=1))
+    return S128, Z128
 
 
 def _nibble_address(kk, r):
@@ -290,9 +310,15 @@ def repack(Q, S, Z, N, K, group=GROUP):
     columns placed by _nibble_address(kk, r)), then 128 fp16 scales (row r at
     8192 + 2r, little endian), then 128 zero points (row r in byte
     8448 + r//2, low nibble = even r).  Rows past N are zero.
+
+    group 256: the super-blocks still span 128 columns; both super-blocks of
+    a group carry that group's scale and zero point (expand_groups).
     """
+    if group not in GROUPS or K % group:
+        raise ValueError("the interleaved layout takes groups of 128 or 256 and K % group == 0")
     if group != GROUP:
-        raise ValueError("the interleaved layout is defined for group 128")
+        S, Z = expand_groups(S, Z, group)
+        group = GROUP
     G = K // group
     Np = -(-N // ROW_TILE) * ROW_TILE
     q = np.zeros((Np, K), np.uint8)
@@ -323,7 +349,15 @@ def repack(Q, S, Z, N, K, group=GROUP):
 
 
 def unrepack(buf, N, K, group=GROUP):
-    """Inverse of repack(): interleaved bytes -> canonical (Q, S, Z)."""
+    """Inverse of repack(): interleaved bytes -> canonical (Q, S, Z).
+    group 256: the scale and zero point of each group are read from its
+    first super-block."""
+    if group not in GROUPS or K % group:
+        raise ValueError("the interleaved layout takes groups of 128 or 256 and K % group == 0")
+    if group != GROUP:
+        Q, S, Z = unrepack(buf, N, K, GROUP)
+        r = group // GROUP
+        return Q, S[:, ::r].copy(), pack_zeros(unpack_zeros(Z, K // GROUP)[:, ::r])
     G = K // group
     Np = -(-N // ROW_TILE) * ROW_TILE
     buf = np.asarray(buf, np.uint8)

@@ -96,7 +96,7 @@ def _edge_matrix():
     return W
 
 
-@pytest.mark.parametrize("group", [128, 8, 4])
+@pytest.mark.parametrize("group", [256, 128, 8, 4])
 def test_vectorised_quantizer_equals_group_loop(group):
     for W in (_edge_matrix(), (np.random.default_rng([0, 42]).standard_normal((17, 256)) * 0.02).astype(np.float32)):
         a = O.quantize(W, group)
@@ -132,7 +132,7 @@ def _on_grid(rng, N, K, group):
     return W.astype(np.float32), s16, z, q.reshape(N, K)
 
 
-@pytest.mark.parametrize("group", [128, 8])
+@pytest.mark.parametrize("group", [256, 128, 8])
 def test_on_grid_weights_reconstruct_exactly(group):
     rng = np.random.default_rng([0, 7, group])
     W, s16, z, q = _on_grid(rng, 6, 4 * group, group)
@@ -271,6 +271,58 @@ def test_repack_roundtrip_and_reader():
     ref = O.dequantize(Q, S, Z)
     got = _brute_tiled_dequant(buf, N, K)
     assert np.array_equal(got[sub], ref[sub])
+
+
+def test_group256_hand_bytes():
+    """Groups of 256 (FastLLM page, section 4.2): super-blocks still span 128
+    columns, and both super-blocks of a group carry its scale and zero point.
+    N=128, K=256: one group per row, super-blocks (0,0) at 0 and (0,1) at
+    8512.  Column 129 of row 0 is kk=1 of super-block 1: byte 8512+2, low
+    nibble (worked as in test_repack_hand_bytes).  Row 3's scale 0x1234 sits
+    at 8192+6 (little endian) in both; row 5's zero 11 in byte 8448+2, high
+    nibble, in both."""
+    N, K = 128, 256
+    q = np.zeros((N, K), np.uint8)
+    q[0, 129] = 6
+    S = np.zeros((N, 1), np.uint16)
+    S[3, 0] = 0x1234
+    z = np.zeros((N, 1), np.uint8)
+    z[5, 0] = 11
+    buf = O.repack(O.pack_codes(q), S, O.pack_zeros(z), N, K, 256)
+    assert buf.size == O.tiled_bytes(N, K, 256) == O.tiled_bytes(N, K, 128) == 2 * 8512
+    expect = {8512 + 2: 0x06}
+    for base in (0, 8512):
+        expect[base + 8192 + 6] = 0x34
+        expect[base + 8192 + 7] = 0x12
+        expect[base + 8448 + 2] = 0xB0
+    for addr, val in expect.items():
+        assert buf[addr] == val, (addr, buf[addr], val)
+    assert set(np.nonzero(buf)[0].tolist()) == set(expect)
+
+
+def test_group256_roundtrip_and_reader():
+    rng = np.random.default_rng([0, 12])
+    N, K = 136, 512   # a full tile + a ragged tail, two groups of 256
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    Q, S, Z = O.quantize(W, 256)
+    assert S.shape == (N, 2) and Z.shape == (N, 1)
+    buf = O.repack(Q, S, Z, N, K, 256)
+    Q2, S2, Z2 = O.unrepack(buf, N, K, 256)
+    assert np.array_equal(Q, Q2) and np.array_equal(S, S2) and np.array_equal(Z, Z2)
+    sub = [0, 5, 127, 128, 135]
+    got = _brute_tiled_dequant(buf, N, K)   # reads per 128-column super-block
+    assert np.array_equal(got[sub], O.dequantize(Q, S, Z, 256)[sub])
+    # the same weights through groups of 128 with the scales repeated
+    S128, Z128 = O.expand_groups(S, Z, 256)
+    assert np.array_equal(O.dequantize(Q, S128, Z128, 128), O.dequantize(Q, S, Z, 256))
+    x = rng.standard_normal((3, K))
+    assert np.array_equal(O.linear(x, Q, S, Z, 256), O.linear(x, Q, S128, Z128, 128))
+
+
+def test_layout_rejects_other_groups():
+    for group, K in ((64, 256), (256, 384), (512, 512)):
+        with pytest.raises(ValueError):
+            O.tiled_bytes(128, K, group)
 
 
 def test_byte_count_per_weight():
