@@ -15,11 +15,14 @@
  * ---------------------------------------
  *  - W is [N, K] in nn.Linear order; y = x . deq(W)^T; x is [M, K] bf16,
  *    row-major, y is [M, N] bf16, row-major.
- *  - group must be 128 (the only group size the GPU kernels accept);
- *    K % 128 == 0.
- *  - Canonical int4g triple (the storage the quantizer produces):
+ *  - group is 128 or 256 (FastLLM page, section 4.2: --group-size 128 by
+ *    default, 256 allowed) and K % group == 0.  Only the quantizer, the
+ *    repack and the unrepack take it: the matmul entry points read the
+ *    interleaved layout, whose super-blocks span 128 columns whatever the
+ *    group size.
+ *  - Canonical int4g triple (the storage the quantizer produces), G = K/group:
  *      q      uint8  [N, K/2]        codes 0..15, low nibble = even k
- *      scales uint16 [N, K/128]      IEEE fp16 bit patterns
+ *      scales uint16 [N, G]          IEEE fp16 bit patterns
  *      zeros  uint8  [N, ceil(G/2)]  zero points 0..15, low nibble = even g
  *    Dequantized weight: w' = s16 * (q - z).
  *  - Interleaved ("tiled") layout used by the matmul kernels, produced by
@@ -37,6 +40,8 @@
  *      [8192, 8448)  128 fp16 scales, row r at 8192 + 2r (little endian);
  *      [8448, 8512)  128 zero points, row r in byte 8448 + r/2, low nibble
  *                    for even r.
+ *    With groups of 256, super-blocks (T, 2j) and (T, 2j+1) both carry the
+ *    scales and zero points of group j.
  *    Size: 0.51953125 bytes per weight (the same as the canonical triple),
  *    plus padding rows.  Each super-block is one contiguous bulk copy.
  *  - All device pointers must be 16-byte aligned.
@@ -69,7 +74,7 @@ typedef struct CUstream_st* fl_stream_t; /* same object as cudaStream_t */
 #define FL_OK               0
 #define FL_ERR_ARG          1  /* null/misaligned pointer, bad size, K % 128 != 0, ... */
 #define FL_ERR_WORKSPACE    2  /* workspace smaller than the *_workspace query */
-#define FL_ERR_UNSUPPORTED  3  /* group != 128, shape beyond a kernel limit */
+#define FL_ERR_UNSUPPORTED  3  /* group not 128 or 256, shape beyond a kernel limit */
 #define FL_ERR_CUDA         4  /* a CUDA launch or query failed */
 #define FL_ERR_TIMEOUT      5  /* a device-side bounded wait ran out (status word) */
 #define FL_ERR_DEVICE_CHECK 6  /* a device-side check failed (status word) */
@@ -96,7 +101,7 @@ int fl_int4g_status(void* ws, fl_stream_t stream, int* out);
 
 /* Online int4g quantization of fp32 weights w [N, K] (device) into the
  * canonical triple (device buffers q, scales, zeros as above).  Per group of
- * 128 along K, in double precision:
+ * `group` (128 or 256) weights along K, in double precision:
  *   s = (max - min)/15, s16 = fp16(s) (nearest even),
  *   z = clamp(round(-min/s16), 0, 15), q = clamp(round(w/s16) + z, 0, 15),
  * round = half away from zero; a constant group c uses the range
@@ -111,7 +116,8 @@ int fl_int4g_quantize(const float* w, int N, int K, int group,
 
 /* ------------------------------------------------------------ a2: repack */
 
-/* Bytes of the interleaved layout for an [N, K] matrix (group 128). */
+/* Bytes of the interleaved layout for an [N, K] matrix (the same for groups
+ * of 128 and 256: 8512 bytes per 128 rows x 128 columns). */
 int fl_int4g_repacked_bytes(int N, int K, int group, size_t* out);
 
 /* Canonical triple -> interleaved layout (FastLLM page, section 3.1:

@@ -5,6 +5,10 @@
 // that every code decision is taken in one fixed precision:
 //   s = (max - min)/15, s16 = fp16(s), z = clamp(round(-min/s16), 0, 15),
 //   q = clamp(round(w/s16) + z, 0, 15), round = half away from zero.
+// Groups of 256 (same page, section 4.2: --group-size 128 by default, 256
+// allowed) are quantized by the same rule; in the interleaved layout, whose
+// super-blocks always span 128 columns, both super-blocks of a group carry
+// its scale and zero point, so every matmul kernel reads them unchanged.
 #include "fl_common.cuh"
 
 using namespace fl;
@@ -19,9 +23,13 @@ __device__ __forceinline__ double round_half_away(double v) {
 
 __device__ __forceinline__ int clamp15(double v) { return v < 0.0 ? 0 : (v > 15.0 ? 15 : static_cast<int>(v)); }
 
-// One warp per (row n, pair of groups 2gp, 2gp+1): the pair shares a zero byte.
+// One warp per (row n, pair of groups 2gp, 2gp+1): the pair shares a zero
+// byte.  GRP/32 consecutive weights per lane.
+template <int GRP>
 __global__ void k_quantize(const float* __restrict__ w, int N, int K, int G, uint8_t* __restrict__ q,
                            uint16_t* __restrict__ sc, uint8_t* __restrict__ zr, int32_t* __restrict__ status) {
+  constexpr int V = GRP / 32;   // 4 or 8
+  static_assert(V == 4 || V == 8, "groups of 128 or 256");
   const int lane = threadIdx.x & 31;
   const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int GP = (G + 1) / 2;
@@ -32,10 +40,21 @@ __global__ void k_quantize(const float* __restrict__ w, int N, int K, int G, uin
   for (int h = 0; h < 2; ++h) {
     const int g = 2 * gp + h;
     if (g >= G) break;
-    const float4 v = *reinterpret_cast<const float4*>(w + static_cast<size_t>(n) * K + g * kGroup + 4 * lane);
-    float mn = fminf(fminf(v.x, v.y), fminf(v.z, v.w));
-    float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-    int bad = isnan(v.x) | isnan(v.y) | isnan(v.z) | isnan(v.w);
+    float vv[V];
+#pragma unroll
+    for (int c = 0; c < V / 4; ++c) {
+      const float4 v4 =
+          *reinterpret_cast<const float4*>(w + static_cast<size_t>(n) * K + static_cast<size_t>(g) * GRP + V * lane + 4 * c);
+      vv[4 * c] = v4.x, vv[4 * c + 1] = v4.y, vv[4 * c + 2] = v4.z, vv[4 * c + 3] = v4.w;
+    }
+    float mn = vv[0], mx = vv[0];
+    int bad = 0;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      mn = fminf(mn, vv[j]);
+      mx = fmaxf(mx, vv[j]);
+      bad |= isnan(vv[j]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
@@ -67,15 +86,17 @@ __global__ void k_quantize(const float* __restrict__ w, int N, int K, int G, uin
     uint32_t packed = 0;
     if (!zero) {
       z = clamp15(round_half_away(-dmn / s16));
-      const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < V; ++j) {
         const int qq = clamp15(round_half_away(static_cast<double>(vv[j]) / s16) + z);
         packed |= static_cast<uint32_t>(qq) << (4 * j);
       }
     }
-    *reinterpret_cast<uint16_t*>(q + static_cast<size_t>(n) * (K / 2) + g * (kGroup / 2) + 2 * lane) =
-        static_cast<uint16_t>(packed);
+    uint8_t* qd = q + static_cast<size_t>(n) * (K / 2) + static_cast<size_t>(g) * (GRP / 2) + (V / 2) * lane;
+    if (V == 4)
+      *reinterpret_cast<uint16_t*>(qd) = static_cast<uint16_t>(packed);
+    else
+      *reinterpret_cast<uint32_t*>(qd) = packed;
     if (lane == 0) sc[static_cast<size_t>(n) * G + g] = sbits;
     zbyte |= static_cast<uint32_t>(z) << (4 * h);
   }
@@ -98,12 +119,16 @@ __device__ __forceinline__ uint32_t tiled_to_canon_word(uint32_t tw) {
   return o;
 }
 
-// One block per super-block (T, g).
+// One block per super-block (T, g), g over the K/128 column blocks; its
+// scale and zero point are those of group g >> gshift (gshift = 1 for groups
+// of 256), whose canonical arrays have Gs = K / group entries per row.
 __global__ void k_repack(const uint8_t* __restrict__ q, const uint16_t* __restrict__ sc,
-                         const uint8_t* __restrict__ zr, int N, int K, int G, uint8_t* __restrict__ out) {
+                         const uint8_t* __restrict__ zr, int N, int K, int G, int gshift,
+                         uint8_t* __restrict__ out) {
   const int sbi = blockIdx.x;
   const int T = sbi / G, g = sbi % G;
-  const int ZB = (G + 1) / 2;
+  const int Gs = G >> gshift, gs = g >> gshift;
+  const int ZB = (Gs + 1) / 2;
   uint8_t* dst = out + static_cast<size_t>(sbi) * kSbBytes;
   for (int wi = threadIdx.x; wi < kSbNib / 4; wi += blockDim.x) {
     const int r = wi >> 4, pw = wi & 15;
@@ -122,41 +147,48 @@ __global__ void k_repack(const uint8_t* __restrict__ q, const uint16_t* __restri
   const int t = threadIdx.x;
   if (t < kRowTile) {
     const int n = T * kRowTile + t;
-    reinterpret_cast<uint16_t*>(dst + kSbNib)[t] = n < N ? sc[static_cast<size_t>(n) * G + g] : 0;
+    reinterpret_cast<uint16_t*>(dst + kSbNib)[t] = n < N ? sc[static_cast<size_t>(n) * Gs + gs] : 0;
   }
   if (t < kRowTile / 2) {
     uint32_t b = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int n = T * kRowTile + 2 * t + h;
-      if (n < N) b |= ((zr[static_cast<size_t>(n) * ZB + g / 2] >> (4 * (g & 1))) & 15u) << (4 * h);
+      if (n < N) b |= ((zr[static_cast<size_t>(n) * ZB + gs / 2] >> (4 * (gs & 1))) & 15u) << (4 * h);
     }
     dst[kSbNib + kSbScale + t] = static_cast<uint8_t>(b);
   }
 }
 
-// One block per (T, pair of groups): a canonical zero byte spans two groups.
-__global__ void k_unrepack(const uint8_t* __restrict__ in, int N, int K, int G, uint8_t* __restrict__ q,
-                           uint16_t* __restrict__ sc, uint8_t* __restrict__ zr) {
-  const int ZB = (G + 1) / 2;
+// One block per (T, pair of groups 2gp, 2gp+1): a canonical zero byte spans
+// two groups.  Codes come from every super-block of the two groups, the
+// scale and zero point of group gs from its first super-block gs << gshift.
+__global__ void k_unrepack(const uint8_t* __restrict__ in, int N, int K, int G, int gshift,
+                           uint8_t* __restrict__ q, uint16_t* __restrict__ sc, uint8_t* __restrict__ zr) {
+  const int Gs = G >> gshift;
+  const int ZB = (Gs + 1) / 2;
   const int T = blockIdx.x / ZB, gp = blockIdx.x % ZB;
   for (int h = 0; h < 2; ++h) {
-    const int g = 2 * gp + h;
-    if (g >= G) break;
-    const uint8_t* src = in + (static_cast<size_t>(T) * G + g) * kSbBytes;
-    for (int wi = threadIdx.x; wi < kSbNib / 4; wi += blockDim.x) {
-      const int r = wi >> 4, pw = wi & 15;
-      const int n = T * kRowTile + r;
-      if (n >= N) continue;
-      const int p = 4 * (((pw >> 2) - (r >> 1)) & 3) + (pw & 3);
-      const int wl = 4 * (p & 3) + (p >> 2);
-      *reinterpret_cast<uint32_t*>(q + static_cast<size_t>(n) * (K / 2) + g * (kGroup / 2) + 4 * wl) =
-          tiled_to_canon_word(reinterpret_cast<const uint32_t*>(src)[wi]);
+    const int gs = 2 * gp + h;
+    if (gs >= Gs) break;
+    for (int sub = 0; sub < (1 << gshift); ++sub) {
+      const int g = (gs << gshift) + sub;
+      const uint8_t* src = in + (static_cast<size_t>(T) * G + g) * kSbBytes;
+      for (int wi = threadIdx.x; wi < kSbNib / 4; wi += blockDim.x) {
+        const int r = wi >> 4, pw = wi & 15;
+        const int n = T * kRowTile + r;
+        if (n >= N) continue;
+        const int p = 4 * (((pw >> 2) - (r >> 1)) & 3) + (pw & 3);
+        const int wl = 4 * (p & 3) + (p >> 2);
+        *reinterpret_cast<uint32_t*>(q + static_cast<size_t>(n) * (K / 2) + g * (kGroup / 2) + 4 * wl) =
+            tiled_to_canon_word(reinterpret_cast<const uint32_t*>(src)[wi]);
+      }
     }
+    const uint8_t* src = in + (static_cast<size_t>(T) * G + (gs << gshift)) * kSbBytes;
     const int t = threadIdx.x;
     if (t < kRowTile) {
       const int n = T * kRowTile + t;
-      if (n < N) sc[static_cast<size_t>(n) * G + g] = reinterpret_cast<const uint16_t*>(src + kSbNib)[t];
+      if (n < N) sc[static_cast<size_t>(n) * Gs + gs] = reinterpret_cast<const uint16_t*>(src + kSbNib)[t];
     }
   }
   const int t = threadIdx.x;
@@ -166,9 +198,9 @@ __global__ void k_unrepack(const uint8_t* __restrict__ in, int N, int K, int G, 
       uint32_t b = 0;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int g = 2 * gp + h;
-        if (g >= G) break;
-        const uint8_t* src = in + (static_cast<size_t>(T) * G + g) * kSbBytes;
+        const int gs = 2 * gp + h;
+        if (gs >= Gs) break;
+        const uint8_t* src = in + (static_cast<size_t>(T) * G + (gs << gshift)) * kSbBytes;
         b |= ((src[kSbNib + kSbScale + t / 2] >> (4 * (t & 1))) & 15u) << (4 * h);
       }
       zr[static_cast<size_t>(n) * ZB + gp] = static_cast<uint8_t>(b);
@@ -176,7 +208,10 @@ __global__ void k_unrepack(const uint8_t* __restrict__ in, int N, int K, int G, 
   }
 }
 
-bool shape_ok(int N, int K, int group) { return N >= 1 && K >= kGroup && K % kGroup == 0 && group == kGroup; }
+// Group sizes of the layout: 128 (gshift 0) and 256 (gshift 1).
+bool group_ok(int group) { return group == kGroup || group == 2 * kGroup; }
+int group_shift(int group) { return group == 2 * kGroup ? 1 : 0; }
+bool shape_ok(int N, int K, int group) { return N >= 1 && K >= group && K % group == 0 && group_ok(group); }
 
 size_t tiled_bytes(int N, int K) {
   const size_t T = (static_cast<size_t>(N) + kRowTile - 1) / kRowTile;
@@ -187,32 +222,36 @@ size_t tiled_bytes(int N, int K) {
 
 extern "C" int fl_int4g_repacked_bytes(int N, int K, int group, size_t* out) {
   if (!out) return FL_ERR_ARG;
-  if (group != kGroup) return FL_ERR_UNSUPPORTED;
-  if (N < 1 || K < kGroup || K % kGroup) return FL_ERR_ARG;
+  if (!group_ok(group)) return FL_ERR_UNSUPPORTED;
+  if (!shape_ok(N, K, group)) return FL_ERR_ARG;
   *out = tiled_bytes(N, K);
   return FL_OK;
 }
 
 extern "C" int fl_int4g_quantize(const float* w, int N, int K, int group, uint8_t* q, uint16_t* scales,
                                  uint8_t* zeros, void* status, fl_stream_t stream) {
-  if (group != kGroup) return FL_ERR_UNSUPPORTED;
+  if (!group_ok(group)) return FL_ERR_UNSUPPORTED;
   if (!shape_ok(N, K, group) || !w || !q || !scales || !zeros || !status) return FL_ERR_ARG;
   if (!flh::aligned16(w) || !flh::aligned16(q) || !flh::aligned16(scales) || !flh::aligned16(zeros) ||
       !flh::aligned16(status))
     return FL_ERR_ARG;
-  const int G = K / kGroup;
+  const int G = K / group;
   const long long warps = static_cast<long long>(N) * ((G + 1) / 2);
   const int threads = 256;
   const long long blocks = (warps * 32 + threads - 1) / threads;
   if (blocks > 0x7fffffffLL) return FL_ERR_UNSUPPORTED;
-  k_quantize<<<static_cast<unsigned>(blocks), threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      w, N, K, G, q, scales, zeros, static_cast<int32_t*>(status));
+  if (group == kGroup)
+    k_quantize<128><<<static_cast<unsigned>(blocks), threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        w, N, K, G, q, scales, zeros, static_cast<int32_t*>(status));
+  else
+    k_quantize<256><<<static_cast<unsigned>(blocks), threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        w, N, K, G, q, scales, zeros, static_cast<int32_t*>(status));
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
 extern "C" int fl_int4g_repack(const uint8_t* q, const uint16_t* scales, const uint8_t* zeros, int N, int K,
                                int group, void* w_out, size_t w_out_bytes, fl_stream_t stream) {
-  if (group != kGroup) return FL_ERR_UNSUPPORTED;
+  if (!group_ok(group)) return FL_ERR_UNSUPPORTED;
   if (!shape_ok(N, K, group) || !q || !scales || !zeros || !w_out) return FL_ERR_ARG;
   if (!flh::aligned16(q) || !flh::aligned16(scales) || !flh::aligned16(zeros) || !flh::aligned16(w_out))
     return FL_ERR_ARG;
@@ -221,21 +260,22 @@ extern "C" int fl_int4g_repack(const uint8_t* q, const uint16_t* scales, const u
   const long long blocks = static_cast<long long>((N + kRowTile - 1) / kRowTile) * G;
   if (blocks > 0x7fffffffLL) return FL_ERR_UNSUPPORTED;
   k_repack<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      q, scales, zeros, N, K, G, static_cast<uint8_t*>(w_out));
+      q, scales, zeros, N, K, G, group_shift(group), static_cast<uint8_t*>(w_out));
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
 extern "C" int fl_int4g_unrepack(const void* w, size_t w_bytes, int N, int K, int group, uint8_t* q,
                                  uint16_t* scales, uint8_t* zeros, fl_stream_t stream) {
-  if (group != kGroup) return FL_ERR_UNSUPPORTED;
+  if (!group_ok(group)) return FL_ERR_UNSUPPORTED;
   if (!shape_ok(N, K, group) || !q || !scales || !zeros || !w) return FL_ERR_ARG;
   if (!flh::aligned16(q) || !flh::aligned16(scales) || !flh::aligned16(zeros) || !flh::aligned16(w))
     return FL_ERR_ARG;
   if (w_bytes < tiled_bytes(N, K)) return FL_ERR_ARG;
   const int G = K / kGroup;
-  const long long blocks = static_cast<long long>((N + kRowTile - 1) / kRowTile) * ((G + 1) / 2);
+  const int Gs = K / group;
+  const long long blocks = static_cast<long long>((N + kRowTile - 1) / kRowTile) * ((Gs + 1) / 2);
   if (blocks > 0x7fffffffLL) return FL_ERR_UNSUPPORTED;
   k_unrepack<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint8_t*>(w), N, K, G, q, scales, zeros);
+      static_cast<const uint8_t*>(w), N, K, G, group_shift(group), q, scales, zeros);
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }

@@ -47,6 +47,10 @@ def test_repacked_bytes(L):
     assert L.fl_int4g_repacked_bytes(128, 100, 128, ctypes.byref(out)) == 1      # K % 128
     assert L.fl_int4g_repacked_bytes(128, 256, 64, ctypes.byref(out)) == 3       # group 64
     assert L.fl_int4g_repacked_bytes(0, 256, 128, ctypes.byref(out)) == 1
+    # groups of 256: the same 128-column super-blocks (two per group)
+    assert fl.fl_int4g_repacked_bytes(4096, 11008, 256) == 32 * 86 * 8512
+    assert L.fl_int4g_repacked_bytes(128, 384, 256, ctypes.byref(out)) == 1      # K % 256
+    assert L.fl_int4g_repacked_bytes(128, 512, 512, ctypes.byref(out)) == 3      # group 512
 
 
 def test_argument_errors_are_caught_on_the_host(L):
@@ -65,5 +69,8 @@ def test_argument_errors_are_caught_on_the_host(L):
     assert L.fl_int4g_linear(fake, 1, 256, fake, 128, fake, fake, 16, None) == 2
     assert L.fl_int4g_repack(fake, fake, fake, 128, 256, 128, fake, 100, None) == 1
     assert L.fl_int4g_repack(fake, fake, fake, 128, 256, 64, fake, 1 << 20, None) == 3
+    assert L.fl_int4g_repack(fake, fake, fake, 128, 384, 256, fake, 1 << 20, None) == 1
+    assert L.fl_int4g_unrepack(fake, 1 << 20, 128, 384, 256, fake, fake, fake, None) == 1
+    assert L.fl_int4g_quantize(fake, 128, 384, 256, fake, fake, fake, fake, None) == 1
     assert L.fl_int4g_quantize(fake, 128, 256, 128, fake, fake, null, fake, None) == 1
     assert L.fl_int4g_status(null, None, ctypes.byref(ctypes.c_int())) == 1

@@ -99,6 +99,53 @@ def test_repack_bit_exact_and_invertible(shape):
     assert np.array_equal(back[0], Q) and np.array_equal(back[1], S) and np.array_equal(back[2], Z)
 
 
+# ------------------------------------------------- groups of 256 (a1, a2, a3)
+# FastLLM page, section 4.2: --group-size 128 by default, 256 allowed.  The
+# interleaved layout keeps 128-column super-blocks; both super-blocks of a
+# group carry its scale and zero point, so the matmul kernels are unchanged.
+
+@pytest.mark.parametrize("shape", [(200, 512), (3, 1024), (129, 1280)])
+def test_quantizer_group256_bit_exact(shape):
+    N, K = shape
+    W = inputs.dense_weight(N, K, layer=80 + N)
+    W[0, :256] = 0.0             # zero group
+    W[1 % N, 256:512] = -0.75    # constant negative group
+    Q, S, Z = O.quantize(W, 256)
+    got = canon_host(*fl.fl_int4g_quantize(to_dev(W), group=256))
+    assert np.array_equal(got[0], Q)
+    assert np.array_equal(got[1], S)
+    assert np.array_equal(got[2], Z)
+
+
+@pytest.mark.parametrize("shape", [(200, 512), (128, 256), (300, 1280)])
+def test_repack_group256_bit_exact_and_invertible(shape):
+    N, K = shape
+    W = inputs.dense_weight(N, K, layer=90 + N)
+    Q, S, Z = O.quantize(W, 256)
+    w = fl.fl_int4g_repack(to_dev(Q), to_dev(S.view(np.int16)), to_dev(Z), N, K, group=256)
+    assert np.array_equal(w.cpu().numpy(), O.repack(Q, S, Z, N, K, 256))
+    back = canon_host(*fl.fl_int4g_unrepack(w, N, K, group=256))
+    assert np.array_equal(back[0], Q) and np.array_equal(back[1], S) and np.array_equal(back[2], Z)
+
+
+@pytest.mark.parametrize("M", [1, 8, 9, 32, 64, 300])
+def test_linear_group256_parity(M):
+    """Decode (rows and tcgen05 kernels) and prefill on group-256 weights,
+    quantized and repacked on the GPU, against the oracle's group-256 linear."""
+    N, K = 384, 1280
+    W = inputs.dense_weight(N, K, layer=95)
+    xb = inputs.activations(M, K, stream=95)
+    Q, S, Z = O.quantize(W, 256)
+    q, s, z = fl.fl_int4g_quantize(to_dev(W), group=256)
+    w = fl.fl_int4g_repack(q, s, z, N, K, group=256)
+    y = fl.fl_int4g_linear(bf16_dev(xb), w, N)
+    xf = O.bf16_value(xb)
+    ref, tol = O.linear(xf, Q, S, Z, 256), O.linear_tolerance(xf, Q, S, Z, 256)
+    got = y.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= tol), f"worst err/tol {np.max(np.abs(got - ref) / tol):.3f}"
+
+
 # ------------------------------------------------------------ a3 linear
 
 def _linear_case(M, N, K, layer):

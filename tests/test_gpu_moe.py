@@ -212,3 +212,24 @@ def test_moe_deepseek_shaped():
         y, ids, wts, offs, perm = run_moe(xb, logits, 8, 2048, ex.w13, ex.w2, fl.FL_SIGMOID, True, ex.sw13, ex.sw2)
         check_routing(logits, 8, fl.FL_SIGMOID, True, ids, wts, offs, perm)
         sampled_check(ex, xb, logits, 8, O.SIGMOID, y, ids, np.array([M - 1]))
+
+
+@pytest.mark.parametrize("M", [5, 64])
+def test_moe_group256_experts(M):
+    """Experts quantized in groups of 256 (FastLLM page, section 4.2): the
+    interleaved layout carries each group's scale in both of its 128-column
+    super-blocks, and the MoE path (rows kernels at M=5, the grouped GEMM at
+    M=64) runs on it unchanged."""
+    E, H, I, k = 4, 512, 256, 2
+    w13 = [O.quantize(inputs.expert_weight(2 * I, H, 97, e, 0), 256) for e in range(E)]
+    w2 = [O.quantize(inputs.expert_weight(H, I, 97, e, 1), 256) for e in range(E)]
+    w13_d = torch.cat([fl.fl_int4g_repack(to_dev(Q), to_dev(S.view(np.int16)), to_dev(Z), 2 * I, H, group=256)
+                       for Q, S, Z in w13])
+    w2_d = torch.cat([fl.fl_int4g_repack(to_dev(Q), to_dev(S.view(np.int16)), to_dev(Z), H, I, group=256)
+                      for Q, S, Z in w2])
+    xb = inputs.activations(M, H, stream=97)
+    logits = inputs.router_logits(M, E, stream=97)
+    y, ids, wts, offs, perm = run_moe(xb, logits, k, I, w13_d, w2_d, O.SOFTMAX, True)
+    ref, tol, rid, rw = O.moe(O.bf16_value(xb), logits, k, w13, w2, O.SOFTMAX, True, group=256)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    check_y(y, ref, tol)
