@@ -228,7 +228,10 @@ def run_gemm_section(torch, np, fl, inputs, dev, pk, reps):
     return out
 
 
-def run_gpu(args):
+def run_gpu(args, barrier=None):
+    """One GPU's run.  barrier: called just before and just after the timed
+    region (after a device synchronize), so that replicas start and stop
+    their timed steps together."""
     import numpy as np
     import torch
 
@@ -237,7 +240,7 @@ def run_gpu(args):
 
     _build.build()
     fl.lib()
-    dev = torch.device("cuda:0")
+    dev = torch.device("cuda", torch.cuda.current_device())
     torch.cuda.set_device(dev)
     pk = peaks()
 
@@ -281,12 +284,16 @@ def run_gpu(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    if barrier:
+        barrier()
     with torch.cuda.stream(stream):
         t0.record(stream)
         for _ in range(args.steps):
             graph.replay()
         t1.record(stream)
     torch.cuda.synchronize()
+    if barrier:
+        barrier()
     clocks = clk.stop()
     ms_total = t0.elapsed_time(t1)
     ms_step = ms_total / args.steps
@@ -561,9 +568,30 @@ def main():
     print(json.dumps(run_gpu(args)))
 
 
+def aggregate_replicas(out, world, max_over_ranks):
+    """Job-wide line of `world` independent replicas from one rank's line:
+    the step time is the maximum over ranks, value = the weight bytes all
+    ranks streamed per step / that time, and the end-to-end figure likewise
+    (world x the slowest rank's).  max_over_ranks(v) returns the maximum of v
+    over the ranks (a collective: every rank calls it, in the same order)."""
+    ms = max_over_ranks(out["ms_per_step"])
+    agg = dict(out)
+    agg["config"] = dict(out["config"])
+    agg["n_gpus"] = world
+    agg["ms_per_step"] = round(ms, 4)
+    agg["value"] = round(out["config"]["weight_bytes_per_step"] * world / (ms * 1e-3) / 1e9, 1)
+    agg["config"]["parallelism"] = f"replicas{world}"
+    if isinstance(out.get("e2e"), dict) and out["e2e"].get("value") is not None:
+        slowest = -max_over_ranks(-out["e2e"]["value"])
+        agg["e2e"] = dict(out["e2e"])
+        agg["e2e"]["value"] = round(world * slowest, 1)
+    return agg
+
+
 def run_replicas(args, rank, world):
     """N independent replicas (the path needs no exchange): each rank runs the
-    same step on its own GPU; value = sum over ranks, time = max over ranks."""
+    same step on its own GPU, starting and stopping its timed region at a
+    barrier; value = sum over ranks, time = max over ranks."""
     import torch
     import torch.distributed as dist
     local = int(os.environ.get("LOCAL_RANK", rank))
@@ -571,16 +599,16 @@ def run_replicas(args, rank, world):
     dist.init_process_group("nccl")
     args.no_cpu_baseline = args.no_cpu_baseline or rank != 0
     dist.barrier()
-    out = run_gpu(args)
-    t = torch.tensor([out["ms_per_step"]], device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item())
-    out["n_gpus"] = world
-    out["ms_per_step"] = round(ms, 4)
-    out["value"] = round(out["config"]["weight_bytes_per_step"] * world / (ms * 1e-3) / 1e9, 1)
-    out["config"]["parallelism"] = f"replicas{world}"
+    out = run_gpu(args, barrier=dist.barrier)
+
+    def max_over_ranks(v):
+        t = torch.tensor([float(v)], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    agg = aggregate_replicas(out, world, max_over_ranks)
     dist.destroy_process_group()
-    return out
+    return agg
 
 
 if __name__ == "__main__":
