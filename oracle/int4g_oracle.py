@@ -386,8 +386,11 @@ SOFTMAX = 0
 SIGMOID = 1
 
 
-def route(logits, k, scoring=SOFTMAX, renorm=True):
+def route(logits, k, scoring=SOFTMAX, renorm=True, bias=None, n_group=1, topk_group=1, scale=1.0):
     """Top-k routing of fp32 router logits [M, E].
+
+    bias / n_group > 1 (sigmoid scoring only) select the DeepSeek-V3 way,
+    see route_keyed(); scale multiplies the final weights in every mode.
 
     Selection uses the raw fp32 logits: the k largest; equal logits go to
     the lower expert index; slots are ordered by descending logit, then
@@ -420,6 +423,50 @@ def route(logits, k, scoring=SOFTMAX, renorm=True):
             wts[t] = sg / sg.sum() if renorm else sg
         else:
             raise ValueError("unknown scoring")
+    if bias is not None or n_group > 1:
+        if scoring != SIGMOID:
+            raise ValueError("the score bias and group-limited routing take sigmoid scoring")
+        ids, wts = route_keyed(logits, k, renorm, bias, n_group, topk_group)
+    return ids, wts * float(scale)
+
+
+def route_keyed(logits, k, renorm=True, bias=None, n_group=1, topk_group=1):
+    """DeepSeek-V3 style selection (sigmoid affinities, auxiliary-loss-free
+    bias, group-limited experts), in double; not on the FastLLM pages, whose
+    MoE options only fix top-k and the shared expert.
+
+      s_e   = sigma(l_e)                         affinity (l: the fp32 logit)
+      key_e = s_e + b_e                          b: fp32 bias, used for the choice only
+      groups: n_group runs of E/n_group consecutive experts; a group's score is
+              the sum of its two largest keys (its one key if it has one);
+              the topk_group best groups are kept (ties: lower group index)
+      experts: the k largest keys among the kept groups' experts (ties: lower
+              index), slots ordered by descending key, then index
+      w_j   = s_{e_j} / sum_sel s (renorm) or s_{e_j}: the bias is not in the weights
+    """
+    logits = np.asarray(logits, np.float32)
+    M, E = logits.shape
+    if n_group < 1 or E % n_group or not (1 <= topk_group <= n_group):
+        raise ValueError("need E % n_group == 0 and 1 <= topk_group <= n_group")
+    gsz = E // n_group
+    if not (1 <= k <= topk_group * gsz):
+        raise ValueError("need 1 <= k <= topk_group * E / n_group")
+    b = np.zeros(E) if bias is None else np.asarray(bias, np.float32).astype(np.float64)
+    ids = np.zeros((M, k), np.int32)
+    wts = np.zeros((M, k), np.float64)
+    for t in range(M):
+        s = 1.0 / (1.0 + np.exp(-logits[t].astype(np.float64)))
+        key = s + b
+        gscore = []
+        for g in range(n_group):
+            kg = sorted(key[g * gsz:(g + 1) * gsz], reverse=True)
+            gscore.append(sum(kg[:2]))
+        kept = sorted(range(n_group), key=lambda g: (-gscore[g], g))[:topk_group]
+        eligible = [e for e in range(E) if e // gsz in kept]
+        sel = sorted(eligible, key=lambda e: (-key[e], e))[:k]
+        ids[t] = sel
+        sg = s[sel]
+        wts[t] = sg / sg.sum() if renorm else sg
     return ids, wts
 
 
@@ -486,7 +533,7 @@ def expert_ffn(x, w13, w2, group=GROUP):
 
 
 def moe(x, logits, k, w13, w2, scoring=SOFTMAX, renorm=True,
-        shared_w13=None, shared_w2=None, group=GROUP):
+        shared_w13=None, shared_w2=None, group=GROUP, routing=None):
     """Routed MoE layer with int4g experts, in double.
 
     x float64 [M, H]; logits fp32 [M, E]; w13[e], w2[e] canonical triples
@@ -498,7 +545,7 @@ def moe(x, logits, k, w13, w2, scoring=SOFTMAX, renorm=True,
     """
     x = np.asarray(x, np.float64)
     M, H = x.shape
-    ids, wts = route(logits, k, scoring, renorm)
+    ids, wts = route(logits, k, scoring, renorm, **(routing or {}))
     y = np.zeros((M, H))
     tol = np.zeros((M, H))
     for e in np.unique(ids):

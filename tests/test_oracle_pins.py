@@ -373,6 +373,88 @@ def test_route_renorm_equals_softmax_all_then_renormalise():
     assert np.allclose(a.sum(axis=1), 1.0, rtol=1e-14)
 
 
+def _logit(p):
+    return np.float32(np.log(p / (1.0 - p)))
+
+
+def test_route_keyed_defaults_equal_plain_sigmoid():
+    """Zero bias, one group, scale 1: the sigmoid keys order the experts as
+    the logits do (sigma is strictly increasing, no saturation here)."""
+    l = np.random.default_rng([0, 31]).standard_normal((20, 16)).astype(np.float32)
+    l[3, 5] = l[3, 9]                                   # a tie: lower index first
+    a = O.route(l, 4, O.SIGMOID, True)
+    b = O.route(l, 4, O.SIGMOID, True, bias=np.zeros(16, np.float32), n_group=1)
+    assert np.array_equal(a[0], b[0]) and np.allclose(a[1], b[1], rtol=1e-15, atol=0)
+
+
+def test_route_bias_hand_case():
+    """Equal logits (sigma = 1/2 each), bias [0, .1, -.1, .05]: keys .5, .6,
+    .4, .55 pick experts 1 and 3; the weights use the unbiased sigma: 1/2
+    each after renormalisation, times the routed scale."""
+    l = np.zeros((1, 4), np.float32)
+    bias = np.array([0.0, 0.1, -0.1, 0.05], np.float32)
+    ids, w = O.route(l, 2, O.SIGMOID, True, bias=bias)
+    assert ids.tolist() == [[1, 3]] and np.allclose(w, 0.5, rtol=0, atol=1e-15)
+    ids, w = O.route(l, 2, O.SIGMOID, False, bias=bias, scale=2.5)
+    assert ids.tolist() == [[1, 3]] and np.allclose(w, 1.25, rtol=0, atol=1e-15)
+
+
+def test_route_group_limited_hand_case():
+    """E=8 in 4 groups of 2, keep 2 groups, k=2.  Affinities .9 .1 | .6 .6 |
+    .95 .02 | .3 .3: group scores (top-2 sums) 1.0, 1.2, .97, .6 keep groups
+    1 and 0; among experts 0..3 the best are 0 (.9) and 2 (.6, tied with 3:
+    lower index).  Without the group limit the choice would be 4 and 0.
+    Weights .9/1.5 and .6/1.5."""
+    p = [0.9, 0.1, 0.6, 0.6, 0.95, 0.02, 0.3, 0.3]
+    l = np.array([[_logit(v) for v in p]], np.float32)
+    ids, w = O.route(l, 2, O.SIGMOID, True, n_group=4, topk_group=2)
+    assert ids.tolist() == [[0, 2]]
+    assert np.allclose(w, [[0.6, 0.4]], rtol=1e-6, atol=0)
+    assert O.route(l, 2, O.SIGMOID, True)[0].tolist() == [[4, 0]]
+
+
+def test_route_group_limited_invariants():
+    """Random logits and bias: every chosen expert lies in a kept group; the
+    kept groups are the best by the sum of their two largest keys (recomputed
+    here with numpy sorts); no eligible expert left out has a larger key than
+    a chosen one; slots are in descending key order; weights are the chosen
+    unbiased affinities, renormalised, times the scale."""
+    rng = np.random.default_rng([0, 32])
+    E, ng, tg, k, M = 16, 4, 2, 3, 40
+    l = rng.standard_normal((M, E)).astype(np.float32)
+    bias = (0.1 * rng.standard_normal(E)).astype(np.float32)
+    ids, w = O.route(l, k, O.SIGMOID, True, bias=bias, n_group=ng, topk_group=tg, scale=2.5)
+    s = 1.0 / (1.0 + np.exp(-l.astype(np.float64)))
+    key = s + bias.astype(np.float64)
+    for t in range(M):
+        gs = np.sort(key[t].reshape(ng, E // ng), axis=1)[:, -2:].sum(axis=1)
+        kept = set(np.argsort(-gs, kind="stable")[:tg].tolist())
+        assert all(e // (E // ng) in kept for e in ids[t])
+        elig = [e for e in range(E) if e // (E // ng) in kept and e not in ids[t]]
+        assert min(key[t, ids[t]]) >= max(key[t, elig])
+        assert np.all(np.diff(key[t, ids[t]]) <= 0)
+        assert np.allclose(w[t], 2.5 * s[t, ids[t]] / s[t, ids[t]].sum(), rtol=1e-14, atol=0)
+
+
+def test_route_one_expert_groups_equal_bias_only():
+    rng = np.random.default_rng([0, 33])
+    l = rng.standard_normal((10, 8)).astype(np.float32)
+    bias = (0.2 * rng.standard_normal(8)).astype(np.float32)
+    a = O.route(l, 3, O.SIGMOID, True, bias=bias)
+    b = O.route(l, 3, O.SIGMOID, True, bias=bias, n_group=8, topk_group=8)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_route_keyed_argument_errors():
+    l = np.zeros((1, 8), np.float32)
+    with pytest.raises(ValueError):
+        O.route(l, 2, O.SOFTMAX, True, bias=np.zeros(8, np.float32))
+    with pytest.raises(ValueError):
+        O.route(l, 2, O.SIGMOID, True, n_group=3, topk_group=1)
+    with pytest.raises(ValueError):
+        O.route(l, 3, O.SIGMOID, True, n_group=4, topk_group=1)   # only 2 experts eligible
+
+
 def test_permute_hand_case_and_invariants():
     ids = np.array([[2, 0], [0, 1], [2, 1]])
     off, perm = O.permute(ids, 3)
