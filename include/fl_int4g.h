@@ -205,6 +205,38 @@ int fl_moe_int4g(const void* x, const float* logits, int M, int H, int E, int k,
                  int32_t* expert_offsets, int32_t* perm,
                  void* ws, size_t ws_bytes, fl_stream_t stream);
 
+/* Routing options of fl_moe_int4g_ex.  fl_moe_int4g is this call with
+ * score_bias = NULL, n_group = 1, topk_group = 1, routed_scale = 1.
+ * score_bias / n_group > 1 select DeepSeek-V3 style (not on the FastLLM
+ * pages, whose MoE options fix only top-k and the shared expert), with
+ * scoring = FL_SIGMOID:
+ *   s_e = sigmoid(l_e), key_e = s_e + score_bias[e] (the bias steers the
+ *   choice only); experts form n_group runs of E/n_group, a group scores the
+ *   sum of its two largest keys, the topk_group best groups are kept (ties:
+ *   lower group index), and the top-k keys among their experts are chosen
+ *   (ties: lower index; slots by descending key).  Keys are compared in
+ *   double precision.  Weights: s_e of the chosen, divided by their sum when
+ *   renorm.  In every mode the final weights are multiplied by routed_scale.
+ * Errors (FL_ERR_ARG): a bias or n_group > 1 with softmax scoring,
+ * E % n_group != 0, topk_group outside 1..n_group, k > topk_group * E /
+ * n_group, routed_scale not positive and finite, a misaligned bias. */
+typedef struct fl_moe_routing {
+  int scoring;               /* FL_SOFTMAX or FL_SIGMOID */
+  int renorm;                /* as in fl_moe_int4g */
+  const float* score_bias;   /* fp32 [E] device, 16-byte aligned, or NULL */
+  int n_group;               /* <= 1: no group limit */
+  int topk_group;            /* groups kept per token when n_group > 1 */
+  float routed_scale;        /* multiplies the final weights (1: none) */
+} fl_moe_routing;
+
+int fl_moe_int4g_ex(const void* x, const float* logits, int M, int H, int E, int k, int I,
+                    const fl_moe_routing* routing,
+                    const void* w13, const void* w2,
+                    const void* shared_w13, const void* shared_w2,
+                    void* y, int32_t* topk_ids, float* topk_w,
+                    int32_t* expert_offsets, int32_t* perm,
+                    void* ws, size_t ws_bytes, fl_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

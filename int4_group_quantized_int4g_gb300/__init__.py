@@ -18,7 +18,7 @@ __all__ = [
     "fl_strerror", "fl_int4g_version", "fl_int4g_status",
     "fl_int4g_quantize", "fl_int4g_repacked_bytes", "fl_int4g_repack", "fl_int4g_unrepack",
     "fl_int4g_linear_workspace", "fl_int4g_linear", "fl_int4g_linear_noalloc",
-    "fl_moe_int4g_workspace", "fl_moe_int4g",
+    "fl_moe_int4g_workspace", "fl_moe_int4g", "FlMoeRouting",
 ]
 
 GROUP = 128
@@ -28,6 +28,13 @@ FL_SIGMOID = 1
 _c_size_p = ctypes.POINTER(ctypes.c_size_t)
 _vp = ctypes.c_void_p
 _i = ctypes.c_int
+
+
+class FlMoeRouting(ctypes.Structure):
+    """struct fl_moe_routing (routing options of fl_moe_int4g_ex)."""
+    _fields_ = [("scoring", ctypes.c_int), ("renorm", ctypes.c_int), ("score_bias", ctypes.c_void_p),
+                ("n_group", ctypes.c_int), ("topk_group", ctypes.c_int), ("routed_scale", ctypes.c_float)]
+
 
 # C signatures: name -> (restype, argtypes)
 SIGNATURES = {
@@ -44,6 +51,8 @@ SIGNATURES = {
     "fl_moe_int4g_workspace": (_i, [_i, _i, _i, _i, _i, _i, _c_size_p]),
     "fl_moe_int4g": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
                           _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "fl_moe_int4g_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(FlMoeRouting), _vp, _vp, _vp, _vp,
+                             _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
 }
 
 _LIB = None
@@ -210,10 +219,13 @@ def fl_moe_int4g_workspace(M, E, k, H, I, has_shared):
 
 
 def fl_moe_int4g(x, logits, k, I, w13, w2, scoring=FL_SOFTMAX, renorm=True, shared_w13=None, shared_w2=None,
-                 y=None, topk_ids=None, topk_w=None, expert_offsets=None, perm=None, ws=None):
+                 y=None, topk_ids=None, topk_w=None, expert_offsets=None, perm=None, ws=None,
+                 score_bias=None, n_group=1, topk_group=1, routed_scale=1.0):
     """Routed MoE layer.  w13 / w2: uint8 CUDA tensors holding the E
     interleaved expert matrices back to back.  Optional routing outputs are
-    written when given."""
+    written when given.  score_bias (fp32 [E] CUDA tensor), n_group /
+    topk_group and routed_scale are the routing options of fl_moe_int4g_ex;
+    with their defaults this is fl_moe_int4g."""
     torch = _torch()
     M, H = x.shape
     E = logits.shape[1]
@@ -223,9 +235,17 @@ def fl_moe_int4g(x, logits, k, I, w13, w2, scoring=FL_SOFTMAX, renorm=True, shar
     nb = fl_moe_int4g_workspace(M, E, k, H, I, has_shared)
     if ws is None:
         ws = _workspace(nb, x.device)
-    _check("fl_moe_int4g",
-           lib().fl_moe_int4g(_p(x), _p(logits), M, H, E, k, I, scoring, int(bool(renorm)),
-                              _p(w13), _p(w2), _p(shared_w13), _p(shared_w2), _p(y),
-                              _p(topk_ids), _p(topk_w), _p(expert_offsets), _p(perm),
-                              _p(ws), ws.numel(), _stream()))
+    if score_bias is None and n_group <= 1 and routed_scale == 1.0:
+        _check("fl_moe_int4g",
+               lib().fl_moe_int4g(_p(x), _p(logits), M, H, E, k, I, scoring, int(bool(renorm)),
+                                  _p(w13), _p(w2), _p(shared_w13), _p(shared_w2), _p(y),
+                                  _p(topk_ids), _p(topk_w), _p(expert_offsets), _p(perm),
+                                  _p(ws), ws.numel(), _stream()))
+        return y
+    r = FlMoeRouting(scoring, int(bool(renorm)), _p(score_bias), int(n_group), int(topk_group), float(routed_scale))
+    _check("fl_moe_int4g_ex",
+           lib().fl_moe_int4g_ex(_p(x), _p(logits), M, H, E, k, I, ctypes.byref(r),
+                                 _p(w13), _p(w2), _p(shared_w13), _p(shared_w2), _p(y),
+                                 _p(topk_ids), _p(topk_w), _p(expert_offsets), _p(perm),
+                                 _p(ws), ws.numel(), _stream()))
     return y

@@ -49,7 +49,8 @@ struct MoePlan {
 __device__ __forceinline__ bool better(float v, int e, float bv, int be) { return v > bv || (v == bv && e < be); }
 
 __global__ void k_moe_route(const float* __restrict__ logits, int M, int E, int k, int scoring, int renorm,
-                            int32_t* __restrict__ ids, float* __restrict__ wts, int32_t* __restrict__ status) {
+                            float scale, int32_t* __restrict__ ids, float* __restrict__ wts,
+                            int32_t* __restrict__ status) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= M) return;
@@ -114,7 +115,115 @@ __global__ void k_moe_route(const float* __restrict__ logits, int M, int E, int 
     for (int j = 0; j < k; ++j) {
       const float num = scoring == FL_SOFTMAX ? expf(selv[j] - selv[0]) : 1.f / (1.f + expf(-selv[j]));
       ids[static_cast<size_t>(t) * k + j] = sele[j];
-      wts[static_cast<size_t>(t) * k + j] = num / den;
+      wts[static_cast<size_t>(t) * k + j] = num / den * scale;
+    }
+  }
+}
+
+__device__ __forceinline__ bool better_d(double v, int e, double bv, int be) {
+  return v > bv || (v == bv && e < be);
+}
+
+// Warp-wide argmax under better_d: every lane ends with the winner.
+__device__ __forceinline__ void warp_best(double& bv, int& be) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+    if (better_d(ov, oe, bv, be)) bv = ov, be = oe;
+  }
+}
+
+// DeepSeek-V3 style routing, one warp per token (kRouteWarps per block): the
+// affinities s_e = sigma(l_e) plus the selection bias b_e give the keys; the
+// experts come in n_group runs of E/n_group, a group scores the sum of its
+// two largest keys, the topk_group best groups are kept, and the top-k keys
+// among their experts are chosen (ties: lower index; slots by descending
+// key).  Weights use the unbiased s_e, renormalised if asked, times scale.
+// Keys and group scores are doubles in shared memory, [warp][E + n_group],
+// so that the choice is taken in double precision.
+constexpr int kRouteWarps = 2;
+__global__ void k_moe_route_keyed(const float* __restrict__ logits, const float* __restrict__ bias, int M, int E,
+                                  int k, int renorm, int n_group, int topk_group, float scale,
+                                  int32_t* __restrict__ ids, float* __restrict__ wts,
+                                  int32_t* __restrict__ status) {
+  extern __shared__ double rk_smem[];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int t = blockIdx.x * kRouteWarps + wib;
+  if (t >= M) return;   // whole warps leave; the kernel has no block-wide barrier
+  double* key = rk_smem + static_cast<size_t>(wib) * (E + n_group);
+  double* gsc = key + E;
+  const float* l = logits + static_cast<size_t>(t) * E;
+  int bad = 0;
+  for (int e = lane; e < E; e += 32) {
+    float x = l[e];
+    if (isnan(x)) bad = 1, x = -INFINITY;
+    double kv = 1.0 / (1.0 + exp(-static_cast<double>(x))) + (bias ? static_cast<double>(bias[e]) : 0.0);
+    if (isnan(kv)) bad = 1, kv = -INFINITY;   // a NaN bias: never chosen before a number
+    key[e] = kv;
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, FL_ERR_DEVICE_CHECK, t);
+  __syncwarp();
+  const int gsz = E / n_group;
+  for (int g = lane; g < n_group; g += 32) {
+    double b1 = -INFINITY, b2 = -INFINITY;
+    for (int i = 0; i < gsz; ++i) {
+      const double v = key[g * gsz + i];
+      if (v > b1) {
+        b2 = b1;
+        b1 = v;
+      } else if (v > b2) {
+        b2 = v;
+      }
+    }
+    const double gs = gsz >= 2 ? b1 + b2 : b1;
+    gsc[g] = isnan(gs) ? -INFINITY : gs;   // inf + -inf from infinite biases
+  }
+  __syncwarp();
+  // kept groups: bit i of lane's mask = group lane + 32 i
+  uint32_t kept = 0;
+  for (int j = 0; j < topk_group; ++j) {
+    double bv = -INFINITY;
+    int bg = 0x7fffffff;
+    for (int i = 0; i < 32 && lane + 32 * i < n_group; ++i) {
+      const int g = lane + 32 * i;
+      if (!((kept >> i) & 1u) && better_d(gsc[g], g, bv, bg)) bv = gsc[g], bg = g;
+    }
+    warp_best(bv, bg);
+    if ((bg & 31) == lane) kept |= 1u << (bg >> 5);
+  }
+  __syncwarp();
+  for (int i = 0; i < 32 && lane + 32 * i < n_group; ++i) gsc[lane + 32 * i] = ((kept >> i) & 1u) ? 1.0 : 0.0;
+  __syncwarp();
+  // experts: bit i of lane's mask = expert lane + 32 i
+  uint32_t taken = 0;
+  int sele[32];   // k <= 32 (checked on the host)
+  for (int j = 0; j < k; ++j) {
+    double bv = -INFINITY;
+    int be = 0x7fffffff;
+    for (int i = 0; i < 32 && lane + 32 * i < E; ++i) {
+      const int e = lane + 32 * i;
+      if (((taken >> i) & 1u) || gsc[e / gsz] == 0.0) continue;
+      if (better_d(key[e], e, bv, be)) bv = key[e], be = e;
+    }
+    warp_best(bv, be);
+    // the host checked k <= topk_group * E / n_group, so an untaken eligible
+    // expert always exists; be stays in range whatever the keys are
+    if (be >= E) be = 0;
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    sele[j] = be;
+  }
+  if (lane == 0) {
+    double sg[32], den = 0.0;
+    for (int j = 0; j < k; ++j) {
+      float x = l[sele[j]];
+      if (isnan(x)) x = -INFINITY;
+      sg[j] = 1.0 / (1.0 + exp(-static_cast<double>(x)));
+      den += sg[j];
+    }
+    for (int j = 0; j < k; ++j) {
+      ids[static_cast<size_t>(t) * k + j] = sele[j];
+      wts[static_cast<size_t>(t) * k + j] = static_cast<float>((renorm ? sg[j] / den : sg[j]) * scale);
     }
   }
 }
@@ -632,14 +741,25 @@ extern "C" int fl_moe_int4g_workspace(int M, int E, int k, int H, int I, int has
   return FL_OK;
 }
 
-extern "C" int fl_moe_int4g(const void* x, const float* logits, int M, int H, int E, int k, int I, int scoring,
-                            int renorm, const void* w13, const void* w2, const void* shared_w13,
-                            const void* shared_w2, void* y, int32_t* topk_ids, float* topk_w,
-                            int32_t* expert_offsets, int32_t* perm, void* ws, size_t ws_bytes,
-                            fl_stream_t stream) {
-  if (!x || !logits || !w13 || !w2 || !y || !ws) return FL_ERR_ARG;
+extern "C" int fl_moe_int4g_ex(const void* x, const float* logits, int M, int H, int E, int k, int I,
+                               const fl_moe_routing* routing, const void* w13, const void* w2,
+                               const void* shared_w13, const void* shared_w2, void* y, int32_t* topk_ids,
+                               float* topk_w, int32_t* expert_offsets, int32_t* perm, void* ws, size_t ws_bytes,
+                               fl_stream_t stream) {
+  if (!x || !logits || !w13 || !w2 || !y || !ws || !routing) return FL_ERR_ARG;
   if ((shared_w13 == nullptr) != (shared_w2 == nullptr)) return FL_ERR_ARG;
+  const int scoring = routing->scoring, renorm = routing->renorm;
   if (scoring != FL_SOFTMAX && scoring != FL_SIGMOID) return FL_ERR_ARG;
+  const float scale = routing->routed_scale;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return FL_ERR_ARG;
+  const int n_group = routing->n_group > 1 ? routing->n_group : 1;
+  const int topk_group = routing->n_group > 1 ? routing->topk_group : 1;
+  const bool keyed = routing->score_bias != nullptr || n_group > 1;
+  if (keyed) {
+    if (scoring != FL_SIGMOID || E < 1 || E % n_group || topk_group < 1 || topk_group > n_group) return FL_ERR_ARG;
+    if (k > topk_group * (E / n_group)) return FL_ERR_ARG;
+    if (routing->score_bias && !flh::aligned16(routing->score_bias)) return FL_ERR_ARG;
+  }
   if (!flh::aligned16(x) || !flh::aligned16(w13) || !flh::aligned16(w2) || !flh::aligned16(y) ||
       !flh::aligned16(ws) || (shared_w13 && (!flh::aligned16(shared_w13) || !flh::aligned16(shared_w2))))
     return FL_ERR_ARG;
@@ -658,10 +778,16 @@ extern "C" int fl_moe_int4g(const void* x, const float* logits, int M, int H, in
 
   // route
   {
-    const int warps = 8;
-    // plain launch: the logits come from whatever ran before this call
-    k_moe_route<<<dim3((M + warps - 1) / warps), dim3(32 * warps), 0, s>>>(logits, M, E, k, scoring, renorm, ids,
-                                                                            wts, status);
+    // plain launches: the logits come from whatever ran before this call
+    if (keyed) {
+      const size_t smem = static_cast<size_t>(kRouteWarps) * (E + n_group) * sizeof(double);
+      k_moe_route_keyed<<<dim3((M + kRouteWarps - 1) / kRouteWarps), dim3(32 * kRouteWarps), smem, s>>>(
+          logits, routing->score_bias, M, E, k, renorm, n_group, topk_group, scale, ids, wts, status);
+    } else {
+      const int warps = 8;
+      k_moe_route<<<dim3((M + warps - 1) / warps), dim3(32 * warps), 0, s>>>(logits, M, E, k, scoring, renorm,
+                                                                              scale, ids, wts, status);
+    }
     if (cudaGetLastError() != cudaSuccess) return FL_ERR_CUDA;
   }
   // permute
@@ -771,4 +897,20 @@ extern "C" int fl_moe_int4g(const void* x, const float* logits, int M, int H, in
                  has_shared, static_cast<__nv_bfloat16*>(y)) != cudaSuccess)
     return FL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+}
+
+extern "C" int fl_moe_int4g(const void* x, const float* logits, int M, int H, int E, int k, int I, int scoring,
+                            int renorm, const void* w13, const void* w2, const void* shared_w13,
+                            const void* shared_w2, void* y, int32_t* topk_ids, float* topk_w,
+                            int32_t* expert_offsets, int32_t* perm, void* ws, size_t ws_bytes,
+                            fl_stream_t stream) {
+  fl_moe_routing r;
+  r.scoring = scoring;
+  r.renorm = renorm;
+  r.score_bias = nullptr;
+  r.n_group = 1;
+  r.topk_group = 1;
+  r.routed_scale = 1.0f;
+  return fl_moe_int4g_ex(x, logits, M, H, E, k, I, &r, w13, w2, shared_w13, shared_w2, y, topk_ids, topk_w,
+                         expert_offsets, perm, ws, ws_bytes, stream);
 }

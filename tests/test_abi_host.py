@@ -74,3 +74,17 @@ def test_argument_errors_are_caught_on_the_host(L):
     assert L.fl_int4g_quantize(fake, 128, 384, 256, fake, fake, fake, fake, None) == 1
     assert L.fl_int4g_quantize(fake, 128, 256, 128, fake, fake, null, fake, None) == 1
     assert L.fl_int4g_status(null, None, ctypes.byref(ctypes.c_int())) == 1
+
+    # routing options of fl_moe_int4g_ex, rejected before any launch
+    def moe_ex(E, k, scoring, bias, n_group, topk_group, scale):
+        r = fl.FlMoeRouting(scoring, 1, bias, n_group, topk_group, scale)
+        return L.fl_moe_int4g_ex(fake, fake, 4, 256, E, k, 128, ctypes.byref(r), fake, fake, None, None, fake,
+                                 None, None, None, None, fake, 1 << 30, None)
+    assert moe_ex(8, 2, fl.FL_SOFTMAX, 0x20000, 1, 1, 1.0) == 1      # a bias needs sigmoid scoring
+    assert moe_ex(8, 2, fl.FL_SOFTMAX, None, 4, 2, 1.0) == 1         # so do groups
+    assert moe_ex(8, 2, fl.FL_SIGMOID, None, 3, 1, 1.0) == 1         # E % n_group
+    assert moe_ex(8, 3, fl.FL_SIGMOID, None, 4, 1, 1.0) == 1         # k > topk_group * E / n_group
+    assert moe_ex(8, 2, fl.FL_SIGMOID, None, 4, 5, 1.0) == 1         # topk_group > n_group
+    assert moe_ex(8, 2, fl.FL_SIGMOID, 0x20004, 1, 1, 1.0) == 1      # misaligned bias
+    assert moe_ex(8, 2, fl.FL_SIGMOID, None, 1, 1, 0.0) == 1         # routed_scale must be positive
+    assert moe_ex(8, 2, fl.FL_SIGMOID, None, 1, 1, float("inf")) == 1

@@ -233,3 +233,62 @@ def test_moe_group256_experts(M):
     ref, tol, rid, rw = O.moe(O.bf16_value(xb), logits, k, w13, w2, O.SOFTMAX, True, group=256)
     assert np.array_equal(ids.cpu().numpy(), rid)
     check_y(y, ref, tol)
+
+
+def _routing_case(M, E, k, H, I, layer):
+    w13, w2 = host_experts(E, H, I, layer)
+    w13_d, w2_d = stack_dev(w13, 2 * I, H), stack_dev(w2, H, I)
+    xb = inputs.activations(M, H, stream=layer)
+    logits = inputs.router_logits(M, E, stream=layer, hot=max(1, E // 5))
+    return w13, w2, w13_d, w2_d, xb, logits
+
+
+def _run_moe_ex(xb, logits, k, I, w13_d, w2_d, scoring, **opts):
+    M, H = xb.shape
+    E = logits.shape[1]
+    ids = torch.empty((M, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((M, k), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(fl.fl_moe_int4g_workspace(M, E, k, H, I, False), dtype=torch.uint8, device=DEV)
+    if opts.get("score_bias") is not None:
+        opts = dict(opts, score_bias=to_dev(opts["score_bias"]))
+    y = fl.fl_moe_int4g(bf16_dev(xb), to_dev(logits), k, I, w13_d, w2_d, scoring=scoring, renorm=True,
+                        topk_ids=ids, topk_w=wts, ws=ws, **opts)
+    torch.cuda.synchronize()
+    assert fl.fl_int4g_status(ws) == 0
+    return y, ids, wts
+
+
+@pytest.mark.parametrize("opts", [
+    {"n_group": 8, "topk_group": 4},
+    {"bias": True},
+    {"bias": True, "n_group": 8, "topk_group": 4, "routed_scale": 2.5},
+])
+def test_moe_deepseek_routing_options(opts):
+    """Sigmoid affinities with the selection bias, group-limited top-k (8
+    groups of 32, 4 kept) and the routed scale, on 256 small experts: ids
+    bit-exact (keys compared in double on both sides), weights within 1e-5
+    relative, y within the propagated bound."""
+    M, E, k, H, I = 96, 256, 8, 256, 128
+    w13, w2, w13_d, w2_d, xb, logits = _routing_case(M, E, k, H, I, layer=98)
+    ro = {"n_group": opts.get("n_group", 1), "topk_group": opts.get("topk_group", 1),
+          "scale": opts.get("routed_scale", 1.0)}
+    dev_opts = {"n_group": ro["n_group"], "topk_group": ro["topk_group"], "routed_scale": ro["scale"]}
+    if opts.get("bias"):
+        bias = (0.05 * np.random.default_rng([0, 6, 98]).standard_normal(E)).astype(np.float32)
+        ro["bias"] = bias
+        dev_opts["score_bias"] = bias
+    y, ids, wts = _run_moe_ex(xb, logits, k, I, w13_d, w2_d, O.SIGMOID, **dev_opts)
+    ref, tol, rid, rw = O.moe(O.bf16_value(xb), logits, k, w13, w2, O.SIGMOID, True, routing=ro)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.allclose(wts.cpu().numpy(), rw, rtol=1e-5, atol=0)
+    check_y(y, ref, tol)
+
+
+def test_moe_routed_scale_softmax():
+    M, E, k, H, I = 9, 8, 2, 256, 128
+    w13, w2, w13_d, w2_d, xb, logits = _routing_case(M, E, k, H, I, layer=99)
+    y, ids, wts = _run_moe_ex(xb, logits, k, I, w13_d, w2_d, O.SOFTMAX, routed_scale=2.5)
+    ref, tol, rid, rw = O.moe(O.bf16_value(xb), logits, k, w13, w2, O.SOFTMAX, True, routing={"scale": 2.5})
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.allclose(wts.cpu().numpy(), rw, rtol=1e-5, atol=0)
+    check_y(y, ref, tol)
