@@ -288,7 +288,6 @@ struct PfSeq {
     if (i < nh() + nt()) return ta + (i - nh());
     return hb + (i - nh() - nt());
   }
-  __device__ int seg_begin(int i) const { return i < nh() ? 0 : i < nh() + nt() ? nh() : nh() + nt(); }
   __device__ int seg_end(int i, int n) const { return i < nh() ? nh() : i < nh() + nt() ? nh() + nt() : n; }
 };
 
