@@ -74,8 +74,10 @@ def round_half_away(v):
 
 
 def fp16_bits(v):
-    """Correctly rounded (nearest even) double -> IEEE half, as uint16 bits."""
-    return np.asarray(v, dtype=np.float64).astype(np.float16).view(np.uint16)
+    """Correctly rounded (nearest even) double -> IEEE half, as uint16 bits.
+    Values beyond the half range give infinity (the callers test for it)."""
+    with np.errstate(over="ignore"):
+        return np.asarray(v, dtype=np.float64).astype(np.float16).view(np.uint16)
 
 
 def fp16_value(bits):
