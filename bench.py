@@ -451,32 +451,47 @@ print(json.dumps({{"bytes": tot_bytes, "seconds": t_all}}))
 """
 
 
-def cpu_baseline(rows=2048, min_seconds=10.0):
-    """The oracle's dequantized linear at M = 1, 8, 32 on a 2048-row slice of
-    each of the 4 Llama matrices, repeated until about 10 s of oracle time,
-    one thread, in a child process (BLAS pinned to 1 thread)."""
+def _oracle_sample(rows, min_seconds):
+    """Runs the bounded oracle sample in a child process (one thread, BLAS
+    pinned to 1 thread): {"bytes", "seconds"} of oracle work, or None and the
+    error text."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     code = _ORACLE_SAMPLE.format(root=ROOT, rows=rows, mats=LLAMA, min_seconds=min_seconds)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
+        return None, r.stderr[-300:]
+    return json.loads(r.stdout.strip().splitlines()[-1]), ""
+
+
+def cpu_baseline(rows=2048, min_seconds=10.0):
+    """The oracle's dequantized linear at M = 1, 8, 32 on a 2048-row slice of
+    each of the 4 Llama matrices, repeated until about 10 s of oracle time,
+    one thread, in a child process (BLAS pinned to 1 thread)."""
+    d, err = _oracle_sample(rows, min_seconds)
+    if d is None:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + err}
     return {"value": round(d["bytes"] / d["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"dequantized linear at M=1,8,32 on {rows} output rows of each Llama matrix, repeated "
                       f"({d['bytes'] / 1e6:.1f} MB of int4g weights in {d['seconds']:.2f} s of oracle time, float64 numpy)"}
 
 
 def run_reference(args):
-    """The CPU oracle as the reference arm: each step is the bounded sample."""
-    steps = []
+    """The CPU oracle as the reference arm: each step is the bounded sample;
+    value = its int4g weight bytes / its oracle time over the timed steps."""
+    nbytes, secs = 0.0, 0.0
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(rows=256, min_seconds=1.0)
+        d, err = _oracle_sample(256, 1.0)
+        if d is None:
+            last = err.strip().splitlines()[-1] if err.strip() else "no error text"
+            return {"impl": "reference", "unavailable": "the CPU oracle sample failed: " + last}
         if i >= args.warmup:
-            steps.append(cb["value"])
-    value = statistics.mean(steps)
+            nbytes += d["bytes"]
+            secs += d["seconds"]
+    value = round(nbytes / secs / 1e9, 4)
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / args.steps, 1),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
