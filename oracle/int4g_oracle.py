@@ -513,9 +513,11 @@ def expert_ffn(x, w13, w2, group=GROUP):
     w13 = (Q, S, Z) of [2I, H]: rows 0..I-1 gate, rows I..2I-1 up.
     w2  = (Q, S, Z) of [H, I].
     h = silu(G x) * (U x);  out = W2 h.
-    Returns (out [T, H], tol_out [T, H]) where tol_out bounds the error of a
-    path that computes both projections to the linear bound (2e-3 relative
-    to sum |a||w'|, fp32 accumulation) and stores h in bf16:
+    Returns (out [T, H], tol_out [T, H]) where tol_out bounds, to first
+    order, the error of a path that computes both projections to the linear
+    bound (2e-3 relative to sum |a||w'|, fp32 accumulation) and stores h in
+    bf16 (the worst case of that error model reaches it up to second-order
+    terms: products of two moves and the curvature of silu):
       tol_h = 2e-3 (|silu'(g)| A_g |u| + |silu(g)| A_u) + 2^-8 |h|
       tol_out = 2e-3 |h| |W2'|^T + tol_h |W2'|^T
     """

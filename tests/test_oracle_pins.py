@@ -532,3 +532,184 @@ def test_moe_single_expert_and_shared():
     ys, _, _, _ = O.moe(x, logits, 1, w13, w2, O.SIGMOID, True, shared_w13=sw13[0], shared_w2=sw2[0], group=8)
     assert np.allclose(ys[1], _brute_ffn(x[1], w13[1], w2[1], 8) + _brute_ffn(x[1], sw13[0], sw2[0], 8),
                        rtol=1e-12, atol=1e-15)
+
+
+# ------------------------------------------------------ MoE error bound
+#
+# The bound the MoE parity tests compare against (expert_ffn's tol_out and
+# moe's combined tol) is pinned three ways: a hand-worked expert whose every
+# term is written out below, a combine case whose weights and per-expert
+# bounds are known, and a brute-force perturbation of the whole expert FFN
+# in double that drives one output as far as the error model allows (each
+# dequantized weight moved by 2e-3 of itself, each stored h by 2^-8 of
+# itself, all signs chosen against that output): the deviation it reaches
+# must equal the bound to first order (sound, and not inflated).
+
+def _triple_from_codes(wdeq):
+    """Canonical triple with scale 1.0 (fp16 0x3C00) and zero point 8 whose
+    dequantized weights are the integer matrix `wdeq` (entries in -8..7);
+    one group per 2 columns."""
+    wdeq = np.asarray(wdeq, np.int64)
+    N, K = wdeq.shape
+    q = (wdeq + 8).astype(np.uint8)
+    S = np.full((N, K // 2), 0x3C00, np.uint16)
+    Z = O.pack_zeros(np.full((N, K // 2), 8, np.uint8))
+    return O.pack_codes(q), S, Z
+
+
+# x = (4, 4, 4, 4); gate rows give g = (0, 112), up rows u = (20, -4)
+_HAND_W13 = [[1, -1, 2, -2],    # gate 0: g0 = 4*(1-1+2-2) = 0,   A_g0 = 4*6  = 24
+             [7, 7, 7, 7],      # gate 1: g1 = 4*28 = 112,        A_g1 = 112
+             [1, 2, 3, -1],     # up 0:   u0 = 4*5 = 20,          A_u0 = 4*7  = 28
+             [-2, 1, 0, 0]]     # up 1:   u1 = -4,                A_u1 = 4*3  = 12
+_HAND_W2 = [[1, 2], [-3, 1], [0, -1], [2, 0]]
+_HAND_X = [4.0, 4.0, 4.0, 4.0]
+
+
+def test_expert_ffn_tolerance_hand_case():
+    """H = 4, I = 2, groups of 2, scale 1, zero point 8 (weights are the
+    integers above).  In double, sigma(112) == 1 exactly, so silu(112) = 112
+    and silu'(112) = 1; silu(0) = 0 and silu'(0) = 1/2.
+      h0 = silu(0) * 20 = 0,  h1 = 112 * (-4) = -448
+      tol_h0 = 2e-3 * (1/2 * 24 * 20 + 0 * 28) + 2^-8 * 0       = 0.48
+      tol_h1 = 2e-3 * (1 * 112 * 4 + 112 * 12) + 2^-8 * 448     = 3.584 + 1.75 = 5.334
+      out = W2' h = (-896, -448, 448, 0)
+      tol_out[n] = 2e-3 * sum_i |h_i| |W2'[n,i]| + sum_i tol_h_i |W2'[n,i]|
+        n=0: 2e-3*896 + 0.48*1 + 5.334*2 = 1.792 + 0.48 + 10.668 = 12.94
+        n=1: 2e-3*448 + 0.48*3 + 5.334*1 = 0.896 + 1.44 + 5.334  = 7.67
+        n=2: 2e-3*448 + 0.48*0 + 5.334*1 = 0.896 + 5.334         = 6.23
+        n=3: 2e-3*0   + 0.48*2 + 5.334*0                         = 0.96
+    """
+    w13 = _triple_from_codes(_HAND_W13)
+    w2 = _triple_from_codes(_HAND_W2)
+    x = np.array([_HAND_X])
+    out, tol = O.expert_ffn(x, w13, w2, group=2)
+    assert out[0].tolist() == [-896.0, -448.0, 448.0, 0.0]
+    assert np.allclose(tol[0], [12.94, 7.67, 6.23, 0.96], rtol=1e-13, atol=0)
+
+
+def test_moe_tolerance_combines_expert_bounds():
+    """k = 2 of E = 3 experts plus a shared expert, all built from the hand
+    expert: expert 0 is it, expert 1 is it with W2' negated (out -> -out, the
+    bound unchanged), expert 2 is never chosen, the shared expert is expert 0.
+    Logits (ln 3, 0, -3) give softmax weights w = (3/4, 1/4) up to the fp32
+    rounding of ln 3.  So
+      y   = w0 out - w1 out + out
+      tol = (w0 + w1) t + t + 1e-5 = 2 t + 1e-5 before the bf16 store,
+    widened by the store to tol (1 + 2^-8) + 2^-8 |y|."""
+    e0 = (_triple_from_codes(_HAND_W13), _triple_from_codes(_HAND_W2))
+    e1 = (_triple_from_codes(_HAND_W13), _triple_from_codes(-np.array(_HAND_W2)))
+    e2 = (_triple_from_codes(np.zeros((4, 4), int)), _triple_from_codes(np.zeros((4, 2), int)))
+    w13 = [e0[0], e1[0], e2[0]]
+    w2 = [e0[1], e1[1], e2[1]]
+    logits = np.array([[math.log(3.0), 0.0, -3.0]], np.float32)
+    y, tol, ids, w = O.moe(np.array([_HAND_X]), logits, 2, w13, w2, O.SOFTMAX, True,
+                           shared_w13=e0[0], shared_w2=e0[1], group=2)
+    assert ids.tolist() == [[0, 1]]
+    assert np.allclose(w[0], [0.75, 0.25], rtol=1e-7, atol=0)
+    out = np.array([-896.0, -448.0, 448.0, 0.0])
+    t = np.array([12.94, 7.67, 6.23, 0.96])
+    assert np.allclose(y[0], (w[0, 0] - w[0, 1] + 1.0) * out, rtol=1e-14, atol=0)
+    raw = 2.0 * t + 1e-5
+    assert np.allclose(tol[0], raw * (1 + 2 ** -8) + 2 ** -8 * np.abs(y[0]), rtol=1e-12, atol=0)
+
+
+def _dq(trip, group):
+    return O.dequantize(*trip, group=group)
+
+
+def _perturbed_expert_out(x, W13, W2, n, signs):
+    """One expert's output n on token x (float64 [H]) with every weight and
+    the stored h moved to the edge of the error model, in double, by plain
+    loops.  signs = None: the moves that push out[n] up (each move's sign is
+    that of its first-order effect on out[n]); else a dict of random signs."""
+    I = W13.shape[0] // 2
+    H = x.shape[0]
+
+    def sgm(a):
+        return 1.0 / (1.0 + math.exp(-a))
+
+    g = [sum(W13[i, c] * x[c] for c in range(H)) for i in range(I)]
+    u = [sum(W13[I + i, c] * x[c] for c in range(H)) for i in range(I)]
+    h = [g[i] * sgm(g[i]) * u[i] for i in range(I)]
+    acc = 0.0
+    for i in range(I):
+        s = sgm(g[i])
+        dsilu = s * (1.0 + g[i] * (1.0 - s))
+        if signs is None:
+            want = 1.0 if W2[n, i] >= 0 else -1.0               # direction that raises out[n]
+            sg = want * (1.0 if dsilu * u[i] >= 0 else -1.0)   # move of g that raises h in `want`
+            su = want * (1.0 if g[i] * s >= 0 else -1.0)
+            sh = want
+            sw = 1.0 if h[i] >= 0 else -1.0
+        else:
+            sg, su, sh, sw = signs["g"][i], signs["u"][i], signs["h"][i], signs["w2"][i]
+        # each gate/up weight moves by 2e-3 of itself; the direction per term
+        # makes the whole move of g (u) equal sg (su) * 2e-3 * sum |x| |w'|
+        gp = sum((W13[i, c] + sg * 2e-3 * abs(W13[i, c]) * (1.0 if x[c] >= 0 else -1.0)) * x[c]
+                 for c in range(H))
+        up = sum((W13[I + i, c] + su * 2e-3 * abs(W13[I + i, c]) * (1.0 if x[c] >= 0 else -1.0))
+                 * x[c] for c in range(H))
+        hp = gp * sgm(gp) * up + sh * 2.0 ** -8 * abs(h[i])      # the bf16 store of h
+        acc += (W2[n, i] + sw * 2e-3 * abs(W2[n, i])) * hp
+    return acc
+
+
+def _moe_case(seed, E=3, H=8, I=4, group=4, M=2, k=2):
+    rng = np.random.default_rng([0, 40, seed])
+    w13 = [O.quantize((rng.standard_normal((2 * I, H)) * 0.3).astype(np.float32), group) for _ in range(E + 1)]
+    w2 = [O.quantize((rng.standard_normal((H, I)) * 0.3).astype(np.float32), group) for _ in range(E + 1)]
+    x = rng.standard_normal((M, H)) * 2.0
+    logits = rng.standard_normal((M, E)).astype(np.float32)
+    return w13, w2, x, logits
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_moe_tolerance_sound_and_tight_under_worst_case_moves(seed):
+    """For every output of a small routed layer with a shared expert, the
+    worst-case moves of the error model (weights 2e-3, stored h 2^-8, routed
+    outputs added with their gate weights) give a deviation within the
+    oracle's bound before the bf16 store of y up to second-order terms, and
+    at least 0.99 of it: the bound is the first-order worst case of that
+    error model, so the two differ only by second-order terms (products of
+    two moves, the curvature of silu; measured within 0.4% here) and the
+    1e-5 floor.  Dropping a term, a gate weight or the silu derivative moves
+    the ratio far outside [0.99, 1.01]."""
+    group, k = 4, 2
+    w13, w2, x, logits = _moe_case(seed, group=group, k=k)
+    E = len(w13) - 1
+    y, tol, ids, w = O.moe(x, logits, k, w13[:E], w2[:E], O.SIGMOID, True,
+                           shared_w13=w13[E], shared_w2=w2[E], group=group)
+    raw = (tol - 2.0 ** -8 * np.abs(y)) / (1 + 2.0 ** -8)     # bound before the bf16 store
+    M, H = y.shape
+    for t in range(M):
+        experts = [(int(ids[t, j]), float(w[t, j])) for j in range(k)] + [(E, 1.0)]
+        for n in range(H):
+            dev = 0.0
+            for e, wt in experts:
+                W13, W2 = _dq(w13[e], group), _dq(w2[e], group)
+                base = _perturbed_expert_out(x[t], W13 * 0, W2 * 0, n, None)   # 0: keeps the loop honest
+                assert base == 0.0
+                hi = _perturbed_expert_out(x[t], W13, W2, n, None)
+                ex = float((W2 @ (O.silu(W13[:W13.shape[0] // 2] @ x[t]) * (W13[W13.shape[0] // 2:] @ x[t])))[n])
+                dev += wt * (hi - ex)
+            ratio = dev / (raw[t, n] - 1e-5)
+            assert ratio <= 1.01, f"bound not sound at ({t},{n}): {dev} > {raw[t, n]}"
+            assert ratio >= 0.99, f"bound inflated at ({t},{n}): {dev} << {raw[t, n]}"
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_expert_ffn_tolerance_sound_under_random_moves(seed):
+    """Random directions of the same moves stay within expert_ffn's bound."""
+    group = 4
+    w13, w2, x, _ = _moe_case(10 + seed, group=group)
+    rng = np.random.default_rng([0, 41, seed])
+    out, tol = O.expert_ffn(x, w13[0], w2[0], group)
+    W13, W2 = _dq(w13[0], group), _dq(w2[0], group)
+    I = W13.shape[0] // 2
+    for t in range(x.shape[0]):
+        for n in range(W2.shape[0]):
+            for _ in range(5):
+                signs = {key: rng.choice([-1.0, 1.0], size=I) for key in ("g", "u", "h", "w2")}
+                d = abs(_perturbed_expert_out(x[t], W13, W2, n, signs) - out[t, n])
+                assert d <= tol[t, n] * (1 + 1e-9)
