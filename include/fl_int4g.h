@@ -156,20 +156,43 @@ int fl_int4g_linear(const void* x, int M, int K, const void* w, int N,
  * callers that cannot allocate device memory where they call (cudaMalloc can
  * synchronize the device or fail under memory pressure, so latency-critical
  * loops and code inside frameworks that own all allocations avoid it).
- * Same arguments and result as fl_int4g_linear for M <= 32; the split-K
- * scratch lives in a 16 MiB array inside the library that every GPU loading
- * the library holds until exit.
+ * Same arguments, same kernels and the same result, bit for bit, as
+ * fl_int4g_linear for M <= 32; the split-K scratch lives in a 16 MiB array
+ * inside the library that every GPU loading the library holds until exit.
  *  - The first call on a device looks up that array's device address
  *    (cudaGetSymbolAddress) with the device current: make it before any
- *    stream capture.
- *  - Each call clears the array's status and counter region on `stream`
- *    (cudaMemsetAsync) before the kernel; all calls share the array, so calls
- *    whose executions overlap on the GPU (different streams, or graphs
- *    launched concurrently) race and must be serialized by the caller.
+ *    stream capture.  The address is cached per device and is not refreshed
+ *    after a device reset: do not use this variant across one.
+ *  - Every call shares the array, which keeps the last call's contents:
+ *    calls whose executions overlap on the GPU (different streams, or graphs
+ *    launched concurrently) race and must be serialized by the caller.  A
+ *    successful call leaves the array's counters zero for the next one.
+ *  - Device-side conditions (FL_ERR_TIMEOUT) are recorded in the array's
+ *    status block: read them with fl_int4g_linear_noalloc_status before the
+ *    next call on the device if they matter.
  *  - FL_ERR_UNSUPPORTED for M > 32; FL_ERR_WORKSPACE when the shape needs more
  *    scratch than the 16 MiB array (large N at M = 32); FL_ERR_ARG as for
- *    fl_int4g_linear.  Device-side status is not reported by this variant. */
+ *    fl_int4g_linear. */
 int fl_int4g_linear_noalloc(const void* x, int M, int K, const void* w, int N, void* y, fl_stream_t stream);
+
+/* Reads and clears the device status block of fl_int4g_linear_noalloc's
+ * array on the current device (as fl_int4g_status does for a workspace);
+ * when an error was recorded it also clears the array's ticket counters, so
+ * that the next call starts clean.  Synchronizes `stream`. */
+int fl_int4g_linear_noalloc_status(fl_stream_t stream, int* out);
+
+/* Test hook of the device-side failure path (no counterpart on the pages:
+ * the library never traps or faults; a wait that runs out is reported).
+ * ns >= 0: every later decode launch of fl_int4g_linear /
+ * fl_int4g_linear_noalloc that reduces its row tiles across a thread-block
+ * cluster withholds one arrival from each tile's reduction barrier, so the
+ * bounded wait of the tile's first CTA runs out after ns nanoseconds.  That
+ * CTA records FL_ERR_TIMEOUT in the status block, makes the missing arrival
+ * itself, waits (normal bound) until its peers' partial sums have landed in
+ * its shared memory, and exits without writing its rows of y.  ns < 0 (the
+ * default) turns the hook off.  Process-wide; for tests only.  Always
+ * FL_OK. */
+int fl_int4g_test_withhold_cluster_arrival(long long ns);
 
 /* ------------------------------------------------------- a5-a7: MoE layer */
 

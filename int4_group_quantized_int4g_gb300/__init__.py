@@ -17,7 +17,8 @@ __all__ = [
     "lib", "Int4gError", "FL_SOFTMAX", "FL_SIGMOID", "GROUP",
     "fl_strerror", "fl_int4g_version", "fl_int4g_status",
     "fl_int4g_quantize", "fl_int4g_repacked_bytes", "fl_int4g_repack", "fl_int4g_unrepack",
-    "fl_int4g_linear_workspace", "fl_int4g_linear", "fl_int4g_linear_noalloc",
+    "fl_int4g_linear_workspace", "fl_int4g_linear", "fl_int4g_linear_noalloc", "fl_int4g_linear_noalloc_status",
+    "fl_int4g_test_withhold_cluster_arrival",
     "fl_moe_int4g_workspace", "fl_moe_int4g", "FlMoeRouting",
 ]
 
@@ -48,6 +49,8 @@ SIGNATURES = {
     "fl_int4g_linear_workspace": (_i, [_i, _i, _i, _c_size_p]),
     "fl_int4g_linear": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
     "fl_int4g_linear_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp]),
+    "fl_int4g_linear_noalloc_status": (_i, [_vp, ctypes.POINTER(_i)]),
+    "fl_int4g_test_withhold_cluster_arrival": (_i, [ctypes.c_longlong]),
     "fl_moe_int4g_workspace": (_i, [_i, _i, _i, _i, _i, _i, _c_size_p]),
     "fl_moe_int4g": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
                           _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
@@ -209,6 +212,21 @@ def fl_int4g_linear_noalloc(x, w, N, y=None):
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _check("fl_int4g_linear_noalloc", lib().fl_int4g_linear_noalloc(_p(x), M, K, _p(w), N, _p(y), _stream()))
     return y
+
+
+def fl_int4g_linear_noalloc_status(stream=None):
+    """Reads and clears the status block of fl_int4g_linear_noalloc's
+    library-held array on the current device (synchronizes the stream)."""
+    out = ctypes.c_int(0)
+    _check("fl_int4g_linear_noalloc_status", lib().fl_int4g_linear_noalloc_status(_stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def fl_int4g_test_withhold_cluster_arrival(ns):
+    """Test hook: ns >= 0 makes the cluster reductions of later decode
+    launches withhold one arrival, so their bounded wait runs out after ns
+    nanoseconds and FL_ERR_TIMEOUT is recorded; ns < 0 turns it off."""
+    lib().fl_int4g_test_withhold_cluster_arrival(int(ns))
 
 
 def fl_moe_int4g_workspace(M, E, k, H, I, has_shared):

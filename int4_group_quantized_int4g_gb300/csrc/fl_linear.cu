@@ -20,6 +20,7 @@
 //    for A and B, which leaves the dot product unchanged); (128 + z) times
 //    the group's sum of x is subtracted afterwards and the fp16 scale
 //    applied to the fp32 group sum (M <= 16; larger M subtracts z per pair).
+#include <atomic>
 #include <mutex>
 
 #include "fl_common.cuh"
@@ -53,6 +54,8 @@ struct RowsParams {
   int csize;         // > 1: clusters of csize CTAs split one row tile over K (DSMEM reduction)
   uint32_t red_off;  // shared-memory offset of the cluster reduction barrier and buffer
   uint32_t zrow_off; // shared-memory offset of 256 zero bytes (x rows of absent tokens)
+  unsigned long long red_wait_ns;  // bound of rank 0's wait for its peers' partial sums
+  int withhold;      // test hook: the reduction barrier expects one arrival nobody makes
 };
 
 // CTA c owns units [unit_begin(c), unit_begin(c+1)); cta_of_unit inverts it.
@@ -167,8 +170,13 @@ __device__ __forceinline__ void cluster_reduce(const RowsParams& p, int T, int r
     if (lane == 0) mbar_arrive_remote_rank0(red_bar);
     return;
   }
-  if (!mbar_wait_cluster(red_bar, 0)) {
+  if (!mbar_wait_cluster(red_bar, 0, p.red_wait_ns)) {
     if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 4);
+    // (test hook) the withheld arrival, made once the wait has run out
+    if (p.withhold && warp == 0 && lane == 0) mbar_arrive(red_bar);
+    // the peers write into this CTA's shared memory: it stays until they are
+    // done (normal bound), then leaves without writing its rows of y
+    mbar_wait_cluster(red_bar, 0);
     return;
   }
   float acc[NT][4];
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
-    if (p.csize > 1) mbar_init(red_bar, (p.csize - 1) * kConsumerWarps);
+    if (p.csize > 1) mbar_init(red_bar, (p.csize - 1) * kConsumerWarps + (p.withhold ? 1 : 0));
     fence_mbar_init();
   }
   if (threadIdx.x < 16) reinterpret_cast<uint4*>(smem + p.zrow_off)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
@@ -567,6 +575,16 @@ int launch_rows(const RowsPlan& pl, const RowsParams& prm, cudaStream_t s) {
 
 }  // namespace
 
+// Test hook of the failure path (fl_int4g_test_withhold_cluster_arrival):
+// < 0 off; otherwise the wait bound in ns of the cluster reductions of the
+// following decode launches, which withhold one arrival.
+static std::atomic<long long> g_withhold_ns{-1};
+
+extern "C" int fl_int4g_test_withhold_cluster_arrival(long long ns) {
+  g_withhold_ns.store(ns < 0 ? -1 : ns);
+  return FL_OK;
+}
+
 // Shared with the MoE and prefill launchers.
 int fl_linear_rows_workspace(int M, int N, int K, size_t* out) {
   RowsPlan pl;
@@ -607,6 +625,9 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   prm.csize = pl.csize;
   prm.red_off = pl.red_off;
   prm.zrow_off = pl.zrow_off;
+  const long long hook = g_withhold_ns.load();
+  prm.withhold = (hook >= 0 && pl.csize > 1) ? 1 : 0;
+  prm.red_wait_ns = prm.withhold ? static_cast<unsigned long long>(hook) : kWaitLimitNs;
   switch (pl.NT) {
     case 1: return pl.minb == 3 ? launch_rows<1, 2, 3>(pl, prm, stream) : launch_rows<1, 2, 2>(pl, prm, stream);
     case 2: return launch_rows<2, 2, 1>(pl, prm, stream);
@@ -642,14 +663,31 @@ static bool tcdec_plan(int M, int N, int K, size_t* cnt_off, size_t* part_off, s
   return true;
 }
 
+// Decode part of the linear (1 <= M <= 32), shared by fl_int4g_linear and
+// the variant that allocates nothing: workspace bytes, and the dispatch.
+int fl_linear_decode_workspace(int M, int N, int K, size_t* out) {
+  size_t a, b;
+  return tcdec_plan(M, N, K, &a, &b, out) ? FL_OK : FL_ERR_ARG;
+}
+
+int fl_linear_decode(const void* x, int M, int K, const void* w, int N, void* y, void* ws, size_t ws_bytes,
+                     cudaStream_t s) {
+  size_t cnt_off, part_off, need;
+  if (!tcdec_plan(M, N, K, &cnt_off, &part_off, &need)) return FL_ERR_ARG;
+  if (ws_bytes < need) return FL_ERR_WORKSPACE;
+  // M <= 8: the register-dequant mma.sync stream is faster (one warp hand-off
+  // per two super-blocks); 8 < M <= 32: tcgen05 (mma.sync issue-bound there)
+  if (M <= 8) return fl_linear_rows(x, M, K, w, N, y, ws, ws_bytes, s);
+  return fl_linear_tcdec(x, M, K, w, N, y, ws, cnt_off, part_off, s);
+}
+
 extern "C" int fl_int4g_linear_workspace(int M, int N, int K, size_t* out) {
   if (!out || M < 1 || N < 1 || K < kGroup || K % kGroup) return FL_ERR_ARG;
   if (M > kMaxTokens) {
     *out = fl_linear_tc_workspace(M);
     return FL_OK;
   }
-  size_t a, b;
-  return tcdec_plan(M, N, K, &a, &b, out) ? FL_OK : FL_ERR_ARG;
+  return fl_linear_decode_workspace(M, N, K, out);
 }
 
 extern "C" int fl_int4g_linear(const void* x, int M, int K, const void* w, int N, void* y, void* ws,
@@ -660,11 +698,5 @@ extern "C" int fl_int4g_linear(const void* x, int M, int K, const void* w, int N
     if (ws_bytes < fl_linear_tc_workspace(M)) return FL_ERR_WORKSPACE;
     return fl_linear_tc(x, M, K, w, N, y, ws, s);
   }
-  size_t cnt_off, part_off, need;
-  if (!tcdec_plan(M, N, K, &cnt_off, &part_off, &need)) return FL_ERR_ARG;
-  if (ws_bytes < need) return FL_ERR_WORKSPACE;
-  // M <= 8: the register-dequant mma.sync stream is faster (one warp hand-off
-  // per two super-blocks); 8 < M <= 32: tcgen05 (mma.sync issue-bound there)
-  if (M <= 8) return fl_linear_rows(x, M, K, w, N, y, ws, ws_bytes, s);
-  return fl_linear_tcdec(x, M, K, w, N, y, ws, cnt_off, part_off, s);
+  return fl_linear_decode(x, M, K, w, N, y, ws, ws_bytes, s);
 }

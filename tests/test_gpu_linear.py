@@ -238,6 +238,50 @@ def test_linear_llama_decode_sampled(KN):
         assert np.sqrt(np.mean((got - ref) ** 2) / np.mean(ref ** 2)) <= 1e-2
 
 
+@pytest.mark.parametrize("M", [1, 8])
+def test_linear_stream_k_many_row_tiles(M):
+    """A vocabulary-sized decode linear (K=4096, N=32000: 250 row tiles, more
+    than half the CTA slots) takes the stream-K split with the ticket
+    hand-off instead of cluster reductions; 96 sampled columns, the first
+    and the last, against the oracle."""
+    K, N = 4096, 32000
+    W = inputs.dense_weight(N, K, layer=N + M)
+    q, s, z = quantize_dev(W)
+    w = fl.fl_int4g_repack(q, s, z, N, K)
+    cols = np.unique(np.concatenate([np.sort(inputs.rng(8, K, N).choice(N, 96, replace=False)), [0, N - 1]]))
+    Qc, Sc, Zc = O.quantize(W[cols])
+    xb = inputs.activations(M, K, stream=N + M)
+    ws = torch.zeros(fl.fl_int4g_linear_workspace(M, N, K), dtype=torch.uint8, device=DEV)
+    for _ in range(2):   # the tickets are left zero for the next call
+        y = fl.fl_int4g_linear(bf16_dev(xb), w, N, ws=ws)
+        xf = O.bf16_value(xb)
+        ref, tol = O.linear_columns(xf, Qc, Sc, Zc, np.arange(len(cols)))
+        got = y.float().cpu().numpy().astype(np.float64)[:, cols]
+        assert np.all(np.abs(got - ref) <= tol), (M, np.max(np.abs(got - ref) / tol))
+    assert fl.fl_int4g_status(ws) == 0
+
+
+def test_cluster_reduction_timeout_is_reported():
+    """The failure path of the decode kernel's bounded inter-CTA wait, made
+    to run out by the test hook (a barrier arrival nobody makes, 1 ms
+    bound): the status block reports FL_ERR_TIMEOUT, the kernel returns (no
+    hang, no fault), and the same workspace then serves a normal call."""
+    M, N, K = 1, 200, 1024   # 2 row tiles: each split over K by a cluster of 8 CTAs
+    _, xb, Q, S, Z, w = _linear_case(M, N, K, layer=72)
+    x = bf16_dev(xb)
+    ws = torch.zeros(fl.fl_int4g_linear_workspace(M, N, K), dtype=torch.uint8, device=DEV)
+    fl.fl_int4g_test_withhold_cluster_arrival(1_000_000)
+    try:
+        fl.fl_int4g_linear(x, w, N, ws=ws)
+        torch.cuda.synchronize()
+    finally:
+        fl.fl_int4g_test_withhold_cluster_arrival(-1)
+    assert fl.fl_int4g_status(ws) == 5
+    y = fl.fl_int4g_linear(x, w, N, ws=ws)
+    _check(y, xb, Q, S, Z)
+    assert fl.fl_int4g_status(ws) == 0
+
+
 def test_linear_one_workspace_across_shapes():
     """One workspace serves shapes with different tile counts in turn: a call
     must not find the previous shape's scratch where its counters are."""

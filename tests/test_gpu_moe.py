@@ -182,36 +182,114 @@ class LazyTriples:
 def sampled_check(ex, xb, logits, k, scoring, y, ids, sample):
     w13 = LazyTriples(ex, 0)
     w2 = LazyTriples(ex, 1)
-    sw13 = ex.oracle_triples(ex.E, 0) if ex.sw13 is not None else None
-    sw2 = ex.oracle_triples(ex.E, 1) if ex.sw2 is not None else None
+    # the oracle quantizes every expert the sampled tokens reach, in parallel
+    need = sorted(set(ids.cpu().numpy()[sample].reshape(-1).tolist()))
+    from oracle_pool import quantize_many
+    jobs = [(e, which) for e in need for which in (0, 1)]
+    if ex.sw13 is not None:
+        jobs += [(ex.E, 0), (ex.E, 1)]
+    trips = quantize_many(lambda i: ex.fp32(*jobs[i]).cpu().numpy(), len(jobs))
+    for (e, which), t in zip(jobs, trips):
+        (w13 if which == 0 else w2).cache[e] = t
+    sw13 = w13.cache[ex.E] if ex.sw13 is not None else None
+    sw2 = w2.cache[ex.E] if ex.sw2 is not None else None
     ref, tol, rid, _ = O.moe(O.bf16_value(xb[sample]), logits[sample], k, w13, w2, scoring, True, sw13, sw2)
     assert np.array_equal(ids.cpu().numpy()[sample], rid)
     check_y(y, ref, tol, rows=sample)
 
 
+def covering_sample(ids, hot, extra=()):
+    """Tokens to check at full size: greedily, until every expert of `hot`
+    that received a token is covered; plus a token of the first and of the
+    last routed expert (the first and last segments of the grouped kernels),
+    the first and the last token, and `extra`."""
+    ids = np.asarray(ids)
+    M = ids.shape[0]
+    want = set(int(e) for e in hot) & set(ids.reshape(-1).tolist())
+    chosen = [0, M - 1]
+    lo, hi = int(ids.min()), int(ids.max())
+    chosen.append(int(np.nonzero((ids == lo).any(axis=1))[0][0]))
+    chosen.append(int(np.nonzero((ids == hi).any(axis=1))[0][-1]))
+    chosen += list(extra)
+    for t in chosen:
+        want -= set(ids[t].tolist())
+    while want:
+        gain = np.array([len(want & set(row.tolist())) for row in ids])
+        t = int(np.argmax(gain))
+        chosen.append(t)
+        want -= set(ids[t].tolist())
+    return np.unique(chosen)
+
+
 def test_moe_qwen3_shaped():
-    """128 experts, hidden 2048, intermediate 768, top-8 softmax; M in {1, 64, 256}."""
+    """128 experts, hidden 2048, intermediate 768, top-8 softmax; M in {1, 64,
+    256} (M = 256 runs the grouped tensor-memory GEMM).  Sampled tokens: the
+    first and last, a token of the first and of the last routed expert, and
+    16 more spread over the batch."""
     ex = DeviceExperts(128, 2048, 768, layer=700, shared=False)
     for M in (1, 64, 256):
         xb = inputs.activations(M, 2048, stream=700 + M)
         logits = inputs.router_logits(M, 128, stream=700 + M)
         y, ids, wts, offs, perm = run_moe(xb, logits, 8, 768, ex.w13, ex.w2, fl.FL_SOFTMAX, True)
         check_routing(logits, 8, fl.FL_SOFTMAX, True, ids, wts, offs, perm)
-        sample = np.unique([0, M - 1])
+        spread = np.linspace(0, M - 1, 16).astype(int) if M > 16 else np.arange(M)
+        sample = covering_sample(ids.cpu().numpy(), [], extra=spread)
         sampled_check(ex, xb, logits, 8, O.SOFTMAX, y, ids, sample)
 
 
-def test_moe_deepseek_shaped():
+@pytest.mark.parametrize("M", [1, 16, 128, 512, 1024])
+def test_moe_deepseek_shaped(M, deepseek_experts):
     """256 routed experts + 1 shared, hidden 7168, intermediate 2048, top-8
-    sigmoid renormalised, skewed logits; M in {1, 16, 512} (sampled tokens;
-    M = 512 runs the grouped tensor-memory GEMM path)."""
+    sigmoid renormalised, logits skewed to 51 hot experts; M in {1, 16, 128,
+    512, 1024} (M >= 128 runs the grouped tensor-memory GEMM).  Sampled
+    tokens: every hot expert that received a token is covered by at least
+    one of them, plus the first and last token and a token of the first and
+    of the last routed expert (the grouped kernels' first and last
+    segments; the shared expert's segments hold every token)."""
+    ex = deepseek_experts
+    xb = inputs.activations(M, 7168, stream=800 + M)
+    logits = inputs.router_logits(M, 256, stream=800 + M, hot=51)
+    y, ids, wts, offs, perm = run_moe(xb, logits, 8, 2048, ex.w13, ex.w2, fl.FL_SIGMOID, True, ex.sw13, ex.sw2)
+    check_routing(logits, 8, fl.FL_SIGMOID, True, ids, wts, offs, perm)
+    sample = covering_sample(ids.cpu().numpy(), inputs.hot_experts(256, 51))
+    sampled_check(ex, xb, logits, 8, O.SIGMOID, y, ids, sample)
+
+
+@pytest.fixture(scope="module")
+def deepseek_experts():
     ex = DeviceExperts(256, 7168, 2048, layer=800, shared=True)
-    for M in (1, 16, 512):
-        xb = inputs.activations(M, 7168, stream=800 + M)
-        logits = inputs.router_logits(M, 256, stream=800 + M, hot=51)
-        y, ids, wts, offs, perm = run_moe(xb, logits, 8, 2048, ex.w13, ex.w2, fl.FL_SIGMOID, True, ex.sw13, ex.sw2)
-        check_routing(logits, 8, fl.FL_SIGMOID, True, ids, wts, offs, perm)
-        sampled_check(ex, xb, logits, 8, O.SIGMOID, y, ids, np.array([M - 1]))
+    yield ex
+    del ex
+    torch.cuda.empty_cache()
+
+
+def test_moe_nan_logit_is_reported():
+    """A NaN router logit is a device-side check failure (FL_ERR_DEVICE_CHECK
+    in the status block); the NaN expert counts as -inf, so the routing of
+    that token still picks valid experts and nothing is read out of bounds."""
+    E, H, I, k, M = 8, 256, 128, 2, 4
+    w13, w2 = host_experts(E, H, I, layer=96)
+    xb = inputs.activations(M, H, stream=96)
+    logits = inputs.router_logits(M, E, stream=96)
+    logits[2, 5] = np.nan
+    ids = torch.empty((M, k), dtype=torch.int32, device=DEV)
+    ws = torch.zeros(fl.fl_moe_int4g_workspace(M, E, k, H, I, False), dtype=torch.uint8, device=DEV)
+    fl.fl_moe_int4g(bf16_dev(xb), to_dev(logits), k, I, stack_dev(w13, 2 * I, H), stack_dev(w2, H, I),
+                    topk_ids=ids, ws=ws)
+    torch.cuda.synchronize()
+    assert fl.fl_int4g_status(ws) == 6
+    got = ids.cpu().numpy()
+    assert np.all((got >= 0) & (got < E)) and 5 not in got[2].tolist()
+    clean = logits.copy()
+    clean[2, 5] = -np.inf
+    rid, _ = O.route(clean, k, O.SOFTMAX, True)
+    assert np.array_equal(got, rid)
+    # the same workspace serves a clean call afterwards
+    logits[2, 5] = 0.0
+    y, ids, wts, offs, perm = run_moe(xb, logits, k, I, stack_dev(w13, 2 * I, H), stack_dev(w2, H, I),
+                                      fl.FL_SOFTMAX, True)
+    ref, tol, _, _ = O.moe(O.bf16_value(xb), logits, k, w13, w2, O.SOFTMAX, True)
+    check_y(y, ref, tol)
 
 
 @pytest.mark.parametrize("M", [5, 64])
