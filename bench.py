@@ -285,6 +285,52 @@ def run_gemm_section(torch, np, fl, inputs, dev, pk):
     return out
 
 
+def _mlp_copies(torch, fl, inputs, dev, H, I, copies, layer0):
+    out = []
+    for i in range(copies):
+        out.append(tuple(_weight_copies(torch, fl, inputs, dev, K, N, 1, layer0 + 10 * i + j)[0]
+                         for j, (K, N) in enumerate([(H, I), (H, I), (I, H)])))
+    return out
+
+
+def run_mlp_section(torch, np, fl, inputs, dev, pk, Ms=(1, 8)):
+    """Llama-7B MLP block (H=4096, I=11008: gate, up, down; 70.3 MB of int4g
+    weights) at M in {1, 8}: the fused block (fl_int4g_mlp, one launch) and,
+    for comparison, the same three matrices as three fl_int4g_linear calls
+    (SwiGLU not applied there).  4 weight copies (281 MB) in one CUDA graph,
+    replayed 30 times."""
+    H, I = 4096, 11008
+    copies = _mlp_copies(torch, fl, inputs, dev, H, I, 4, 5000)
+    wb = BYTES_PER_WEIGHT * 3 * H * I
+    stream = torch.cuda.Stream(device=dev)
+    out = {}
+    for M in Ms:
+        x = torch.from_numpy(inputs.activations(M, H, stream=M).view(np.int16)).to(dev).view(torch.bfloat16)
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(fl.fl_int4g_mlp_workspace(M, H, I), dtype=torch.uint8, device=dev)
+        ms = _graph_time_per_launch(torch, [lambda c=c: fl.fl_int4g_mlp(x, c[0], c[1], c[2], I, y=y, ws=ws)
+                                            for c in copies], stream, 30)
+        assert fl.fl_int4g_status(ws) == 0
+        hx = torch.from_numpy(inputs.activations(M, I, stream=M).view(np.int16)).to(dev).view(torch.bfloat16)
+        gu = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
+        lw = torch.zeros(max(fl.fl_int4g_linear_workspace(M, I, H), fl.fl_int4g_linear_workspace(M, H, I)),
+                         dtype=torch.uint8, device=dev)
+        launches = []
+        for c in copies:
+            launches += [lambda c=c: fl.fl_int4g_linear(x, c[0], I, y=gu, ws=lw),
+                         lambda c=c: fl.fl_int4g_linear(x, c[1], I, y=gu, ws=lw),
+                         lambda c=c: fl.fl_int4g_linear(hx, c[2], H, y=y, ws=lw)]
+        ms3 = _graph_time_per_launch(torch, launches, stream, 30) * 3
+        out[str(M)] = {"us_per_block": round(ms * 1e3, 3), "weight_GBps": round(wb / (ms * 1e-3) / 1e9, 1),
+                       "hbm_frac_of_measured": round(wb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                       "three_linear_calls_us": round(ms3 * 1e3, 3),
+                       "three_linear_calls_GBps": round(wb / (ms3 * 1e-3) / 1e9, 1)}
+    del copies
+    torch.cuda.empty_cache()
+    out["timing"] = "graph of 4 blocks over 4 weight copies (281 MB), 30 replays; weight bytes 70.3 MB per block"
+    return out
+
+
 def input_digests(np, calls):
     """numpy / torch versions and SHA-256 (first 16 hex digits) of each decode
     call's inputs: x (bf16 bits) and the interleaved weights."""
@@ -457,7 +503,8 @@ def run_gpu(args, barrier=None):
     e2e_value = wbytes / (e2e_ms * 1e-3) / 1e9
 
     inputs_digest = input_digests(np, calls)
-    sections = {"gemv_qwen3_up": run_gemv_config1(torch, np, fl, inputs, dev, pk)}
+    sections = {"gemv_qwen3_up": run_gemv_config1(torch, np, fl, inputs, dev, pk),
+                "mlp_block": run_mlp_section(torch, np, fl, inputs, dev, pk)}
     if not args.no_sections:
         sections["moe"] = run_moe_section(torch, np, fl, inputs, dev, pk, reps=5)
         sections["gemm"] = run_gemm_section(torch, np, fl, inputs, dev, pk)
@@ -653,9 +700,10 @@ def run_reference(args):
 
 
 def run_case(args):
-    """One shape on its own (profiling): --case linear --M --K --N.  Enough
-    weight copies to exceed 2x L2 are launched back to back in one CUDA graph;
-    reports the mean time per launch."""
+    """One shape on its own (profiling): --case linear --M --K --N, or --case
+    mlp --M (the Llama-7B MLP block).  Enough weight copies to exceed 2x L2
+    are launched back to back in one CUDA graph; reports the mean time per
+    launch."""
     import numpy as np
     import torch
 
@@ -665,6 +713,10 @@ def run_case(args):
     _build.build()
     fl.lib()
     dev = torch.device("cuda:0")
+    if args.case == "mlp":
+        print(json.dumps({"case": f"mlp M={args.M}", **run_mlp_section(torch, np, fl, inputs, dev, peaks(),
+                                                                        Ms=(args.M,))}))
+        return
     M, K, N = args.M, args.K, args.N
     nb = BYTES_PER_WEIGHT * N * K
     copies = max(1, min(64, int(np.ceil(300e6 / nb))))
@@ -709,7 +761,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sections", action="store_true", help="skip the MoE and prefill GEMM sections")
-    ap.add_argument("--case", choices=["linear"], help="time one shape on its own (profiling)")
+    ap.add_argument("--case", choices=["linear", "mlp"], help="time one shape on its own (profiling)")
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--K", type=int, default=4096)
     ap.add_argument("--N", type=int, default=12288)

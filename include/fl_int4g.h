@@ -48,10 +48,14 @@
  *  - Every call is asynchronous on `stream` (0 = legacy default stream) and
  *    allocates no memory: the caller owns all buffers, including the
  *    workspaces whose sizes the *_workspace queries return.
- *  - Workspaces must be zero-filled before their first use.  A successful
- *    call leaves the workspace zero-filled again except for its scratch
- *    areas, so one workspace can be reused by consecutive calls on one
- *    stream.  Calls that run concurrently must not share a workspace.
+ *  - Workspaces must be zero-filled before their first use.  Every entry
+ *    point lays its workspace out the same way: a 16-byte status block, a
+ *    counter region (up to byte 262,400) that a successful call leaves
+ *    zero-filled again, and scratch after it.  So one workspace, sized for
+ *    the largest query, can be reused by consecutive calls of any entry
+ *    points on one stream.  Calls that run concurrently must not share a
+ *    workspace; after a call reports a device-side error, zero the
+ *    workspace again before reusing it.
  *  - The first 16 bytes of every workspace are a device status block; kernels
  *    OR error bits into it instead of trapping.  fl_int4g_status reads and
  *    clears it.
@@ -181,6 +185,28 @@ int fl_int4g_linear_noalloc(const void* x, int M, int K, const void* w, int N, v
  * that the next call starts clean.  Synchronizes `stream`. */
 int fl_int4g_linear_noalloc_status(fl_stream_t stream, int* out);
 
+/* --------------------------------------- f3: fused decode MLP block */
+
+/* Workspace bytes needed by fl_int4g_mlp. */
+int fl_int4g_mlp_workspace(int M, int H, int I, size_t* out);
+
+/* Decode MLP block in one launch, for 1 <= M <= 8 tokens:
+ *   h = silu(G x) * (U x)  (h stored as bf16),   y = D h,
+ * every product an int4g linear as in fl_int4g_linear (FastLLM page,
+ * section 3.1; fastllm README, section 2: --dtype int4g applies to every
+ * linear of the model).
+ *   x       bf16 [M, H] device          y  bf16 [M, H] device
+ *   w_gate  interleaved layout of G [I, H]     w_up  of U [I, H]
+ *   w_down  interleaved layout of D [H, I]     ws    workspace (conventions)
+ * H % 128 == 0, I % 128 == 0.  One cooperative grid (two CTAs per SM) runs
+ * gate/up with SwiGLU, hands h over through a grid-wide counter (a bounded
+ * wait: FL_ERR_TIMEOUT in the status block if it runs out) and runs the
+ * down projection, so the weight stream does not stop between the two.
+ * Reduction order is fixed: results are deterministic.  FL_ERR_UNSUPPORTED
+ * for M > 8 or when two CTAs per SM do not fit. */
+int fl_int4g_mlp(const void* x, int M, int H, int I, const void* w_gate, const void* w_up,
+                 const void* w_down, void* y, void* ws, size_t ws_bytes, fl_stream_t stream);
+
 /* Test hook of the device-side failure path (no counterpart on the pages:
  * the library never traps or faults; a wait that runs out is reported).
  * ns >= 0: every later decode launch of fl_int4g_linear /
@@ -219,7 +245,9 @@ int fl_moe_int4g_workspace(int M, int E, int k, int H, int I, int has_shared, si
  *   y       bf16 [M, H] device
  *   topk_ids int32 [M, k], topk_w fp32 [M, k], expert_offsets int32 [E+1],
  *   perm int32 [M*k] -- optional device outputs (NULL = not written).
- * H % 128 == 0, I % 128 == 0, 1 <= k <= E <= 1024. */
+ * H % 128 == 0, I % 128 == 0, 1 <= k <= min(E, 32), E <= 1024, and
+ * M * k <= 16384 (the permutation is one CTA's counting sort): larger
+ * batches are split by the caller.  FL_ERR_ARG otherwise. */
 int fl_moe_int4g(const void* x, const float* logits, int M, int H, int E, int k, int I,
                  int scoring, int renorm,
                  const void* w13, const void* w2,
@@ -259,6 +287,41 @@ int fl_moe_int4g_ex(const void* x, const float* logits, int M, int H, int E, int
                     void* y, int32_t* topk_ids, float* topk_w,
                     int32_t* expert_offsets, int32_t* perm,
                     void* ws, size_t ws_bytes, fl_stream_t stream);
+
+/* ------------------------------------------- f2: router projection */
+
+/* Workspace bytes needed by fl_moe_router_logits. */
+int fl_moe_router_logits_workspace(int M, int H, int E, size_t* out);
+
+/* Router logits of the routed MoE layer, logits = x . Wr^T, fp32
+ * accumulation (the input of the top-k choice of fl_moe_int4g; the fastllm
+ * README, section "5. 其它参数", sets only top-k; the dense projection is the
+ * plain reading).
+ *   x       bf16 [M, H] device, row-major     w_router bf16 [E, H] device, row-major
+ *   logits  fp32 [M, E] device, row-major     ws       workspace (conventions)
+ * H % 64 == 0, 1 <= E <= 65536.  Tensor cores (bf16 in, fp32 accumulate);
+ * few output tiles split K over several CTAs, whose partials are summed in a
+ * fixed order: deterministic. */
+int fl_moe_router_logits(const void* x, int M, int H, const void* w_router, int E, float* logits,
+                         void* ws, size_t ws_bytes, fl_stream_t stream);
+
+/* fl_moe_int4g_ex with each expert's matrices at its own address: w13 and
+ * w2 are DEVICE arrays of E device pointers (w13[e]: interleaved [2I, H] of
+ * expert e, w2[e]: interleaved [H, I]), each 16-byte aligned, for callers
+ * whose experts were loaded into separate allocations.  The tables are read
+ * on the device, so a call can be captured in a CUDA graph and the caller
+ * may update the tables between calls (stream order).  A null or misaligned
+ * entry is detected on the device: FL_ERR_DEVICE_CHECK in the status block,
+ * that expert's weight copies are skipped and the outputs of its tokens are
+ * undefined.  The tables themselves must be 8-byte aligned (FL_ERR_ARG).
+ * Everything else as fl_moe_int4g_ex. */
+int fl_moe_int4g_ptrs(const void* x, const float* logits, int M, int H, int E, int k, int I,
+                      const fl_moe_routing* routing,
+                      const void* const* w13, const void* const* w2,
+                      const void* shared_w13, const void* shared_w2,
+                      void* y, int32_t* topk_ids, float* topk_w,
+                      int32_t* expert_offsets, int32_t* perm,
+                      void* ws, size_t ws_bytes, fl_stream_t stream);
 
 #ifdef __cplusplus
 }

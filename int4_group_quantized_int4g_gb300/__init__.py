@@ -19,7 +19,9 @@ __all__ = [
     "fl_int4g_quantize", "fl_int4g_repacked_bytes", "fl_int4g_repack", "fl_int4g_unrepack",
     "fl_int4g_linear_workspace", "fl_int4g_linear", "fl_int4g_linear_noalloc", "fl_int4g_linear_noalloc_status",
     "fl_int4g_test_withhold_cluster_arrival",
-    "fl_moe_int4g_workspace", "fl_moe_int4g", "FlMoeRouting",
+    "fl_moe_int4g_workspace", "fl_moe_int4g", "fl_moe_int4g_ptrs", "FlMoeRouting", "fl_int4g_mlp_workspace",
+    "fl_moe_router_logits_workspace", "fl_moe_router_logits",
+    "fl_int4g_mlp",
 ]
 
 GROUP = 128
@@ -52,10 +54,16 @@ SIGNATURES = {
     "fl_int4g_linear_noalloc_status": (_i, [_vp, ctypes.POINTER(_i)]),
     "fl_int4g_test_withhold_cluster_arrival": (_i, [ctypes.c_longlong]),
     "fl_moe_int4g_workspace": (_i, [_i, _i, _i, _i, _i, _i, _c_size_p]),
+    "fl_int4g_mlp_workspace": (_i, [_i, _i, _i, _c_size_p]),
+    "fl_moe_router_logits_workspace": (_i, [_i, _i, _i, _c_size_p]),
+    "fl_moe_router_logits": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
+    "fl_int4g_mlp": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "fl_moe_int4g": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
                           _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "fl_moe_int4g_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(FlMoeRouting), _vp, _vp, _vp, _vp,
                              _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "fl_moe_int4g_ptrs": (_i, [_vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(FlMoeRouting), _vp, _vp, _vp, _vp,
+                               _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
 }
 
 _LIB = None
@@ -229,6 +237,27 @@ def fl_int4g_test_withhold_cluster_arrival(ns):
     lib().fl_int4g_test_withhold_cluster_arrival(int(ns))
 
 
+def fl_int4g_mlp_workspace(M, H, I):
+    out = ctypes.c_size_t(0)
+    _check("fl_int4g_mlp_workspace", lib().fl_int4g_mlp_workspace(M, H, I, ctypes.byref(out)))
+    return out.value
+
+
+def fl_int4g_mlp(x, w_gate, w_up, w_down, I, y=None, ws=None):
+    """Fused decode MLP block (M <= 8): y = D . (silu(G x) * (U x)), the
+    three matrices in the interleaved layout (G, U: [I, H]; D: [H, I])."""
+    torch = _torch()
+    M, H = x.shape
+    if y is None:
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    nb = fl_int4g_mlp_workspace(M, H, I)
+    if ws is None:
+        ws = _workspace(nb, x.device)
+    _check("fl_int4g_mlp", lib().fl_int4g_mlp(_p(x), M, H, I, _p(w_gate), _p(w_up), _p(w_down), _p(y), _p(ws),
+                                              ws.numel(), _stream()))
+    return y
+
+
 def fl_moe_int4g_workspace(M, E, k, H, I, has_shared):
     out = ctypes.c_size_t(0)
     _check("fl_moe_int4g_workspace",
@@ -267,3 +296,51 @@ def fl_moe_int4g(x, logits, k, I, w13, w2, scoring=FL_SOFTMAX, renorm=True, shar
                                  _p(topk_ids), _p(topk_w), _p(expert_offsets), _p(perm),
                                  _p(ws), ws.numel(), _stream()))
     return y
+
+
+def fl_moe_int4g_ptrs(x, logits, k, I, w13_list, w2_list, scoring=FL_SOFTMAX, renorm=True, shared_w13=None,
+                      shared_w2=None, y=None, topk_ids=None, topk_w=None, expert_offsets=None, perm=None, ws=None,
+                      score_bias=None, n_group=1, topk_group=1, routed_scale=1.0, tables=None):
+    """Routed MoE layer with each expert's matrices in its own CUDA tensor
+    (w13_list[e]: interleaved [2I, H], w2_list[e]: interleaved [H, I]).  The
+    device tables of expert pointers are built here (int64 CUDA tensors) or
+    taken from `tables` = (w13_table, w2_table) when given."""
+    torch = _torch()
+    M, H = x.shape
+    E = logits.shape[1]
+    if y is None:
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    if tables is None:
+        tables = (torch.tensor([t.data_ptr() for t in w13_list], dtype=torch.int64, device=x.device),
+                  torch.tensor([t.data_ptr() for t in w2_list], dtype=torch.int64, device=x.device))
+    nb = fl_moe_int4g_workspace(M, E, k, H, I, shared_w13 is not None)
+    if ws is None:
+        ws = _workspace(nb, x.device)
+    r = FlMoeRouting(scoring, int(bool(renorm)), _p(score_bias), int(n_group), int(topk_group), float(routed_scale))
+    _check("fl_moe_int4g_ptrs",
+           lib().fl_moe_int4g_ptrs(_p(x), _p(logits), M, H, E, k, I, ctypes.byref(r),
+                                   _p(tables[0]), _p(tables[1]), _p(shared_w13), _p(shared_w2), _p(y),
+                                   _p(topk_ids), _p(topk_w), _p(expert_offsets), _p(perm),
+                                   _p(ws), ws.numel(), _stream()))
+    return y
+
+
+def fl_moe_router_logits_workspace(M, H, E):
+    out = ctypes.c_size_t(0)
+    _check("fl_moe_router_logits_workspace", lib().fl_moe_router_logits_workspace(M, H, E, ctypes.byref(out)))
+    return out.value
+
+
+def fl_moe_router_logits(x, w_router, logits=None, ws=None):
+    """fp32 [M, E] router logits = x[M, H] . w_router[E, H]^T (bf16 inputs)."""
+    torch = _torch()
+    M, H = x.shape
+    E = w_router.shape[0]
+    if logits is None:
+        logits = torch.empty((M, E), dtype=torch.float32, device=x.device)
+    nb = fl_moe_router_logits_workspace(M, H, E)
+    if ws is None:
+        ws = _workspace(nb, x.device)
+    _check("fl_moe_router_logits", lib().fl_moe_router_logits(_p(x), M, H, _p(w_router), E, _p(logits), _p(ws),
+                                                               ws.numel(), _stream()))
+    return logits

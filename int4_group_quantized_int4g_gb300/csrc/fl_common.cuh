@@ -17,6 +17,7 @@ constexpr int kSbNib = 8192;    // 128 rows x 64 B of codes
 constexpr int kSbScale = 256;   // 128 fp16 scales
 constexpr int kSbZero = 64;     // 128 4-bit zero points
 constexpr int kSbBytes = kSbNib + kSbScale + kSbZero;  // 8512
+constexpr int kSbSide = kSbScale + kSbZero;             // 320: groups of 64, the odd group's scales and zeros
 constexpr int kStatusBytes = 16;
 // Workspace layout shared by every split kernel of the linear: the status
 // block, then ticket counters for up to kTicketTiles tiles x 8 warps at a fixed
@@ -37,6 +38,21 @@ __device__ __forceinline__ void set_status(int32_t* st, int code, int detail) {
   atomicCAS(st, 0, code);
   atomicOr(st + 1, 1 << code);
   st[2] = detail;
+}
+
+// Base of expert e's interleaved matrix: entry e of a device table of
+// expert pointers when one is given, else w + e * wbytes (experts back to
+// back).  A null or misaligned table entry is recorded in the status block
+// (FL_ERR_DEVICE_CHECK) and returned as null: the caller skips its copy.
+__device__ __forceinline__ const uint8_t* expert_base(const uint8_t* w, const uint8_t* const* wtab, size_t wbytes,
+                                                      int e, int32_t* status) {
+  if (!wtab) return w + static_cast<size_t>(e) * wbytes;
+  const uint8_t* b = wtab[e];
+  if (b == nullptr || (reinterpret_cast<uintptr_t>(b) & 15u) != 0) {
+    set_status(status, FL_ERR_DEVICE_CHECK, 30);
+    return nullptr;
+  }
+  return b;
 }
 
 // ----------------------------------------------------------------- smem/ptx

@@ -1098,7 +1098,8 @@ int launch_tcdec(const void* x, int M, int K, const void* w, int N, void* y, voi
 // warps.  Output: fp32 rows of the segment's positions, times wpos[pos] when
 // given (the down projection), else as they are (gate/up).
 struct MgParams {
-  const uint8_t* w;          // routed experts back to back
+  const uint8_t* w;          // routed experts back to back (when wtab is null)
+  const uint8_t* const* wtab;  // device table of E expert pointers, or null
   const uint8_t* w_shared;   // shared expert (expert index E) or null
   size_t wbytes;             // bytes of one expert's interleaved matrix
   const int32_t* seg_e;
@@ -1210,13 +1211,19 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
       bool ok = true;
       for (int t = t0; t < t1 && ok; ++t) {
         const int sg = t / p.TT, nt = t - sg * p.TT, e = p.seg_e[sg];
-        const uint8_t* base = e == p.E ? p.w_shared : p.w + static_cast<size_t>(e) * p.wbytes;
+        // a bad table entry (recorded) skips the copies: the stages complete
+        // without data and the tile's result is garbage
+        const uint8_t* base = e == p.E ? p.w_shared : expert_base(p.w, p.wtab, p.wbytes, e, p.status);
         for (int g = 0; g < p.G; ++g, ++i) {
           const int sI = i % NSS;
           if (i >= NSS && !mbar_wait(&sempty[sI], static_cast<uint32_t>(i / NSS - 1) & 1u)) {
             set_status(p.status, FL_ERR_TIMEOUT, 42);
             ok = false;
             break;
+          }
+          if (!base) {
+            mbar_arrive(&sfull[sI]);
+            continue;
           }
           mbar_arrive_expect_tx(&sfull[sI], kSbBytes);
           bulk_g2s_hint(smem + C::kSOff + sI * kSbBytes, base + (static_cast<size_t>(nt) * p.G + g) * kSbBytes,
@@ -1380,9 +1387,9 @@ int fl_linear_tcdec(const void* x, int M, int K, const void* w, int N, void* y, 
 // Grouped expert GEMM of the MoE layer (see k_moe_gemm).  x: [npos, K] bf16
 // rows in position order; out: [npos, ldo] fp32.  nseg, seg_* and wpos are
 // device arrays written by earlier kernels on the same stream.
-int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* w_shared, size_t wbytes, int E, int Nout,
-                const int32_t* seg_e, const int32_t* seg_pos, const int32_t* seg_n, const int32_t* nseg,
-                const float* wpos, float* out, int32_t* status, cudaStream_t s) {
+int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* const* wtab, const void* w_shared,
+                size_t wbytes, int E, int Nout, const int32_t* seg_e, const int32_t* seg_pos, const int32_t* seg_n,
+                const int32_t* nseg, const float* wpos, float* out, int32_t* status, cudaStream_t s) {
   auto enc = encode_fn();
   if (!enc) return FL_ERR_CUDA;
   CUtensorMap map;
@@ -1404,6 +1411,7 @@ int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* w_sha
   }
   MgParams p;
   p.w = static_cast<const uint8_t*>(w);
+  p.wtab = reinterpret_cast<const uint8_t* const*>(wtab);
   p.w_shared = static_cast<const uint8_t*>(w_shared);
   p.wbytes = wbytes;
   p.seg_e = seg_e;

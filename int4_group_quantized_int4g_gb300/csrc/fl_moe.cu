@@ -364,7 +364,8 @@ __global__ void __launch_bounds__(1024, 1) k_moe_permute(const PermuteArgs a) {
 // MODE 1: down.  A unit is (segment, tile, group) of W2; x rows = h rows of
 //         the segment's positions.  Output out = w_pos * sum, fp32.
 struct MoeRowsParams {
-  const uint8_t* w;            // routed experts back to back
+  const uint8_t* w;            // routed experts back to back (when wtab is null)
+  const uint8_t* const* wtab;  // device table of E expert pointers, or null
   const uint8_t* w_shared;     // shared expert (or null)
   size_t wbytes;               // bytes of one expert's matrix
   const __nv_bfloat16* x;      // MODE 0: x [M, K]; MODE 1: h [pos, K]
@@ -543,14 +544,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p)
       }
       const int seg = u / TG, rem = u - seg * TG, tile = rem / p.G, g = rem - tile * p.G;
       const int e = p.seg_e[seg], pos0 = p.seg_pos[seg], nt_ok = p.seg_n[seg];
-      const uint8_t* base = e == p.E ? p.w_shared : p.w + static_cast<size_t>(e) * p.wbytes;
       uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(SB * kSbBytes + nt_ok * 256));
-        bulk_g2s_hint(st, base + (static_cast<size_t>(tile) * p.G + g) * kSbBytes, kSbBytes, &full[s], pol);
-        if (SB == 2)
-          bulk_g2s_hint(st + kSbBytes, base + (static_cast<size_t>(tile + p.up_off) * p.G + g) * kSbBytes, kSbBytes,
-                        &full[s], pol);
+        // a bad table entry (recorded) skips the weight copy: the stage then
+        // completes on its activations alone and its result is garbage
+        const uint8_t* base = e == p.E ? p.w_shared : expert_base(p.w, p.wtab, p.wbytes, e, p.status);
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>((base ? SB * kSbBytes : 0) + nt_ok * 256));
+        if (base) {
+          bulk_g2s_hint(st, base + (static_cast<size_t>(tile) * p.G + g) * kSbBytes, kSbBytes, &full[s], pol);
+          if (SB == 2)
+            bulk_g2s_hint(st + kSbBytes, base + (static_cast<size_t>(tile + p.up_off) * p.G + g) * kSbBytes,
+                          kSbBytes, &full[s], pol);
+        }
       }
       __syncwarp();
       if (lane < nt_ok) {
@@ -680,7 +685,9 @@ bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeL
   L->nseg_max = std::min(E, n) + (n + kSegRows - 1) / kSegRows + (has_shared ? (M + kSegRows - 1) / kSegRows : 0);
   L->P = sms;
   const int TT13 = I / kRowTile, TT2 = H / kRowTile;
-  size_t o = kStatusBytes;
+  // everything after the counter region that the linear kernels keep zero
+  // between calls: one workspace can serve calls of every entry point
+  size_t o = kScratchOff;
   L->plan = o; o = al(o + sizeof(MoePlan));
   L->ids = o; o = al(o + 4ull * n);
   L->wts = o; o = al(o + 4ull * n);
@@ -729,9 +736,9 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 }  // namespace
 
-int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* w_shared, size_t wbytes, int E, int Nout,
-                const int32_t* seg_e, const int32_t* seg_pos, const int32_t* seg_n, const int32_t* nseg,
-                const float* wpos, float* out, int32_t* status, cudaStream_t s);
+int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* const* wtab, const void* w_shared,
+                size_t wbytes, int E, int Nout, const int32_t* seg_e, const int32_t* seg_pos, const int32_t* seg_n,
+                const int32_t* nseg, const float* wpos, float* out, int32_t* status, cudaStream_t s);
 
 extern "C" int fl_moe_int4g_workspace(int M, int E, int k, int H, int I, int has_shared, size_t* out) {
   if (!out) return FL_ERR_ARG;
@@ -741,12 +748,14 @@ extern "C" int fl_moe_int4g_workspace(int M, int E, int k, int H, int I, int has
   return FL_OK;
 }
 
-extern "C" int fl_moe_int4g_ex(const void* x, const float* logits, int M, int H, int E, int k, int I,
-                               const fl_moe_routing* routing, const void* w13, const void* w2,
-                               const void* shared_w13, const void* shared_w2, void* y, int32_t* topk_ids,
-                               float* topk_w, int32_t* expert_offsets, int32_t* perm, void* ws, size_t ws_bytes,
-                               fl_stream_t stream) {
-  if (!x || !logits || !w13 || !w2 || !y || !ws || !routing) return FL_ERR_ARG;
+// The routed layer; the experts are either back to back (w13, w2) or given
+// by device tables of E pointers (w13tab, w2tab).
+static int moe_layer(const void* x, const float* logits, int M, int H, int E, int k, int I,
+                     const fl_moe_routing* routing, const void* w13, const void* w2, const void* const* w13tab,
+                     const void* const* w2tab, const void* shared_w13, const void* shared_w2, void* y,
+                     int32_t* topk_ids, float* topk_w, int32_t* expert_offsets, int32_t* perm, void* ws,
+                     size_t ws_bytes, fl_stream_t stream) {
+  if (!x || !logits || !y || !ws || !routing) return FL_ERR_ARG;
   if ((shared_w13 == nullptr) != (shared_w2 == nullptr)) return FL_ERR_ARG;
   const int scoring = routing->scoring, renorm = routing->renorm;
   if (scoring != FL_SOFTMAX && scoring != FL_SIGMOID) return FL_ERR_ARG;
@@ -761,6 +770,7 @@ extern "C" int fl_moe_int4g_ex(const void* x, const float* logits, int M, int H,
     if (routing->score_bias && !flh::aligned16(routing->score_bias)) return FL_ERR_ARG;
   }
   if (!flh::aligned16(x) || !flh::aligned16(w13) || !flh::aligned16(w2) || !flh::aligned16(y) ||
+      (reinterpret_cast<uintptr_t>(w13tab) & 7u) || (reinterpret_cast<uintptr_t>(w2tab) & 7u) ||
       !flh::aligned16(ws) || (shared_w13 && (!flh::aligned16(shared_w13) || !flh::aligned16(shared_w2))))
     return FL_ERR_ARG;
   const int has_shared = shared_w13 != nullptr;
@@ -843,12 +853,13 @@ extern "C" int fl_moe_int4g_ex(const void* x, const float* logits, int M, int H,
     if (launch_pdl(k_moe_gather, dim3(4 * sms), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(x),
                    reinterpret_cast<const int32_t*>(W + L.tok), npos, H, xp) != cudaSuccess)
       return FL_ERR_CUDA;
-    int rc = fl_moe_gemm(xp, npos, H, w13, shared_w13, b13, E, 2 * I, sege, segp, segn, nseg, nullptr, gu, status, s);
+    int rc = fl_moe_gemm(xp, npos, H, w13, w13tab, shared_w13, b13, E, 2 * I, sege, segp, segn, nseg, nullptr, gu,
+                         status, s);
     if (rc != FL_OK) return rc;
     if (launch_pdl(k_moe_swiglu, dim3(4 * sms), dim3(256), 0, s, static_cast<const float*>(gu), npos, I, h) !=
         cudaSuccess)
       return FL_ERR_CUDA;
-    rc = fl_moe_gemm(h, npos, I, w2, shared_w2, b2, E, H, sege, segp, segn, nseg,
+    rc = fl_moe_gemm(h, npos, I, w2, w2tab, shared_w2, b2, E, H, sege, segp, segn, nseg,
                      reinterpret_cast<const float*>(W + L.wpos), reinterpret_cast<float*>(W + L.out), status, s);
     if (rc != FL_OK) return rc;
   }
@@ -856,6 +867,7 @@ extern "C" int fl_moe_int4g_ex(const void* x, const float* logits, int M, int H,
   for (int mode = 0; mode < 2 && !L.gemm; ++mode) {
     MoeRowsParams p;
     p.w = static_cast<const uint8_t*>(mode == 0 ? w13 : w2);
+    p.wtab = reinterpret_cast<const uint8_t* const*>(mode == 0 ? w13tab : w2tab);
     p.w_shared = static_cast<const uint8_t*>(mode == 0 ? shared_w13 : shared_w2);
     p.wbytes = mode == 0 ? b13 : b2;
     p.x = mode == 0 ? static_cast<const __nv_bfloat16*>(x) : reinterpret_cast<const __nv_bfloat16*>(W + L.h);
@@ -897,6 +909,26 @@ extern "C" int fl_moe_int4g_ex(const void* x, const float* logits, int M, int H,
                  has_shared, static_cast<__nv_bfloat16*>(y)) != cudaSuccess)
     return FL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
+}
+
+extern "C" int fl_moe_int4g_ex(const void* x, const float* logits, int M, int H, int E, int k, int I,
+                               const fl_moe_routing* routing, const void* w13, const void* w2,
+                               const void* shared_w13, const void* shared_w2, void* y, int32_t* topk_ids,
+                               float* topk_w, int32_t* expert_offsets, int32_t* perm, void* ws, size_t ws_bytes,
+                               fl_stream_t stream) {
+  if (!w13 || !w2) return FL_ERR_ARG;
+  return moe_layer(x, logits, M, H, E, k, I, routing, w13, w2, nullptr, nullptr, shared_w13, shared_w2, y, topk_ids,
+                   topk_w, expert_offsets, perm, ws, ws_bytes, stream);
+}
+
+extern "C" int fl_moe_int4g_ptrs(const void* x, const float* logits, int M, int H, int E, int k, int I,
+                                 const fl_moe_routing* routing, const void* const* w13, const void* const* w2,
+                                 const void* shared_w13, const void* shared_w2, void* y, int32_t* topk_ids,
+                                 float* topk_w, int32_t* expert_offsets, int32_t* perm, void* ws, size_t ws_bytes,
+                                 fl_stream_t stream) {
+  if (!w13 || !w2) return FL_ERR_ARG;
+  return moe_layer(x, logits, M, H, E, k, I, routing, nullptr, nullptr, w13, w2, shared_w13, shared_w2, y, topk_ids,
+                   topk_w, expert_offsets, perm, ws, ws_bytes, stream);
 }
 
 extern "C" int fl_moe_int4g(const void* x, const float* logits, int M, int H, int E, int k, int I, int scoring,

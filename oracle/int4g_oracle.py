@@ -28,7 +28,13 @@ What it computes, and where it comes from:
   Its super-blocks always span 128 columns.  Groups of 256 (same page,
   section 4.2 "模型转换与格式说明": --group-size defaults to 128 and may be
   raised to 256) are stored as two consecutive super-blocks that carry the
-  same scale and zero point; the dequantized weights are unchanged.
+  same scale and zero point; the dequantized weights are unchanged.  Groups
+  of 64 (section 5.4 "精度与速度平衡": a group size of 64 for more precision)
+  keep the super-blocks, which then carry the scale and zero point of the
+  first 64 columns, and append a side array with those of the second 64
+  columns of every super-block.
+* the router projection logits = x . Wr^T in front of the top-k choice (not
+  detailed on the pages; the plain dense projection);
 * the routed MoE expert FFN with int4g experts -- fastllm README (gittoolsai
   mirror), "2. 如何设定推理精度" (--moe_dtype int4g) and "5. 其它参数"
   (--moe_experts = top-k, --cuda_se = shared expert): top-k routing,
@@ -47,7 +53,9 @@ from __future__ import annotations
 import numpy as np
 
 GROUP = 128          # weights per group along K (FastLLM page, section 3.1)
-GROUPS = (128, 256)  # group sizes of the layout (section 4.2: 128 by default, 256 allowed)
+GROUPS = (64, 128, 256)  # group sizes of the layout (section 4.2: 128 by default, 256 allowed;
+                         # section 5.4: 64 for more precision)
+SB_SIDE = 320        # groups of 64: per super-block, the second group's 128 scales + 128 zeros
 QMAX = 15            # 4-bit codes 0..15
 ROW_TILE = 128       # rows per super-block of the interleaved layout
 SB_NIB = 8192        # nibble bytes per super-block: 128 rows x 64 B
@@ -264,13 +272,19 @@ def linear_columns(x, Q, S, Z, cols, group=GROUP):
 # a2: tile-interleaved layout ("int4g-tiled")
 # --------------------------------------------------------------------------
 
+def _check_layout(K, group):
+    if group not in GROUPS or K % group or K % GROUP:
+        raise ValueError("the interleaved layout takes groups of 64, 128 or 256, K % group == 0 and K % 128 == 0")
+
+
 def tiled_bytes(N, K, group=GROUP):
     """Bytes of the interleaved layout: one 8512-byte super-block per 128
-    rows x 128 columns, whatever the group size."""
-    if group not in GROUPS or K % group:
-        raise ValueError("the interleaved layout takes groups of 128 or 256 and K % group == 0")
+    rows x 128 columns, plus (groups of 64) a 320-byte side entry per
+    super-block."""
+    _check_layout(K, group)
     Np = -(-N // ROW_TILE) * ROW_TILE
-    return (Np // ROW_TILE) * (K // GROUP) * SB_BYTES
+    nsb = (Np // ROW_TILE) * (K // GROUP)
+    return nsb * (SB_BYTES + (SB_SIDE if group == 64 else 0))
 
 
 def expand_groups(S, Z, group):
@@ -316,8 +330,9 @@ def repack(Q, S, Z, N, K, group=GROUP):
     group 256: the super-blocks still span 128 columns; both super-blocks of
     a group carry that group's scale and zero point (expand_groups).
     """
-    if group not in GROUPS or K % group:
-        raise ValueError("the interleaved layout takes groups of 128 or 256 and K % group == 0")
+    _check_layout(K, group)
+    if group == 64:
+        return _repack_g64(Q, S, Z, N, K)
     if group != GROUP:
         S, Z = expand_groups(S, Z, group)
         group = GROUP
@@ -354,8 +369,9 @@ def unrepack(buf, N, K, group=GROUP):
     """Inverse of repack(): interleaved bytes -> canonical (Q, S, Z).
     group 256: the scale and zero point of each group are read from its
     first super-block."""
-    if group not in GROUPS or K % group:
-        raise ValueError("the interleaved layout takes groups of 128 or 256 and K % group == 0")
+    _check_layout(K, group)
+    if group == 64:
+        return _unrepack_g64(buf, N, K)
     if group != GROUP:
         Q, S, Z = unrepack(buf, N, K, GROUP)
         r = group // GROUP
@@ -378,6 +394,74 @@ def unrepack(buf, N, K, group=GROUP):
             zb = buf[base + SB_NIB + SB_SCALE:base + SB_BYTES]
             z[T * ROW_TILE:(T + 1) * ROW_TILE, g] = (zb[rows // 2] >> (4 * (rows % 2))) & 0xF
     return pack_codes(q[:N]), s[:N].copy(), pack_zeros(z[:N])
+
+
+def _repack_g64(Q, S, Z, N, K):
+    """Groups of 64: the super-blocks of the 128-column layout carry the
+    scale and zero point of the even group (columns 0..63 of the 128); the
+    side array that follows them, one 320-byte entry per super-block in the
+    same order, carries those of the odd group (columns 64..127): 128 fp16
+    scales (row r at 2r, little endian), then 128 zero points (row r in byte
+    256 + r//2, low nibble = even r)."""
+    G64 = K // 64
+    z = unpack_zeros(Z, G64)
+    main = repack(Q, S[:, 0::2].copy(), pack_zeros(z[:, 0::2]), N, K, GROUP)
+    Np = -(-N // ROW_TILE) * ROW_TILE
+    nsb = (Np // ROW_TILE) * (K // GROUP)
+    side = np.zeros(nsb * SB_SIDE, np.uint8)
+    s_odd = np.zeros((Np, K // GROUP), np.uint16)
+    s_odd[:N] = S[:, 1::2]
+    z_odd = np.zeros((Np, K // GROUP), np.uint8)
+    z_odd[:N] = z[:, 1::2]
+    rows = np.arange(ROW_TILE)
+    for u in range(nsb):
+        T, g = divmod(u, K // GROUP)
+        e = side[u * SB_SIDE:(u + 1) * SB_SIDE]
+        e[:256] = s_odd[T * ROW_TILE:(T + 1) * ROW_TILE, g].astype('<u2').view(np.uint8)
+        zz = z_odd[T * ROW_TILE:(T + 1) * ROW_TILE, g]
+        for r in rows:
+            e[256 + r // 2] |= (zz[r] << (4 * (r % 2))).astype(np.uint8)
+    return np.concatenate([main, side])
+
+
+def _unrepack_g64(buf, N, K):
+    """Inverse of _repack_g64."""
+    Np = -(-N // ROW_TILE) * ROW_TILE
+    nsb = (Np // ROW_TILE) * (K // GROUP)
+    buf = np.asarray(buf, np.uint8)
+    Q, S_even, Z_even = unrepack(buf[:nsb * SB_BYTES], N, K, GROUP)
+    S = np.zeros((N, K // 64), np.uint16)
+    z = np.zeros((N, K // 64), np.uint8)
+    S[:, 0::2] = S_even
+    z[:, 0::2] = unpack_zeros(Z_even, K // GROUP)
+    side = buf[nsb * SB_BYTES:]
+    rows = np.arange(ROW_TILE)
+    s_odd = np.zeros((Np, K // GROUP), np.uint16)
+    z_odd = np.zeros((Np, K // GROUP), np.uint8)
+    for u in range(nsb):
+        T, g = divmod(u, K // GROUP)
+        e = side[u * SB_SIDE:(u + 1) * SB_SIDE]
+        s_odd[T * ROW_TILE:(T + 1) * ROW_TILE, g] = e[:256].view('<u2')
+        z_odd[T * ROW_TILE:(T + 1) * ROW_TILE, g] = (e[256 + rows // 2] >> (4 * (rows % 2))) & 0xF
+    S[:, 1::2] = s_odd[:N]
+    z[:, 1::2] = z_odd[:N]
+    return Q, S, pack_zeros(z)
+
+
+# --------------------------------------------------------------------------
+# f2: router projection
+# --------------------------------------------------------------------------
+
+def router_logits(x, w_router):
+    """Router logits of the routed MoE layer, logits[m, e] = sum_h x[m, h] *
+    Wr[e, h], in double (x float64 [M, H], Wr float64 [E, H]).  The pages
+    give no detail of the router (the fastllm README only sets top-k, section
+    "5. 其它参数"); the plain dense projection is the reading taken.  Returns
+    (logits, tol) with the linear bound tol = 2e-3 * sum_h |x||Wr| + 1e-5 of
+    an fp32-accumulated result."""
+    x = np.asarray(x, np.float64)
+    w = np.asarray(w_router, np.float64)
+    return x @ w.T, 2e-3 * (np.abs(x) @ np.abs(w).T) + 1e-5
 
 
 # --------------------------------------------------------------------------

@@ -45,7 +45,10 @@ def test_repacked_bytes(L):
     assert fl.fl_int4g_repacked_bytes(200, 384) == 2 * 3 * 8512     # padded to 2 row tiles
     out = ctypes.c_size_t(0)
     assert L.fl_int4g_repacked_bytes(128, 100, 128, ctypes.byref(out)) == 1      # K % 128
-    assert L.fl_int4g_repacked_bytes(128, 256, 64, ctypes.byref(out)) == 3       # group 64
+    assert L.fl_int4g_repacked_bytes(128, 256, 32, ctypes.byref(out)) == 3       # group 32
+    # groups of 64: the super-blocks plus a 320-byte side entry each
+    assert fl.fl_int4g_repacked_bytes(200, 384, 64) == 2 * 3 * (8512 + 320)
+    assert L.fl_int4g_repacked_bytes(128, 192, 64, ctypes.byref(out)) == 1       # K % 128
     assert L.fl_int4g_repacked_bytes(0, 256, 128, ctypes.byref(out)) == 1
     # groups of 256: the same 128-column super-blocks (two per group)
     assert fl.fl_int4g_repacked_bytes(4096, 11008, 256) == 32 * 86 * 8512
@@ -68,7 +71,7 @@ def test_argument_errors_are_caught_on_the_host(L):
     # workspace too small
     assert L.fl_int4g_linear(fake, 1, 256, fake, 128, fake, fake, 16, None) == 2
     assert L.fl_int4g_repack(fake, fake, fake, 128, 256, 128, fake, 100, None) == 1
-    assert L.fl_int4g_repack(fake, fake, fake, 128, 256, 64, fake, 1 << 20, None) == 3
+    assert L.fl_int4g_repack(fake, fake, fake, 128, 256, 32, fake, 1 << 20, None) == 3
     assert L.fl_int4g_repack(fake, fake, fake, 128, 384, 256, fake, 1 << 20, None) == 1
     assert L.fl_int4g_unrepack(fake, 1 << 20, 128, 384, 256, fake, fake, fake, None) == 1
     assert L.fl_int4g_quantize(fake, 128, 384, 256, fake, fake, fake, fake, None) == 1

@@ -128,6 +128,34 @@ def test_repack_group256_bit_exact_and_invertible(shape):
     assert np.array_equal(back[0], Q) and np.array_equal(back[1], S) and np.array_equal(back[2], Z)
 
 
+# Groups of 64 (FastLLM page, section 5.4): the super-blocks carry the even
+# group's scale and zero point, a side array after them the odd group's.
+
+@pytest.mark.parametrize("shape", [(200, 384), (3, 1024), (129, 1280)])
+def test_quantizer_group64_bit_exact(shape):
+    N, K = shape
+    W = inputs.dense_weight(N, K, layer=70 + N)
+    W[0, :64] = 0.0              # zero group
+    W[1 % N, 64:128] = 0.5       # constant positive group
+    W[2 % N, 128:192] = np.abs(W[2 % N, 128:192]) + 0.25   # all positive: clamped zero point
+    Q, S, Z = O.quantize(W, 64)
+    got = canon_host(*fl.fl_int4g_quantize(to_dev(W), group=64))
+    assert np.array_equal(got[0], Q)
+    assert np.array_equal(got[1], S)
+    assert np.array_equal(got[2], Z)
+
+
+@pytest.mark.parametrize("shape", [(200, 384), (128, 128), (300, 1280)])
+def test_repack_group64_bit_exact_and_invertible(shape):
+    N, K = shape
+    W = inputs.dense_weight(N, K, layer=60 + N)
+    Q, S, Z = O.quantize(W, 64)
+    w = fl.fl_int4g_repack(to_dev(Q), to_dev(S.view(np.int16)), to_dev(Z), N, K, group=64)
+    assert np.array_equal(w.cpu().numpy(), O.repack(Q, S, Z, N, K, 64))
+    back = canon_host(*fl.fl_int4g_unrepack(w, N, K, group=64))
+    assert np.array_equal(back[0], Q) and np.array_equal(back[1], S) and np.array_equal(back[2], Z)
+
+
 @pytest.mark.parametrize("M", [1, 8, 9, 32, 64, 300])
 def test_linear_group256_parity(M):
     """Decode (rows and tcgen05 kernels) and prefill on group-256 weights,
@@ -324,3 +352,30 @@ def test_prefill_full_size_sampled(KN):
         got = y.float().cpu().numpy().astype(np.float64)[:, cols]
         assert np.all(np.abs(got - ref) <= tol), (M, np.max(np.abs(got - ref) / tol))
         assert np.sqrt(np.mean((got - ref) ** 2) / np.mean(ref ** 2)) <= 1e-2
+
+
+def test_one_workspace_across_entry_points():
+    """One workspace serves the linear, the MoE layer, the router projection
+    and the MLP block in turn: every entry point keeps its scratch out of the
+    counter region that the others need zero."""
+    M, N, K = 12, 512, 1280
+    _, xb, Q, S, Z, w = _linear_case(M, N, K, layer=85)
+    E, H, I = 8, 256, 128
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=DEV)
+    x = bf16_dev(xb)
+    y0 = fl.fl_int4g_linear(x, w, N, ws=ws).clone()
+    w13 = torch.cat([fl.fl_int4g_repack(*quantize_dev(inputs.expert_weight(2 * I, H, 86, e, 0)), 2 * I, H)
+                     for e in range(E)])
+    w2 = torch.cat([fl.fl_int4g_repack(*quantize_dev(inputs.expert_weight(H, I, 86, e, 1)), H, I) for e in range(E)])
+    xm = bf16_dev(inputs.activations(40, H, stream=86))
+    fl.fl_moe_int4g(xm, to_dev(inputs.router_logits(40, E, stream=86)), 2, I, w13, w2, ws=ws)
+    wr = bf16_dev(inputs.to_bf16_bits(inputs.expert_weight(E, H, 87, 0, 0)))
+    fl.fl_moe_router_logits(xm, wr, ws=ws)
+    g, u, d = (fl.fl_int4g_repack(*quantize_dev(inputs.dense_weight(n, k, layer=88 + i)), n, k)
+               for i, (n, k) in enumerate([(I, H), (I, H), (H, I)]))
+    fl.fl_int4g_mlp(xm[:4].contiguous(), g, u, d, I, ws=ws)
+    for _ in range(2):
+        y = fl.fl_int4g_linear(x, w, N, ws=ws)
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+    assert fl.fl_int4g_status(ws) == 0
+    _check(y0, xb, Q, S, Z)

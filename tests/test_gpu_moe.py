@@ -370,3 +370,106 @@ def test_moe_routed_scale_softmax():
     assert np.array_equal(ids.cpu().numpy(), rid)
     assert np.allclose(wts.cpu().numpy(), rw, rtol=1e-5, atol=0)
     check_y(y, ref, tol)
+
+
+@pytest.mark.parametrize("M", [5, 96])
+def test_moe_expert_pointer_tables(M):
+    """Experts in separate allocations, passed as device tables of pointers
+    (fl_moe_int4g_ptrs): the same bits as the back-to-back call, on the rows
+    kernels (M = 5) and the grouped GEMM (M = 96, 24 positions per expert)."""
+    E, H, I, k = 8, 512, 256, 2
+    w13, w2 = host_experts(E, H, I, layer=95)
+    sw13, sw2 = host_experts(1, H, I, layer=94)
+    w13_each = [repack_dev(*t, 2 * I, H) for t in w13]
+    w2_each = [repack_dev(*t, H, I) for t in w2]
+    xb = inputs.activations(M, H, stream=95)
+    logits = inputs.router_logits(M, E, stream=95)
+    sd13, sd2 = repack_dev(*sw13[0], 2 * I, H), repack_dev(*sw2[0], H, I)
+    y_ref, ids, wts, offs, perm = run_moe(xb, logits, k, I, torch.cat(w13_each), torch.cat(w2_each), fl.FL_SIGMOID,
+                                          True, sd13, sd2)
+    y_ref = y_ref.clone()
+    ws = torch.zeros(fl.fl_moe_int4g_workspace(M, E, k, H, I, True), dtype=torch.uint8, device=DEV)
+    y = fl.fl_moe_int4g_ptrs(bf16_dev(xb), to_dev(logits), k, I, w13_each, w2_each, scoring=fl.FL_SIGMOID,
+                             shared_w13=sd13, shared_w2=sd2, ws=ws)
+    torch.cuda.synchronize()
+    assert fl.fl_int4g_status(ws) == 0
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+    ref, tol, _, _ = O.moe(O.bf16_value(xb), logits, k, w13, w2, O.SIGMOID, True, sw13[0], sw2[0])
+    check_y(y, ref, tol)
+
+
+def test_moe_expert_pointer_table_bad_entry_is_reported():
+    """A misaligned table entry is caught on the device (FL_ERR_DEVICE_CHECK):
+    that expert's copies are skipped (no fault), the call completes."""
+    E, H, I, k, M = 4, 256, 128, 2, 6
+    w13, w2 = host_experts(E, H, I, layer=93)
+    w13_each = [repack_dev(*t, 2 * I, H) for t in w13]
+    w2_each = [repack_dev(*t, H, I) for t in w2]
+    xb = inputs.activations(M, H, stream=93)
+    logits = inputs.router_logits(M, E, stream=93)
+    logits[:, 1] += 10.0   # every token is routed to expert 1
+    t13 = torch.tensor([t.data_ptr() for t in w13_each], dtype=torch.int64, device=DEV)
+    t2 = torch.tensor([t.data_ptr() for t in w2_each], dtype=torch.int64, device=DEV)
+    t13[1] += 8   # misaligned: 8 bytes past expert 1's start (inside its buffer)
+    ws = torch.zeros(fl.fl_moe_int4g_workspace(M, E, k, H, I, False), dtype=torch.uint8, device=DEV)
+    fl.fl_moe_int4g_ptrs(bf16_dev(xb), to_dev(logits), k, I, w13_each, w2_each, ws=ws, tables=(t13, t2))
+    torch.cuda.synchronize()
+    assert fl.fl_int4g_status(ws) == 6
+
+
+# ------------------------------------------------------------------ router projection
+
+def _router_case(M, H, E, layer):
+    rng = np.random.default_rng([0, 7, layer])
+    w = inputs.to_bf16_bits((rng.standard_normal((E, H)) * 0.02).astype(np.float32))
+    xb = inputs.activations(M, H, stream=layer)
+    return xb, w
+
+
+@pytest.mark.parametrize("MHE", [(1, 7168, 256), (16, 7168, 256), (128, 7168, 256), (1024, 7168, 256),
+                                 (1, 2048, 128), (256, 2048, 128), (37, 192, 70), (130, 256, 8)])
+def test_router_logits_parity(MHE):
+    """Router logits against the oracle's double projection, every output,
+    within 2e-3 * sum |x||Wr| + 1e-5; two calls give the same bits (the
+    split-K partials are added in a fixed order)."""
+    M, H, E = MHE
+    xb, wb = _router_case(M, H, E, layer=M + H + E)
+    x = bf16_dev(xb)
+    w = bf16_dev(wb)
+    ws = torch.zeros(fl.fl_moe_router_logits_workspace(M, H, E), dtype=torch.uint8, device=DEV)
+    l1 = fl.fl_moe_router_logits(x, w, ws=ws).clone()
+    l2 = fl.fl_moe_router_logits(x, w, ws=ws).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(l1, l2)
+    ref, tol = O.router_logits(O.bf16_value(xb), O.bf16_value(wb))
+    got = l1.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= tol), np.max(np.abs(got - ref) / tol)
+
+
+def test_router_then_moe_deepseek_routing():
+    """The router projection feeding the layer (DeepSeek-V3-shaped router:
+    H=7168, E=256, top-8 sigmoid): the ids chosen from the device logits
+    equal the oracle's wherever the oracle's k-th and (k+1)-th logits are
+    further apart than the logits' error bound; elsewhere either choice is
+    correct and the chosen experts must be among the near-tied ones."""
+    M, H, E, k = 64, 7168, 256, 8
+    xb, wb = _router_case(M, H, E, layer=77)
+    logits = fl.fl_moe_router_logits(bf16_dev(xb), bf16_dev(wb))
+    torch.cuda.synchronize()
+    ref, tol = O.router_logits(O.bf16_value(xb), O.bf16_value(wb))
+    # routing of the device logits on the device (small experts: only the ids matter here)
+    Ie, He = 128, H
+    ids = torch.empty((M, k), dtype=torch.int32, device=DEV)
+    ex13 = torch.zeros(fl.fl_int4g_repacked_bytes(2 * Ie, He) * E, dtype=torch.uint8, device=DEV)
+    ex2 = torch.zeros(fl.fl_int4g_repacked_bytes(He, Ie) * E, dtype=torch.uint8, device=DEV)
+    fl.fl_moe_int4g(bf16_dev(xb), logits, k, Ie, ex13, ex2, scoring=fl.FL_SIGMOID, topk_ids=ids)
+    torch.cuda.synchronize()
+    got = ids.cpu().numpy()
+    rid, _ = O.route(ref.astype(np.float32), k, O.SIGMOID, True)
+    for t in range(M):
+        order = np.sort(ref[t])[::-1]
+        margin = order[k - 1] - order[k]
+        if margin > 2 * tol[t].max():
+            assert set(got[t].tolist()) == set(rid[t].tolist()), t
+        else:
+            assert np.all(ref[t][got[t]] >= order[k - 1] - 2 * tol[t].max()), t
