@@ -16,10 +16,12 @@
  *  - W is [N, K] in nn.Linear order; y = x . deq(W)^T; x is [M, K] bf16,
  *    row-major, y is [M, N] bf16, row-major.
  *  - group is 128 or 256 (FastLLM page, section 4.2: --group-size 128 by
- *    default, 256 allowed) and K % group == 0.  Only the quantizer, the
- *    repack and the unrepack take it: the matmul entry points read the
- *    interleaved layout, whose super-blocks span 128 columns whatever the
- *    group size.
+ *    default, 256 allowed) or 64 (section 5.4: 64 for more precision),
+ *    K % group == 0 and K % 128 == 0.  The quantizer, the repack and the
+ *    unrepack take it; the matmul entry points read the interleaved layout,
+ *    whose super-blocks span 128 columns whatever the group size, and take
+ *    a group argument only where groups of 64 are supported
+ *    (fl_int4g_linear_g, fl_moe_int4g_g).
  *  - Canonical int4g triple (the storage the quantizer produces), G = K/group:
  *      q      uint8  [N, K/2]        codes 0..15, low nibble = even k
  *      scales uint16 [N, G]          IEEE fp16 bit patterns
@@ -41,7 +43,12 @@
  *      [8448, 8512)  128 zero points, row r in byte 8448 + r/2, low nibble
  *                    for even r.
  *    With groups of 256, super-blocks (T, 2j) and (T, 2j+1) both carry the
- *    scales and zero points of group j.
+ *    scales and zero points of group j.  With groups of 64, super-block
+ *    (T, g) carries those of group 2g (its columns 0..63), and a side array
+ *    after all super-blocks, one 320-byte entry per super-block in the same
+ *    order at offset (#super-blocks * 8512) + (T * G + g) * 320, carries
+ *    those of group 2g+1: 128 fp16 scales (row r at 2r), then 128 zero
+ *    points (row r in byte 256 + r/2, low nibble for even r).
  *    Size: 0.51953125 bytes per weight (the same as the canonical triple),
  *    plus padding rows.  Each super-block is one contiguous bulk copy.
  *  - All device pointers must be 16-byte aligned.
@@ -154,6 +161,17 @@ int fl_int4g_linear_workspace(int M, int N, int K, size_t* out);
  * order is fixed, so results are deterministic. */
 int fl_int4g_linear(const void* x, int M, int K, const void* w, int N,
                     void* y, void* ws, size_t ws_bytes, fl_stream_t stream);
+
+/* fl_int4g_linear for weights in the layout of any group size: group 128
+ * or 256 (the same layout) is fl_int4g_linear; group 64 (FastLLM page,
+ * section 5.4: groups of 64 for more precision) reads the side array of
+ * the layout as well (fl_int4g_repack with group 64), each 64-column group
+ * with its own scale and zero point.  The workspace is the one
+ * fl_int4g_linear_workspace returns.  Group 64 runs the mma.sync decode
+ * kernel for every M <= 32 and the tcgen05 prefill GEMM above.
+ * FL_ERR_UNSUPPORTED for other group sizes. */
+int fl_int4g_linear_g(const void* x, int M, int K, const void* w, int N, int group,
+                      void* y, void* ws, size_t ws_bytes, fl_stream_t stream);
 
 /* Decode linear (M <= 32) that allocates nothing and takes no workspace.
  * Not a step of the method: the pages have no counterpart; it exists for
@@ -304,6 +322,21 @@ int fl_moe_router_logits_workspace(int M, int H, int E, size_t* out);
  * fixed order: deterministic. */
 int fl_moe_router_logits(const void* x, int M, int H, const void* w_router, int E, float* logits,
                          void* ws, size_t ws_bytes, fl_stream_t stream);
+
+/* fl_moe_int4g_ex for experts in the layout of any group size: group 128
+ * or 256 is fl_moe_int4g_ex; group 64 (FastLLM page, section 5.4) reads
+ * each expert matrix's side array as well.  Experts back to back with the
+ * stride fl_int4g_repacked_bytes(rows, cols, group) (for group 64 that
+ * includes the side array); the shared expert likewise.  The workspace is
+ * the one fl_moe_int4g_workspace returns.  FL_ERR_UNSUPPORTED for other
+ * group sizes. */
+int fl_moe_int4g_g(const void* x, const float* logits, int M, int H, int E, int k, int I,
+                   const fl_moe_routing* routing, int group,
+                   const void* w13, const void* w2,
+                   const void* shared_w13, const void* shared_w2,
+                   void* y, int32_t* topk_ids, float* topk_w,
+                   int32_t* expert_offsets, int32_t* perm,
+                   void* ws, size_t ws_bytes, fl_stream_t stream);
 
 /* fl_moe_int4g_ex with each expert's matrices at its own address: w13 and
  * w2 are DEVICE arrays of E device pointers (w13[e]: interleaved [2I, H] of

@@ -18,6 +18,7 @@ __all__ = [
     "fl_strerror", "fl_int4g_version", "fl_int4g_status",
     "fl_int4g_quantize", "fl_int4g_repacked_bytes", "fl_int4g_repack", "fl_int4g_unrepack",
     "fl_int4g_linear_workspace", "fl_int4g_linear", "fl_int4g_linear_noalloc", "fl_int4g_linear_noalloc_status",
+    "fl_int4g_linear_g", "fl_moe_int4g_g",
     "fl_int4g_test_withhold_cluster_arrival",
     "fl_moe_int4g_workspace", "fl_moe_int4g", "fl_moe_int4g_ptrs", "FlMoeRouting", "fl_int4g_mlp_workspace",
     "fl_moe_router_logits_workspace", "fl_moe_router_logits",
@@ -50,6 +51,9 @@ SIGNATURES = {
     "fl_int4g_unrepack": (_i, [_vp, ctypes.c_size_t, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "fl_int4g_linear_workspace": (_i, [_i, _i, _i, _c_size_p]),
     "fl_int4g_linear": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
+    "fl_int4g_linear_g": (_i, [_vp, _i, _i, _vp, _i, _i, _vp, _vp, ctypes.c_size_t, _vp]),
+    "fl_moe_int4g_g": (_i, [_vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(FlMoeRouting), _i, _vp, _vp, _vp, _vp,
+                            _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "fl_int4g_linear_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp]),
     "fl_int4g_linear_noalloc_status": (_i, [_vp, ctypes.POINTER(_i)]),
     "fl_int4g_test_withhold_cluster_arrival": (_i, [ctypes.c_longlong]),
@@ -195,8 +199,10 @@ def fl_int4g_linear_workspace(M, N, K):
     return out.value
 
 
-def fl_int4g_linear(x, w, N, y=None, ws=None):
-    """y[M, N] bf16 = x[M, K] bf16 . deq(W)^T, W given in the interleaved layout."""
+def fl_int4g_linear(x, w, N, y=None, ws=None, group=GROUP):
+    """y[M, N] bf16 = x[M, K] bf16 . deq(W)^T, W given in the interleaved
+    layout of groups of `group` (128 and 256 share one layout; 64 adds the
+    side array: fl_int4g_linear_g)."""
     torch = _torch()
     M, K = x.shape
     if y is None:
@@ -204,8 +210,12 @@ def fl_int4g_linear(x, w, N, y=None, ws=None):
     nb = fl_int4g_linear_workspace(M, N, K)
     if ws is None:
         ws = _workspace(nb, x.device)
-    _check("fl_int4g_linear",
-           lib().fl_int4g_linear(_p(x), M, K, _p(w), N, _p(y), _p(ws), ws.numel(), _stream()))
+    if group == GROUP:
+        _check("fl_int4g_linear",
+               lib().fl_int4g_linear(_p(x), M, K, _p(w), N, _p(y), _p(ws), ws.numel(), _stream()))
+    else:
+        _check("fl_int4g_linear_g",
+               lib().fl_int4g_linear_g(_p(x), M, K, _p(w), N, int(group), _p(y), _p(ws), ws.numel(), _stream()))
     return y
 
 
@@ -267,7 +277,7 @@ def fl_moe_int4g_workspace(M, E, k, H, I, has_shared):
 
 def fl_moe_int4g(x, logits, k, I, w13, w2, scoring=FL_SOFTMAX, renorm=True, shared_w13=None, shared_w2=None,
                  y=None, topk_ids=None, topk_w=None, expert_offsets=None, perm=None, ws=None,
-                 score_bias=None, n_group=1, topk_group=1, routed_scale=1.0):
+                 score_bias=None, n_group=1, topk_group=1, routed_scale=1.0, group=GROUP):
     """Routed MoE layer.  w13 / w2: uint8 CUDA tensors holding the E
     interleaved expert matrices back to back.  Optional routing outputs are
     written when given.  score_bias (fp32 [E] CUDA tensor), n_group /
@@ -282,6 +292,15 @@ def fl_moe_int4g(x, logits, k, I, w13, w2, scoring=FL_SOFTMAX, renorm=True, shar
     nb = fl_moe_int4g_workspace(M, E, k, H, I, has_shared)
     if ws is None:
         ws = _workspace(nb, x.device)
+    if group != GROUP:
+        r = FlMoeRouting(scoring, int(bool(renorm)), _p(score_bias), int(n_group), int(topk_group),
+                         float(routed_scale))
+        _check("fl_moe_int4g_g",
+               lib().fl_moe_int4g_g(_p(x), _p(logits), M, H, E, k, I, ctypes.byref(r), int(group),
+                                    _p(w13), _p(w2), _p(shared_w13), _p(shared_w2), _p(y),
+                                    _p(topk_ids), _p(topk_w), _p(expert_offsets), _p(perm),
+                                    _p(ws), ws.numel(), _stream()))
+        return y
     if score_bias is None and n_group <= 1 and routed_scale == 1.0:
         _check("fl_moe_int4g",
                lib().fl_moe_int4g(_p(x), _p(logits), M, H, E, k, I, scoring, int(bool(renorm)),

@@ -59,6 +59,7 @@ struct PfCfg {
 
 struct PfParams {
   const uint8_t* w;    // interleaved weights, first row tile of this launch
+  const uint8_t* side; // groups of 64: side entries of the same super-blocks (else null)
   __nv_bfloat16* y;    // y + n0 (first row of this launch)
   float* part;         // 2P partial slots of 128 x BN floats, [column][row]
   int32_t* cnt;        // ticket counters [tile][8]
@@ -437,13 +438,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
     const uint32_t trow = static_cast<uint32_t>(q * 32) << 16;
     for (int i = 0; i < nu; ++i) {
       const int sI = i % NSS, a = i % RA;
+      // groups of 64: the upper K half takes the odd group's scale and zero
+      // point from the side entry (read before the wait, to overlap it)
+      const bool odd = p.side != nullptr && h == 1;
+      float sf = 0.f;
+      uint32_t z = 0;
+      if (odd) {
+        const int u = sq.at(i), T = u / p.G, g = u - T * p.G, nt = T / p.mtiles;
+        const uint8_t* sd = p.side + (static_cast<size_t>(nt) * p.G + g) * kSbSide;
+        sf = __half2float(__ldg(reinterpret_cast<const __half*>(sd) + r));
+        z = (__ldg(sd + kSbScale + (r >> 1)) >> ((r & 1) * 4)) & 15u;
+      }
       if (!mbar_wait(&sfull[sI], static_cast<uint32_t>(i / NSS) & 1u)) {
         set_status(p.status, FL_ERR_TIMEOUT, 35);
         break;
       }
       const uint8_t* sb = smem + C::kSOff + sI * kSbBytes;
-      const float sf = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
-      const uint32_t z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
+      if (!odd) {
+        sf = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
+        z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
+      }
       uint4 cv[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) cv[t] = *reinterpret_cast<const uint4*>(sb + r * 64 + ((t + (r >> 1)) & 3) * 16);
@@ -646,7 +660,8 @@ size_t pf_workspace(int M) {
 }
 
 template <int BN>
-int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, void* ws, cudaStream_t s) {
+int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, void* ws, cudaStream_t s,
+              const uint8_t* side) {
   using C = PfCfg<BN>;
   auto enc = encode_fn();
   if (!enc) return FL_ERR_CUDA;
@@ -680,6 +695,7 @@ int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, void* 
     const int nts = ntiles - nt0 < nt_chunk ? ntiles - nt0 : nt_chunk;
     PfParams p;
     p.w = static_cast<const uint8_t*>(w) + static_cast<size_t>(nt0) * G * kSbBytes;
+    p.side = side ? side + static_cast<size_t>(nt0) * G * kSbSide : nullptr;
     p.y = static_cast<__nv_bfloat16*>(y) + static_cast<size_t>(nt0) * kRowTile;
     p.part = reinterpret_cast<float*>(wsb + kScratchOff);
     p.cnt = reinterpret_cast<int32_t*>(wsb + kTicketOff);
@@ -1102,6 +1118,7 @@ struct MgParams {
   const uint8_t* const* wtab;  // device table of E expert pointers, or null
   const uint8_t* w_shared;   // shared expert (expert index E) or null
   size_t wbytes;             // bytes of one expert's interleaved matrix
+  size_t side_off;           // groups of 64: offset of an expert's side array from its base (0: none)
   const int32_t* seg_e;
   const int32_t* seg_pos;
   const int32_t* seg_n;
@@ -1272,13 +1289,32 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
     const uint32_t trow = static_cast<uint32_t>(q * 32) << 16;
     for (int i = 0; i < nu; ++i) {
       const int sI = i % NSS, a = i % RA;
+      // groups of 64: the upper K half takes the odd group's scale and zero
+      // point from the expert's side entry (read before the wait)
+      const bool odd = p.side_off != 0 && h == 1;
+      float sf = 0.f;
+      uint32_t z = 0;
+      bool odd_ok = false;
+      if (odd) {
+        const int t = t0 + i / p.G, g = i - (i / p.G) * p.G;
+        const int sg = t / p.TT, nt = t - sg * p.TT, e = p.seg_e[sg];
+        const uint8_t* base = e == p.E ? p.w_shared : expert_base(p.w, p.wtab, p.wbytes, e, p.status);
+        if (base) {
+          const uint8_t* sd = base + p.side_off + (static_cast<size_t>(nt) * p.G + g) * kSbSide;
+          sf = __half2float(__ldg(reinterpret_cast<const __half*>(sd) + r));
+          z = (__ldg(sd + kSbScale + (r >> 1)) >> ((r & 1) * 4)) & 15u;
+          odd_ok = true;
+        }
+      }
       if (!mbar_wait(&sfull[sI], static_cast<uint32_t>(i / NSS) & 1u)) {
         set_status(p.status, FL_ERR_TIMEOUT, 44);
         break;
       }
       const uint8_t* sb = smem + C::kSOff + sI * kSbBytes;
-      const float sf = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
-      const uint32_t z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
+      if (!odd_ok) {
+        sf = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
+        z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
+      }
       uint4 cv[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) cv[t] = *reinterpret_cast<const uint4*>(sb + r * 64 + ((t + (r >> 1)) & 3) * 16);
@@ -1370,9 +1406,12 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
 // Prefill path of fl_int4g_linear (M > 32): persistent stream-K tcgen05 GEMM.
 size_t fl_linear_tc_workspace(int M) { return pf_workspace(M); }
 
-int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, void* ws, cudaStream_t s) {
-  if (pf_bn(M) == 256) return launch_tc<256>(x, M, K, w, N, y, ws, s);
-  return launch_tc<128>(x, M, K, w, N, y, ws, s);
+// side: groups of 64, the side array of w (null for groups of 128 / 256).
+int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, void* ws, cudaStream_t s,
+                 const void* side) {
+  const uint8_t* sd = static_cast<const uint8_t*>(side);
+  if (pf_bn(M) == 256) return launch_tc<256>(x, M, K, w, N, y, ws, s, sd);
+  return launch_tc<128>(x, M, K, w, N, y, ws, s, sd);
 }
 
 // Decode path of fl_int4g_linear on tcgen05 (M <= 32); the workspace layout is
@@ -1388,8 +1427,9 @@ int fl_linear_tcdec(const void* x, int M, int K, const void* w, int N, void* y, 
 // rows in position order; out: [npos, ldo] fp32.  nseg, seg_* and wpos are
 // device arrays written by earlier kernels on the same stream.
 int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* const* wtab, const void* w_shared,
-                size_t wbytes, int E, int Nout, const int32_t* seg_e, const int32_t* seg_pos, const int32_t* seg_n,
-                const int32_t* nseg, const float* wpos, float* out, int32_t* status, cudaStream_t s) {
+                size_t wbytes, size_t side_off, int E, int Nout, const int32_t* seg_e, const int32_t* seg_pos,
+                const int32_t* seg_n, const int32_t* nseg, const float* wpos, float* out, int32_t* status,
+                cudaStream_t s) {
   auto enc = encode_fn();
   if (!enc) return FL_ERR_CUDA;
   CUtensorMap map;
@@ -1414,6 +1454,7 @@ int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* const
   p.wtab = reinterpret_cast<const uint8_t* const*>(wtab);
   p.w_shared = static_cast<const uint8_t*>(w_shared);
   p.wbytes = wbytes;
+  p.side_off = side_off;
   p.seg_e = seg_e;
   p.seg_pos = seg_pos;
   p.seg_n = seg_n;

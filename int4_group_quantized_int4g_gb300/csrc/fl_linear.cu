@@ -42,6 +42,7 @@ static_assert(kMaxRowTiles == kTicketTiles && kConsumerWarps == kTicketWarps,
 
 struct RowsParams {
   const uint8_t* w;
+  const uint8_t* side;   // groups of 64: the side array (the odd groups' scales and zeros), else null
   const __nv_bfloat16* x;
   __nv_bfloat16* y;
   float* part;       // [P + T][128][Mp] fp32 partial sums (slot = CTA + tile)
@@ -209,14 +210,16 @@ __device__ __forceinline__ void cluster_reduce(const RowsParams& p, int T, int r
 // a cluster sharing a row tile (its range lies inside that tile, group slot
 // = unit index in the range, no tile boundaries); otherwise a stream-K range
 // that may cross row tiles, finished through the ticket hand-off.
-template <int NT, int UPS, bool CL>
+template <int NT, int UPS, bool CL, bool G64>
 __device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                              const float* xsum, int u0, int u1, int g0, int nslot, int nstage,
                                              int c, int rank, int warp, int lane, uint64_t* red_bar,
                                              float* red_buf) {
   constexpr bool FOLD = NT <= 2;
   constexpr int Mp = 8 * NT;
+  constexpr int XS = G64 ? 2 : 1;          // token sums per group slot: one per 64-column group
   const uint32_t xoff = UPS * kSbBytes;
+  const uint32_t soff = xoff + UPS * p.M * kXRowStride;   // G64: the stage's side entries
   const int gid = lane >> 2, tig = lane & 3;
   const int r0 = warp * 16 + gid;
   const uint8_t* xzero = smem + p.zrow_off;
@@ -236,16 +239,27 @@ __device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem,
       return;
     }
     const uint8_t* sb = smem + static_cast<size_t>(s) * p.stage_bytes;
-    float acc[UPS][NT][4];
-    float sc[UPS][2];
-    uint32_t zr[UPS][2];
+    // G64: index [half] = the 64-column group (0: columns 0..63 of the super-block)
+    float acc[UPS][XS][NT][4];
+    float sc[UPS][XS][2];
+    uint32_t zr[UPS][XS][2];
     // Every slot of the stage is computed, in one basic block so that the
     // compiler interleaves the independent MMA chains; a slot past the end
     // of the range holds stale shared memory and its result is dropped.
 #pragma unroll
-    for (int i = 0; i < UPS; ++i)
-      unit_dot<NT, FOLD, true>(sb + i * kSbBytes, sb + xoff + i * p.M * kXRowStride, p.M, r0, gid, tig, acc[i],
-                               sc[i][0], sc[i][1], zr[i][0], zr[i][1], NT, xzero);
+    for (int i = 0; i < UPS; ++i) {
+      if constexpr (G64) {
+        float s0[2], s1[2];
+        uint32_t z0[2], z1[2];
+        unit_dot64<NT, FOLD, true>(sb + i * kSbBytes, sb + soff + i * kSbSide, sb + xoff + i * p.M * kXRowStride, p.M,
+                                   r0, gid, tig, acc[i], s0, s1, z0, z1, NT, xzero);
+#pragma unroll
+        for (int hh = 0; hh < XS; ++hh) sc[i][hh][0] = s0[hh], sc[i][hh][1] = s1[hh], zr[i][hh][0] = z0[hh], zr[i][hh][1] = z1[hh];
+      } else {
+        unit_dot<NT, FOLD, true>(sb + i * kSbBytes, sb + xoff + i * p.M * kXRowStride, p.M, r0, gid, tig, acc[i][0],
+                                 sc[i][0][0], sc[i][0][1], zr[i][0][0], zr[i][0][1], NT, xzero);
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
@@ -253,15 +267,17 @@ __device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem,
       if (i < n) {
         const int sl = CL ? k * UPS + i : (slot < nslot ? slot : 0);
 #pragma unroll
+        for (int hh = 0; hh < XS; ++hh)
+#pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float2 xs = make_float2(0.f, 0.f);
-          if (FOLD) xs = *reinterpret_cast<const float2*>(xsum + sl * Mp + nt * 8 + 2 * tig);
+          if (FOLD) xs = *reinterpret_cast<const float2*>(xsum + (sl * XS + hh) * Mp + nt * 8 + 2 * tig);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float v = acc[i][nt][e];
+            float v = acc[i][hh][nt][e];
             // 128 + z as a float without a conversion: z in the mantissa of 128.0
-            if (FOLD) v = fmaf(-__uint_as_float(0x43000000u + (zr[i][e >> 1] << 16)), (e & 1) ? xs.y : xs.x, v);
-            tot[nt][e] = fmaf(sc[i][e >> 1], v, tot[nt][e]);
+            if (FOLD) v = fmaf(-__uint_as_float(0x43000000u + (zr[i][hh][e >> 1] << 16)), (e & 1) ? xs.y : xs.x, v);
+            tot[nt][e] = fmaf(sc[i][hh][e >> 1], v, tot[nt][e]);
           }
         }
         if (!CL) {
@@ -300,14 +316,15 @@ __device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem,
 // 2 (M <= 8, ~100 KB of stages each), 3 (M <= 8 when the row tiles' clusters
 // would fill the GPU's cluster capacity at 2: smaller stages, fewer
 // registers, so that every cluster is resident in one wave) or 1 (M > 8).
-template <int NT, int UPS, int MINB>
+template <int NT, int UPS, int MINB, bool G64>
 __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams p) {
   constexpr bool FOLD = NT <= 2;
   constexpr int Mp = 8 * NT;
+  constexpr int XS = G64 ? 2 : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
   uint64_t* empty = full + p.stages;
-  float* xsum = reinterpret_cast<float*>(empty + p.stages);   // [group slot][Mp]: sum_k x over each group
+  float* xsum = reinterpret_cast<float*>(empty + p.stages);   // [group slot][XS][Mp]: sum_k x over each group
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   // stream-K ranges, or (clusters) K slice `rank` of row tile c / csize
@@ -346,12 +363,16 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
   if (warp == kConsumerWarps) {
     // ---------------- producer warp
     const uint64_t pol = policy_evict_first();
-    auto issue_w = [&](int k, int slot) {   // weights of stage k (contiguous super-blocks)
+    auto issue_w = [&](int k, int slot) {   // weights of stage k (contiguous super-blocks, and side entries)
       const int ua = u0 + k * UPS, n = min(UPS, u1 - ua);
       if (lane == 0) {
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(n) * (kSbBytes + p.M * 256u));
-        bulk_g2s_hint(smem + static_cast<size_t>(slot) * p.stage_bytes, p.w + static_cast<size_t>(ua) * kSbBytes,
-                      static_cast<uint32_t>(n) * kSbBytes, &full[slot], pol);
+        uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(n) * (kSbBytes + p.M * 256u + (G64 ? kSbSide : 0)));
+        bulk_g2s_hint(st, p.w + static_cast<size_t>(ua) * kSbBytes, static_cast<uint32_t>(n) * kSbBytes, &full[slot],
+                      pol);
+        if (G64)
+          bulk_g2s_hint(st + xoff + UPS * p.M * kXRowStride, p.side + static_cast<size_t>(ua) * kSbSide,
+                        static_cast<uint32_t>(n) * kSbSide, &full[slot], pol);
       }
     };
     auto issue_x = [&](int k, int slot) {   // the M token rows' slices of stage k's groups
@@ -426,22 +447,27 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
         }
         v = (a[0] + a[1]) + (a[2] + a[3]);
       }
+      // part 0, 1: columns 0..63 of the group, 2, 3: columns 64..127
       v += __shfl_xor_sync(0xffffffffu, v, 1);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      if (part == 0 && it < items) xsum[(it / p.M) * Mp + it % p.M] = v;
+      if (G64) {
+        if ((part & 1) == 0 && it < items) xsum[((it / p.M) * XS + (part >> 1)) * Mp + it % p.M] = v;
+      } else {
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (part == 0 && it < items) xsum[(it / p.M) * Mp + it % p.M] = v;
+      }
     }
-    for (int idx = threadIdx.x; idx < nslot * (Mp - p.M); idx += kConsumerWarps * 32) {
+    for (int idx = threadIdx.x; idx < nslot * XS * (Mp - p.M); idx += kConsumerWarps * 32) {
       const int i = idx / (Mp - p.M), m = p.M + idx - i * (Mp - p.M);
       xsum[i * Mp + m] = 0.f;
     }
     named_bar(1, kConsumerWarps * 32);
   }
   if (p.csize > 1)
-    rows_consume<NT, UPS, true>(p, smem, full, empty, xsum, u0, u1, g0, nslot, nstage, c, rank, warp, lane,
-                                red_bar, red_buf);
+    rows_consume<NT, UPS, true, G64>(p, smem, full, empty, xsum, u0, u1, g0, nslot, nstage, c, rank, warp, lane,
+                                     red_bar, red_buf);
   else
-    rows_consume<NT, UPS, false>(p, smem, full, empty, xsum, u0, u1, g0, nslot, nstage, c, rank, warp, lane,
-                                 red_bar, red_buf);
+    rows_consume<NT, UPS, false, G64>(p, smem, full, empty, xsum, u0, u1, g0, nslot, nstage, c, rank, warp, lane,
+                                      red_bar, red_buf);
 }
 
 // ------------------------------------------------------------------ plan
@@ -453,8 +479,9 @@ struct RowsPlan {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// minb: CTAs per SM the kernel is built for (0 = the default for M).
-bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0) {
+// minb: CTAs per SM the kernel is built for (0 = the default for M); g64:
+// groups of 64 (side entries in the stages, two token sums per group).
+bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bool g64 = false) {
   if (M < 1 || M > kMaxTokens || N < 1 || K < kGroup || K % kGroup || sms < 1) return false;
   if ((N + kRowTile - 1) / kRowTile > kMaxRowTiles) return false;
   pl->T = (N + kRowTile - 1) / kRowTile;
@@ -484,15 +511,15 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0) {
     pl->P = static_cast<int>(U < slots ? U : slots);
   const size_t red_bytes =
       pl->csize > 1 ? 16 + static_cast<size_t>(pl->csize - 1) * kConsumerWarps * 32 * 4 * pl->NT * sizeof(float) : 0;
-  pl->stage_bytes = static_cast<uint32_t>(
-      align_up(static_cast<size_t>(pl->ups) * (kSbBytes + static_cast<size_t>(M) * kXRowStride), 128));
+  pl->stage_bytes = static_cast<uint32_t>(align_up(
+      static_cast<size_t>(pl->ups) * (kSbBytes + static_cast<size_t>(M) * kXRowStride + (g64 ? kSbSide : 0)), 128));
   const size_t budget = (pl->minb == 3 ? 66u * 1024u : pl->minb == 2 ? 100u * 1024u : 200u * 1024u) - red_bytes;
   int stages = static_cast<int>(budget / pl->stage_bytes);
   pl->stages = stages > 12 ? 12 : (stages < 2 ? 2 : stages);
   const int units_max = pl->csize > 1 ? (pl->G + pl->csize - 1) / pl->csize : (pl->U + pl->P - 1) / pl->P;
   const int nslot = units_max < pl->G ? units_max : pl->G;
   pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes + 2 * pl->stages * sizeof(uint64_t) +
-             static_cast<size_t>(nslot) * 8 * pl->NT * sizeof(float);
+             static_cast<size_t>(nslot) * (g64 ? 2 : 1) * 8 * pl->NT * sizeof(float);
   pl->zrow_off = static_cast<uint32_t>(align_up(pl->smem, 16));
   pl->smem = pl->zrow_off + 256;
   pl->red_off = static_cast<uint32_t>(align_up(pl->smem, 16));
@@ -503,12 +530,12 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0) {
   return true;
 }
 
-template <int NT, int UPS, int MINB>
+template <int NT, int UPS, int MINB, bool G64>
 bool rows_attr(int dev) {
   static bool attr_done[64] = {false};
   if (dev < 0 || dev >= 64) return false;
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(k_linear_rows<NT, UPS, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_linear_rows<NT, UPS, MINB, G64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              227 * 1024) != cudaSuccess)
       return false;
     attr_done[dev] = true;
@@ -529,7 +556,7 @@ int rows_cluster_capacity(const RowsPlan& pl) {
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n; ++i)
     if (cache[i].dev == dev && cache[i].csize == pl.csize && cache[i].smem == pl.smem) return cache[i].cap;
-  if (!rows_attr<1, 2, 2>(dev)) return -1;
+  if (!rows_attr<1, 2, 2, false>(dev)) return -1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.P);
   cfg.blockDim = dim3(kThreads);
@@ -542,7 +569,7 @@ int rows_cluster_capacity(const RowsPlan& pl) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int cap = -1;
-  if (cudaOccupancyMaxActiveClusters(&cap, k_linear_rows<1, 2, 2>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&cap, k_linear_rows<1, 2, 2, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     cap = -1;
   }
@@ -550,11 +577,11 @@ int rows_cluster_capacity(const RowsPlan& pl) {
   return cap;
 }
 
-template <int NT, int UPS, int MINB>
+template <int NT, int UPS, int MINB, bool G64>
 int launch_rows(const RowsPlan& pl, const RowsParams& prm, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (!rows_attr<NT, UPS, MINB>(dev)) return FL_ERR_CUDA;
+  if (!rows_attr<NT, UPS, MINB, G64>(dev)) return FL_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.P);
   cfg.blockDim = dim3(kThreads);
@@ -569,7 +596,7 @@ int launch_rows(const RowsPlan& pl, const RowsParams& prm, cudaStream_t s) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pl.csize > 1 ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, k_linear_rows<NT, UPS, MINB>, prm) != cudaSuccess) return FL_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, k_linear_rows<NT, UPS, MINB, G64>, prm) != cudaSuccess) return FL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
@@ -593,10 +620,12 @@ int fl_linear_rows_workspace(int M, int N, int K, size_t* out) {
   return FL_OK;
 }
 
+// group: 128 (or 256: the same layout) or 64 (side array after the super-blocks).
 int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, void* ws, size_t ws_bytes,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, int group = kGroup) {
+  const bool g64 = group == kGroup / 2;
   RowsPlan pl;
-  if (!make_rows_plan(M, N, K, flh::sm_count(), &pl)) return FL_ERR_ARG;
+  if (!make_rows_plan(M, N, K, flh::sm_count(), &pl, 0, g64)) return FL_ERR_ARG;
   if (ws_bytes < pl.ws_bytes) return FL_ERR_WORKSPACE;
   // Clusters that would fill the GPU's cluster capacity leave some of them
   // waiting for a second wave whenever the previous kernel's exits fragment
@@ -604,10 +633,11 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   // grid, same workspace), which has capacity to spare.
   if (pl.NT == 1 && pl.csize > 1) {
     const int cap = rows_cluster_capacity(pl);
-    if (cap > 0 && pl.T > cap - 2 && !make_rows_plan(M, N, K, flh::sm_count(), &pl, 3)) return FL_ERR_ARG;
+    if (cap > 0 && pl.T > cap - 2 && !make_rows_plan(M, N, K, flh::sm_count(), &pl, 3, g64)) return FL_ERR_ARG;
   }
   RowsParams prm;
   prm.w = static_cast<const uint8_t*>(w);
+  prm.side = g64 ? static_cast<const uint8_t*>(w) + static_cast<size_t>(pl.U) * kSbBytes : nullptr;
   prm.x = static_cast<const __nv_bfloat16*>(x);
   prm.y = static_cast<__nv_bfloat16*>(y);
   prm.status = static_cast<int32_t*>(ws);
@@ -628,11 +658,21 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   const long long hook = g_withhold_ns.load();
   prm.withhold = (hook >= 0 && pl.csize > 1) ? 1 : 0;
   prm.red_wait_ns = prm.withhold ? static_cast<unsigned long long>(hook) : kWaitLimitNs;
+  if (g64) {
+    switch (pl.NT) {
+      case 1:
+        return pl.minb == 3 ? launch_rows<1, 2, 3, true>(pl, prm, stream) : launch_rows<1, 2, 2, true>(pl, prm, stream);
+      case 2: return launch_rows<2, 2, 1, true>(pl, prm, stream);
+      case 3: return launch_rows<3, 1, 1, true>(pl, prm, stream);
+      default: return launch_rows<4, 1, 1, true>(pl, prm, stream);
+    }
+  }
   switch (pl.NT) {
-    case 1: return pl.minb == 3 ? launch_rows<1, 2, 3>(pl, prm, stream) : launch_rows<1, 2, 2>(pl, prm, stream);
-    case 2: return launch_rows<2, 2, 1>(pl, prm, stream);
-    case 3: return launch_rows<3, 1, 1>(pl, prm, stream);
-    default: return launch_rows<4, 1, 1>(pl, prm, stream);
+    case 1:
+      return pl.minb == 3 ? launch_rows<1, 2, 3, false>(pl, prm, stream) : launch_rows<1, 2, 2, false>(pl, prm, stream);
+    case 2: return launch_rows<2, 2, 1, false>(pl, prm, stream);
+    case 3: return launch_rows<3, 1, 1, false>(pl, prm, stream);
+    default: return launch_rows<4, 1, 1, false>(pl, prm, stream);
   }
 }
 
@@ -643,7 +683,8 @@ static bool linear_args_ok(const void* x, int M, int K, const void* w, int N, co
 }
 
 size_t fl_linear_tc_workspace(int M);
-int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, void* ws, cudaStream_t s);
+int fl_linear_tc(const void* x, int M, int K, const void* w, int N, void* y, void* ws, cudaStream_t s,
+                 const void* side);
 int fl_linear_tcdec(const void* x, int M, int K, const void* w, int N, void* y, void* ws, size_t cnt_off,
                     size_t part_off, cudaStream_t s);
 
@@ -696,7 +737,27 @@ extern "C" int fl_int4g_linear(const void* x, int M, int K, const void* w, int N
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (M > kMaxTokens) {
     if (ws_bytes < fl_linear_tc_workspace(M)) return FL_ERR_WORKSPACE;
-    return fl_linear_tc(x, M, K, w, N, y, ws, s);
+    return fl_linear_tc(x, M, K, w, N, y, ws, s, nullptr);
   }
   return fl_linear_decode(x, M, K, w, N, y, ws, ws_bytes, s);
+}
+
+extern "C" int fl_int4g_linear_g(const void* x, int M, int K, const void* w, int N, int group, void* y, void* ws,
+                                 size_t ws_bytes, fl_stream_t stream) {
+  if (group == kGroup || group == 2 * kGroup) return fl_int4g_linear(x, M, K, w, N, y, ws, ws_bytes, stream);
+  if (group != kGroup / 2) return FL_ERR_UNSUPPORTED;
+  if (!linear_args_ok(x, M, K, w, N, y, ws)) return FL_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t nsb = static_cast<size_t>((N + kRowTile - 1) / kRowTile) * (K / kGroup);
+  const uint8_t* side = static_cast<const uint8_t*>(w) + nsb * kSbBytes;
+  if (M > kMaxTokens) {
+    if (ws_bytes < fl_linear_tc_workspace(M)) return FL_ERR_WORKSPACE;
+    return fl_linear_tc(x, M, K, w, N, y, ws, s, side);
+  }
+  // decode: the mma.sync kernel for every M <= 32 (the tcgen05 decode kernel
+  // keeps one accumulator per 128 columns)
+  size_t need = 0;
+  if (fl_linear_decode_workspace(M, N, K, &need) != FL_OK) return FL_ERR_ARG;
+  if (ws_bytes < need) return FL_ERR_WORKSPACE;
+  return fl_linear_rows(x, M, K, w, N, y, ws, ws_bytes, s, kGroup / 2);
 }

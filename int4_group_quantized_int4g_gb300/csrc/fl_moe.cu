@@ -368,6 +368,7 @@ struct MoeRowsParams {
   const uint8_t* const* wtab;  // device table of E expert pointers, or null
   const uint8_t* w_shared;     // shared expert (or null)
   size_t wbytes;               // bytes of one expert's matrix
+  size_t side_off;             // groups of 64: offset of an expert's side array from its base (0: none)
   const __nv_bfloat16* x;      // MODE 0: x [M, K]; MODE 1: h [pos, K]
   int K, G, TT;                // K = reduction length, G = K/128, TT = output tiles
   int up_off;                  // MODE 0: I/128
@@ -501,9 +502,10 @@ __device__ __forceinline__ bool store(const MoeRowsParams& p, int gt, int c, int
   return true;
 }
 
-template <int MODE>
+template <int MODE, bool G64>
 __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p) {
   constexpr int SB = MoeIO<MODE>::kSB;
+  constexpr int XS = G64 ? 2 : 1;   // accumulator chains per super-block: one per 64-column group
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
   uint64_t* empty = full + p.stages;
@@ -549,12 +551,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p)
         // a bad table entry (recorded) skips the weight copy: the stage then
         // completes on its activations alone and its result is garbage
         const uint8_t* base = e == p.E ? p.w_shared : expert_base(p.w, p.wtab, p.wbytes, e, p.status);
-        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>((base ? SB * kSbBytes : 0) + nt_ok * 256));
+        mbar_arrive_expect_tx(&full[s],
+                              static_cast<uint32_t>((base ? SB * (kSbBytes + (G64 ? kSbSide : 0)) : 0) + nt_ok * 256));
         if (base) {
-          bulk_g2s_hint(st, base + (static_cast<size_t>(tile) * p.G + g) * kSbBytes, kSbBytes, &full[s], pol);
-          if (SB == 2)
-            bulk_g2s_hint(st + kSbBytes, base + (static_cast<size_t>(tile + p.up_off) * p.G + g) * kSbBytes,
-                          kSbBytes, &full[s], pol);
+          const size_t u_a = static_cast<size_t>(tile) * p.G + g, u_b = static_cast<size_t>(tile + p.up_off) * p.G + g;
+          bulk_g2s_hint(st, base + u_a * kSbBytes, kSbBytes, &full[s], pol);
+          if (SB == 2) bulk_g2s_hint(st + kSbBytes, base + u_b * kSbBytes, kSbBytes, &full[s], pol);
+          if (G64) {   // side entries after the x rows
+            uint8_t* sd = st + xoff + kSegRows * kXRowStride;
+            bulk_g2s_hint(sd, base + p.side_off + u_a * kSbSide, kSbSide, &full[s], pol);
+            if (SB == 2) bulk_g2s_hint(sd + kSbSide, base + p.side_off + u_b * kSbSide, kSbSide, &full[s], pol);
+          }
         }
       }
       __syncwarp();
@@ -587,20 +594,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p)
       return;
     }
     const uint8_t* sb = smem + static_cast<size_t>(s) * p.stage_bytes;
-    float ag[kNT][4], au[kNT][4];
-    float s0g, s1g, s0u = 0.f, s1u = 0.f;
-    uint32_t z0, z1;
+    float ag[XS][kNT][4], au[XS][kNT][4];
+    float s0g[XS], s1g[XS], s0u[XS], s1u[XS];
     const int ntiles = (nt_ok + 7) / 8;
-    unit_dot<kNT, false>(sb, sb + xoff, nt_ok, r0, gid, tig, ag, s0g, s1g, z0, z1, ntiles);
-    if (SB == 2) unit_dot<kNT, false>(sb + kSbBytes, sb + xoff, nt_ok, r0, gid, tig, au, s0u, s1u, z0, z1, ntiles);
+    if constexpr (G64) {
+      const uint8_t* sd = sb + xoff + kSegRows * kXRowStride;
+      uint32_t z0[2], z1[2];
+      unit_dot64<kNT, false>(sb, sd, sb + xoff, nt_ok, r0, gid, tig, ag, s0g, s1g, z0, z1, ntiles);
+      if (SB == 2)
+        unit_dot64<kNT, false>(sb + kSbBytes, sd + kSbSide, sb + xoff, nt_ok, r0, gid, tig, au, s0u, s1u, z0, z1,
+                               ntiles);
+    } else {
+      uint32_t z0, z1;
+      unit_dot<kNT, false>(sb, sb + xoff, nt_ok, r0, gid, tig, ag[0], s0g[0], s1g[0], z0, z1, ntiles);
+      if (SB == 2)
+        unit_dot<kNT, false>(sb + kSbBytes, sb + xoff, nt_ok, r0, gid, tig, au[0], s0u[0], s1u[0], z0, z1, ntiles);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+    for (int hh = 0; hh < XS; ++hh)
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        tg[nt][e] = fmaf(e < 2 ? s0g : s1g, ag[nt][e], tg[nt][e]);
-        if (SB == 2) tu[nt][e] = fmaf(e < 2 ? s0u : s1u, au[nt][e], tu[nt][e]);
+        tg[nt][e] = fmaf(e < 2 ? s0g[hh] : s1g[hh], ag[hh][nt][e], tg[nt][e]);
+        if (SB == 2) tu[nt][e] = fmaf(e < 2 ? s0u[hh] : s1u[hh], au[hh][nt][e], tu[nt][e]);
       }
     if (++s == p.stages) s = 0, ph ^= 1u;
     if ((u + 1) % p.G == 0 && u + 1 < u1) {
@@ -676,7 +695,7 @@ bool moe_uses_gemm(int M, int E, int k, int H) {
   return n >= 8LL * E || (n >= 2LL * E && H >= 4096);
 }
 
-bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeLayout* L) {
+bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeLayout* L, bool g64 = false) {
   if (M < 1 || E < 1 || E > kMaxE || k < 1 || k > E || k > 32 || H < kGroup || I < kGroup || H % kGroup ||
       I % kGroup || sms < 1)
     return false;
@@ -709,8 +728,9 @@ bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeL
   L->xp = o; o = al(o + (L->gemm ? 2ull * npos * H : 0));
   L->gu = o; o = al(o + (L->gemm ? 4ull * npos * 2 * I : 0));
   L->total = o;
-  L->stage13 = static_cast<uint32_t>((2 * kSbBytes + kSegRows * kXRowStride + 127) / 128 * 128);
-  L->stage2 = static_cast<uint32_t>((kSbBytes + kSegRows * kXRowStride + 127) / 128 * 128);
+  const int side = g64 ? kSbSide : 0;
+  L->stage13 = static_cast<uint32_t>((2 * (kSbBytes + side) + kSegRows * kXRowStride + 127) / 128 * 128);
+  L->stage2 = static_cast<uint32_t>((kSbBytes + side + kSegRows * kXRowStride + 127) / 128 * 128);
   L->stages13 = std::min(8, static_cast<int>((200u * 1024u) / L->stage13));
   L->stages2 = std::min(12, static_cast<int>((200u * 1024u) / L->stage2));
   return true;
@@ -737,8 +757,9 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 }  // namespace
 
 int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* const* wtab, const void* w_shared,
-                size_t wbytes, int E, int Nout, const int32_t* seg_e, const int32_t* seg_pos, const int32_t* seg_n,
-                const int32_t* nseg, const float* wpos, float* out, int32_t* status, cudaStream_t s);
+                size_t wbytes, size_t side_off, int E, int Nout, const int32_t* seg_e, const int32_t* seg_pos,
+                const int32_t* seg_n, const int32_t* nseg, const float* wpos, float* out, int32_t* status,
+                cudaStream_t s);
 
 extern "C" int fl_moe_int4g_workspace(int M, int E, int k, int H, int I, int has_shared, size_t* out) {
   if (!out) return FL_ERR_ARG;
@@ -754,8 +775,10 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
                      const fl_moe_routing* routing, const void* w13, const void* w2, const void* const* w13tab,
                      const void* const* w2tab, const void* shared_w13, const void* shared_w2, void* y,
                      int32_t* topk_ids, float* topk_w, int32_t* expert_offsets, int32_t* perm, void* ws,
-                     size_t ws_bytes, fl_stream_t stream) {
+                     size_t ws_bytes, fl_stream_t stream, int group = kGroup) {
   if (!x || !logits || !y || !ws || !routing) return FL_ERR_ARG;
+  if (group != kGroup && group != 2 * kGroup && group != kGroup / 2) return FL_ERR_UNSUPPORTED;
+  const bool g64 = group == kGroup / 2;
   if ((shared_w13 == nullptr) != (shared_w2 == nullptr)) return FL_ERR_ARG;
   const int scoring = routing->scoring, renorm = routing->renorm;
   if (scoring != FL_SOFTMAX && scoring != FL_SIGMOID) return FL_ERR_ARG;
@@ -775,7 +798,7 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     return FL_ERR_ARG;
   const int has_shared = shared_w13 != nullptr;
   MoeLayout L;
-  if (!moe_layout(M, E, k, H, I, has_shared, flh::sm_count(), &L)) return FL_ERR_ARG;
+  if (!moe_layout(M, E, k, H, I, has_shared, flh::sm_count(), &L, g64)) return FL_ERR_ARG;
   if (ws_bytes < L.total) return FL_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* W = static_cast<uint8_t*>(ws);
@@ -783,8 +806,11 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
   int32_t* ids = topk_ids ? topk_ids : reinterpret_cast<int32_t*>(W + L.ids);
   float* wts = topk_w ? topk_w : reinterpret_cast<float*>(W + L.wts);
   MoePlan* plan = reinterpret_cast<MoePlan*>(W + L.plan);
-  const size_t b13 = static_cast<size_t>(2 * I / kRowTile) * (H / kGroup) * kSbBytes;
-  const size_t b2 = static_cast<size_t>(H / kRowTile) * (I / kGroup) * kSbBytes;
+  // one expert's matrices: super-blocks, then (groups of 64) their side entries
+  const size_t n13 = static_cast<size_t>(2 * I / kRowTile) * (H / kGroup), n2 = static_cast<size_t>(H / kRowTile) * (I / kGroup);
+  const size_t side13 = g64 ? n13 * kSbBytes : 0, side2 = g64 ? n2 * kSbBytes : 0;
+  const size_t b13 = n13 * (kSbBytes + (g64 ? kSbSide : 0));
+  const size_t b2 = n2 * (kSbBytes + (g64 ? kSbSide : 0));
 
   // route
   {
@@ -853,13 +879,13 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     if (launch_pdl(k_moe_gather, dim3(4 * sms), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(x),
                    reinterpret_cast<const int32_t*>(W + L.tok), npos, H, xp) != cudaSuccess)
       return FL_ERR_CUDA;
-    int rc = fl_moe_gemm(xp, npos, H, w13, w13tab, shared_w13, b13, E, 2 * I, sege, segp, segn, nseg, nullptr, gu,
-                         status, s);
+    int rc = fl_moe_gemm(xp, npos, H, w13, w13tab, shared_w13, b13, side13, E, 2 * I, sege, segp, segn, nseg,
+                         nullptr, gu, status, s);
     if (rc != FL_OK) return rc;
     if (launch_pdl(k_moe_swiglu, dim3(4 * sms), dim3(256), 0, s, static_cast<const float*>(gu), npos, I, h) !=
         cudaSuccess)
       return FL_ERR_CUDA;
-    rc = fl_moe_gemm(h, npos, I, w2, w2tab, shared_w2, b2, E, H, sege, segp, segn, nseg,
+    rc = fl_moe_gemm(h, npos, I, w2, w2tab, shared_w2, b2, side2, E, H, sege, segp, segn, nseg,
                      reinterpret_cast<const float*>(W + L.wpos), reinterpret_cast<float*>(W + L.out), status, s);
     if (rc != FL_OK) return rc;
   }
@@ -870,6 +896,7 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     p.wtab = reinterpret_cast<const uint8_t* const*>(mode == 0 ? w13tab : w2tab);
     p.w_shared = static_cast<const uint8_t*>(mode == 0 ? shared_w13 : shared_w2);
     p.wbytes = mode == 0 ? b13 : b2;
+    p.side_off = mode == 0 ? side13 : side2;
     p.x = mode == 0 ? static_cast<const __nv_bfloat16*>(x) : reinterpret_cast<const __nv_bfloat16*>(W + L.h);
     p.K = mode == 0 ? H : I;
     p.G = p.K / kGroup;
@@ -892,14 +919,16 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     p.stages = mode == 0 ? L.stages13 : L.stages2;
     p.stage_bytes = mode == 0 ? L.stage13 : L.stage2;
     const size_t smem = static_cast<size_t>(p.stages) * p.stage_bytes + 2 * p.stages * sizeof(uint64_t);
-    static bool attr_done[2][64] = {{false}};
+    static bool attr_done[4][64] = {{false}};
     int dev = 0;
     cudaGetDevice(&dev);
-    auto kern = mode == 0 ? k_moe_rows<0> : k_moe_rows<1>;
-    if (dev >= 0 && dev < 64 && !attr_done[mode][dev]) {
+    auto kern = g64 ? (mode == 0 ? k_moe_rows<0, true> : k_moe_rows<1, true>)
+                    : (mode == 0 ? k_moe_rows<0, false> : k_moe_rows<1, false>);
+    const int ki = 2 * (g64 ? 1 : 0) + mode;
+    if (dev >= 0 && dev < 64 && !attr_done[ki][dev]) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
         return FL_ERR_CUDA;
-      attr_done[mode][dev] = true;
+      attr_done[ki][dev] = true;
     }
     if (launch_pdl(kern, dim3(L.P), dim3(kThreads), smem, s, p) != cudaSuccess) return FL_ERR_CUDA;
   }
@@ -919,6 +948,16 @@ extern "C" int fl_moe_int4g_ex(const void* x, const float* logits, int M, int H,
   if (!w13 || !w2) return FL_ERR_ARG;
   return moe_layer(x, logits, M, H, E, k, I, routing, w13, w2, nullptr, nullptr, shared_w13, shared_w2, y, topk_ids,
                    topk_w, expert_offsets, perm, ws, ws_bytes, stream);
+}
+
+extern "C" int fl_moe_int4g_g(const void* x, const float* logits, int M, int H, int E, int k, int I,
+                              const fl_moe_routing* routing, int group, const void* w13, const void* w2,
+                              const void* shared_w13, const void* shared_w2, void* y, int32_t* topk_ids,
+                              float* topk_w, int32_t* expert_offsets, int32_t* perm, void* ws, size_t ws_bytes,
+                              fl_stream_t stream) {
+  if (!w13 || !w2) return FL_ERR_ARG;
+  return moe_layer(x, logits, M, H, E, k, I, routing, w13, w2, nullptr, nullptr, shared_w13, shared_w2, y, topk_ids,
+                   topk_w, expert_offsets, perm, ws, ws_bytes, stream, group);
 }
 
 extern "C" int fl_moe_int4g_ptrs(const void* x, const float* logits, int M, int H, int E, int k, int I,

@@ -156,6 +156,48 @@ def test_repack_group64_bit_exact_and_invertible(shape):
     assert np.array_equal(back[0], Q) and np.array_equal(back[1], S) and np.array_equal(back[2], Z)
 
 
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 16, 32, 33, 64, 300])
+@pytest.mark.parametrize("NK", [(384, 1280), (200, 256)])
+def test_linear_group64_parity(M, NK):
+    """Decode (the mma.sync kernel, one accumulator per 64-column group) and
+    prefill (the tcgen05 GEMM, each K half dequantized with its own group's
+    scale) on group-64 weights quantized and repacked on the GPU, against
+    the oracle's group-64 linear, every output."""
+    N, K = NK
+    W = inputs.dense_weight(N, K, layer=40 + M + N)
+    Q, S, Z = O.quantize(W, 64)
+    q, s_, z = fl.fl_int4g_quantize(to_dev(W), group=64)
+    w = fl.fl_int4g_repack(q, s_, z, N, K, group=64)
+    xb = inputs.activations(M, K, stream=40 + M)
+    y = fl.fl_int4g_linear(bf16_dev(xb), w, N, group=64)
+    xf = O.bf16_value(xb)
+    ref, tol = O.linear(xf, Q, S, Z, 64), O.linear_tolerance(xf, Q, S, Z, 64)
+    got = y.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= tol), f"worst err/tol {np.max(np.abs(got - ref) / tol):.3f}"
+    # the groups of 64 matter: the same codes read as groups of 128 (the even
+    # groups' scales only) give a different result
+    y128 = fl.fl_int4g_linear(bf16_dev(xb), w, N)
+    assert not torch.equal(y.view(torch.int16), y128.view(torch.int16))
+
+
+def test_linear_group64_llama_sampled():
+    """K=4096, N=11008 at M in {1, 8, 32, 512}: 64 sampled columns."""
+    K, N = 4096, 11008
+    W = inputs.dense_weight(N, K, layer=64064)
+    q, s_, z = fl.fl_int4g_quantize(to_dev(W), group=64)
+    w = fl.fl_int4g_repack(q, s_, z, N, K, group=64)
+    cols = np.unique(np.concatenate([np.sort(inputs.rng(9, K, N).choice(N, 64, replace=False)), [0, N - 1]]))
+    Qc, Sc, Zc = O.quantize(W[cols], 64)
+    for M in (1, 8, 32, 512):
+        xb = inputs.activations(M, K, stream=M + 64)
+        y = fl.fl_int4g_linear(bf16_dev(xb), w, N, group=64)
+        xf = O.bf16_value(xb)
+        ref, tol = O.linear(xf, Qc, Sc, Zc, 64), O.linear_tolerance(xf, Qc, Sc, Zc, 64)
+        got = y.float().cpu().numpy().astype(np.float64)[:, cols]
+        assert np.all(np.abs(got - ref) <= tol), (M, np.max(np.abs(got - ref) / tol))
+
+
 @pytest.mark.parametrize("M", [1, 8, 9, 32, 64, 300])
 def test_linear_group256_parity(M):
     """Decode (rows and tcgen05 kernels) and prefill on group-256 weights,

@@ -313,6 +313,32 @@ def test_moe_group256_experts(M):
     check_y(y, ref, tol)
 
 
+@pytest.mark.parametrize("M", [5, 64])
+def test_moe_group64_experts(M):
+    """Experts quantized in groups of 64 (FastLLM page, section 5.4): each
+    expert matrix carries its side array; the rows kernels (M=5) and the
+    grouped GEMM (M=64) read each 64-column group's scale and zero point.
+    With a shared expert."""
+    E, H, I, k = 4, 512, 256, 2
+    w13 = [O.quantize(inputs.expert_weight(2 * I, H, 92, e, 0), 64) for e in range(E + 1)]
+    w2 = [O.quantize(inputs.expert_weight(H, I, 92, e, 1), 64) for e in range(E + 1)]
+    rp = lambda t, n, kk: fl.fl_int4g_repack(to_dev(t[0]), to_dev(t[1].view(np.int16)), to_dev(t[2]), n, kk, group=64)
+    w13_d = torch.cat([rp(t, 2 * I, H) for t in w13[:E]])
+    w2_d = torch.cat([rp(t, H, I) for t in w2[:E]])
+    xb = inputs.activations(M, H, stream=92)
+    logits = inputs.router_logits(M, E, stream=92)
+    ids = torch.empty((M, k), dtype=torch.int32, device=DEV)
+    ws = torch.zeros(fl.fl_moe_int4g_workspace(M, E, k, H, I, True), dtype=torch.uint8, device=DEV)
+    y = fl.fl_moe_int4g(bf16_dev(xb), to_dev(logits), k, I, w13_d, w2_d, scoring=fl.FL_SIGMOID,
+                        shared_w13=rp(w13[E], 2 * I, H), shared_w2=rp(w2[E], H, I), topk_ids=ids, ws=ws, group=64)
+    torch.cuda.synchronize()
+    assert fl.fl_int4g_status(ws) == 0
+    ref, tol, rid, rw = O.moe(O.bf16_value(xb), logits, k, w13[:E], w2[:E], O.SIGMOID, True, w13[E], w2[E],
+                              group=64)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    check_y(y, ref, tol)
+
+
 def _routing_case(M, E, k, H, I, layer):
     w13, w2 = host_experts(E, H, I, layer)
     w13_d, w2_d = stack_dev(w13, 2 * I, H), stack_dev(w2, H, I)
