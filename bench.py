@@ -36,12 +36,12 @@ BYTES_PER_WEIGHT = 0.51953125          # 0.5 B code + 2 B scale / 128 + 0.5 B ze
 LLAMA = [("qkv", 4096, 12288), ("gate", 4096, 11008), ("up", 4096, 11008), ("down", 11008, 4096)]
 DECODE_M = [1, 8, 32]
 # DRAM traffic / algorithmic bytes of k_linear_rows, from one ncu capture of
-# the M=1 fused-QKV launch (summary kept under profiles/): 26,212,864 B
+# the M=1 fused-QKV launch (summary kept under profiles/): 26,213,376 B
 # read, 0 written, for 26,181,632 algorithmic bytes.  Traffic grows in
 # proportion to the super-blocks a launch streams, so the per-launch traffic
 # is scaled from it.  Reset to None whenever the kernel changes after that
 # capture.
-TRAFFIC_RATIO = 26212864 / 26181632
+TRAFFIC_RATIO = 26213376 / 26181632
 WORKLOAD = "llama7b-decode-linears int4g g128: (K,N) in {(4096,12288),(4096,11008)x2,(11008,4096)} x M in {1,8,32}"
 
 
@@ -156,12 +156,12 @@ def _median_time(torch, fn, flush, reps, stream):
     return statistics.median(ts)
 
 
-def run_moe_section(torch, np, fl, inputs, dev, pk, reps):
+def run_moe_section(torch, np, fl, inputs, dev, pk, reps, cfgs=(QWEN, DSV3)):
     """MoE layer tokens/s for the Qwen3- and DeepSeek-V3-shaped configs."""
     out = {}
     stream = torch.cuda.current_stream()
     flushbuf = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
-    for cfg in (QWEN, DSV3):
+    for cfg in cfgs:
         E, H, I, k = cfg["E"], cfg["H"], cfg["I"], cfg["k"]
 
         def packed(e, which, layer=1000):
@@ -295,7 +295,8 @@ def _mlp_copies(torch, fl, inputs, dev, H, I, copies, layer0):
 
 def run_mlp_section(torch, np, fl, inputs, dev, pk, Ms=(1, 8)):
     """Llama-7B MLP block (H=4096, I=11008: gate, up, down; 70.3 MB of int4g
-    weights) at M in {1, 8}: the fused block (fl_int4g_mlp, one launch) and,
+    weights) at M in {1, 8}: fl_int4g_mlp (gate/up + SwiGLU launch, then the
+    down launch), the one-launch cooperative form (fl_int4g_mlp_fused) and,
     for comparison, the same three matrices as three fl_int4g_linear calls
     (SwiGLU not applied there).  4 weight copies (281 MB) in one CUDA graph,
     replayed 30 times."""
@@ -310,6 +311,9 @@ def run_mlp_section(torch, np, fl, inputs, dev, pk, Ms=(1, 8)):
         ws = torch.zeros(fl.fl_int4g_mlp_workspace(M, H, I), dtype=torch.uint8, device=dev)
         ms = _graph_time_per_launch(torch, [lambda c=c: fl.fl_int4g_mlp(x, c[0], c[1], c[2], I, y=y, ws=ws)
                                             for c in copies], stream, 30)
+        ms1 = _graph_time_per_launch(torch, [lambda c=c: fl.fl_int4g_mlp(x, c[0], c[1], c[2], I, y=y, ws=ws,
+                                                                         one_launch=True)
+                                             for c in copies], stream, 30)
         assert fl.fl_int4g_status(ws) == 0
         hx = torch.from_numpy(inputs.activations(M, I, stream=M).view(np.int16)).to(dev).view(torch.bfloat16)
         gu = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
@@ -323,6 +327,7 @@ def run_mlp_section(torch, np, fl, inputs, dev, pk, Ms=(1, 8)):
         ms3 = _graph_time_per_launch(torch, launches, stream, 30) * 3
         out[str(M)] = {"us_per_block": round(ms * 1e3, 3), "weight_GBps": round(wb / (ms * 1e-3) / 1e9, 1),
                        "hbm_frac_of_measured": round(wb / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                       "one_launch_us": round(ms1 * 1e3, 3), "one_launch_GBps": round(wb / (ms1 * 1e-3) / 1e9, 1),
                        "three_linear_calls_us": round(ms3 * 1e3, 3),
                        "three_linear_calls_GBps": round(wb / (ms3 * 1e-3) / 1e9, 1)}
     del copies
@@ -717,6 +722,11 @@ def run_case(args):
         print(json.dumps({"case": f"mlp M={args.M}", **run_mlp_section(torch, np, fl, inputs, dev, peaks(),
                                                                         Ms=(args.M,))}))
         return
+    if args.case == "moe":
+        cfg = dict(QWEN if args.model == "qwen3" else DSV3, Ms=(args.M,))
+        print(json.dumps({"case": f"moe {cfg['name']} M={args.M}",
+                          **run_moe_section(torch, np, fl, inputs, dev, peaks(), reps=args.iters, cfgs=(cfg,))}))
+        return
     M, K, N = args.M, args.K, args.N
     nb = BYTES_PER_WEIGHT * N * K
     copies = max(1, min(64, int(np.ceil(300e6 / nb))))
@@ -761,7 +771,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sections", action="store_true", help="skip the MoE and prefill GEMM sections")
-    ap.add_argument("--case", choices=["linear", "mlp"], help="time one shape on its own (profiling)")
+    ap.add_argument("--case", choices=["linear", "mlp", "moe"], help="time one shape on its own (profiling)")
+    ap.add_argument("--model", choices=["qwen3", "deepseek"], default="qwen3", help="--case moe: the layer shape")
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--K", type=int, default=4096)
     ap.add_argument("--N", type=int, default=12288)

@@ -208,7 +208,7 @@ int fl_int4g_linear_noalloc_status(fl_stream_t stream, int* out);
 /* Workspace bytes needed by fl_int4g_mlp. */
 int fl_int4g_mlp_workspace(int M, int H, int I, size_t* out);
 
-/* Decode MLP block in one launch, for 1 <= M <= 8 tokens:
+/* Decode MLP block, for 1 <= M <= 8 tokens:
  *   h = silu(G x) * (U x)  (h stored as bf16),   y = D h,
  * every product an int4g linear as in fl_int4g_linear (FastLLM page,
  * section 3.1; fastllm README, section 2: --dtype int4g applies to every
@@ -216,14 +216,25 @@ int fl_int4g_mlp_workspace(int M, int H, int I, size_t* out);
  *   x       bf16 [M, H] device          y  bf16 [M, H] device
  *   w_gate  interleaved layout of G [I, H]     w_up  of U [I, H]
  *   w_down  interleaved layout of D [H, I]     ws    workspace (conventions)
- * H % 128 == 0, I % 128 == 0.  One cooperative grid (two CTAs per SM) runs
- * gate/up with SwiGLU, hands h over through a grid-wide counter (a bounded
- * wait: FL_ERR_TIMEOUT in the status block if it runs out) and runs the
- * down projection, so the weight stream does not stop between the two.
- * Reduction order is fixed: results are deterministic.  FL_ERR_UNSUPPORTED
- * for M > 8 or when two CTAs per SM do not fit. */
+ * H % 128 == 0, I % 128 == 0.  Two launches chained by programmatic launch:
+ * the gate and up super-blocks stream through one decode kernel whose
+ * thread-block clusters reduce each row tile and store h = silu(gate) * up,
+ * then the down projection; shapes whose row tiles do not take that
+ * cluster split run fl_int4g_mlp_fused.  Reduction order is fixed: results
+ * are deterministic (both forms give the same h rounding, not the same
+ * bits).  FL_ERR_UNSUPPORTED for M > 8. */
 int fl_int4g_mlp(const void* x, int M, int H, int I, const void* w_gate, const void* w_up,
                  const void* w_down, void* y, void* ws, size_t ws_bytes, fl_stream_t stream);
+
+/* The same block in ONE launch: a cooperative grid (two CTAs per SM) runs
+ * gate/up with SwiGLU (split over K across the CTAs, ticketed partial sums),
+ * hands h over through a grid-wide counter (a bounded wait: FL_ERR_TIMEOUT
+ * in the status block if it runs out) and runs the down projection, while
+ * the down weights already stream into the CTAs' rings.  Workspace as for
+ * fl_int4g_mlp.  FL_ERR_UNSUPPORTED for M > 8 or when two CTAs per SM do not
+ * fit. */
+int fl_int4g_mlp_fused(const void* x, int M, int H, int I, const void* w_gate, const void* w_up,
+                       const void* w_down, void* y, void* ws, size_t ws_bytes, fl_stream_t stream);
 
 /* Test hook of the device-side failure path (no counterpart on the pages:
  * the library never traps or faults; a wait that runs out is reported).

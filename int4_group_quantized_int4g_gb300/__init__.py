@@ -22,7 +22,7 @@ __all__ = [
     "fl_int4g_test_withhold_cluster_arrival",
     "fl_moe_int4g_workspace", "fl_moe_int4g", "fl_moe_int4g_ptrs", "FlMoeRouting", "fl_int4g_mlp_workspace",
     "fl_moe_router_logits_workspace", "fl_moe_router_logits",
-    "fl_int4g_mlp",
+    "fl_int4g_mlp", "fl_int4g_mlp_fused",
 ]
 
 GROUP = 128
@@ -62,6 +62,7 @@ SIGNATURES = {
     "fl_moe_router_logits_workspace": (_i, [_i, _i, _i, _c_size_p]),
     "fl_moe_router_logits": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, ctypes.c_size_t, _vp]),
     "fl_int4g_mlp": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "fl_int4g_mlp_fused": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "fl_moe_int4g": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
                           _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
     "fl_moe_int4g_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _i, ctypes.POINTER(FlMoeRouting), _vp, _vp, _vp, _vp,
@@ -253,9 +254,10 @@ def fl_int4g_mlp_workspace(M, H, I):
     return out.value
 
 
-def fl_int4g_mlp(x, w_gate, w_up, w_down, I, y=None, ws=None):
-    """Fused decode MLP block (M <= 8): y = D . (silu(G x) * (U x)), the
-    three matrices in the interleaved layout (G, U: [I, H]; D: [H, I])."""
+def fl_int4g_mlp(x, w_gate, w_up, w_down, I, y=None, ws=None, one_launch=False):
+    """Decode MLP block (M <= 8): y = D . (silu(G x) * (U x)), the three
+    matrices in the interleaved layout (G, U: [I, H]; D: [H, I]).
+    one_launch: the cooperative single-launch form (fl_int4g_mlp_fused)."""
     torch = _torch()
     M, H = x.shape
     if y is None:
@@ -263,8 +265,9 @@ def fl_int4g_mlp(x, w_gate, w_up, w_down, I, y=None, ws=None):
     nb = fl_int4g_mlp_workspace(M, H, I)
     if ws is None:
         ws = _workspace(nb, x.device)
-    _check("fl_int4g_mlp", lib().fl_int4g_mlp(_p(x), M, H, I, _p(w_gate), _p(w_up), _p(w_down), _p(y), _p(ws),
-                                              ws.numel(), _stream()))
+    name = "fl_int4g_mlp_fused" if one_launch else "fl_int4g_mlp"
+    _check(name, getattr(lib(), name)(_p(x), M, H, I, _p(w_gate), _p(w_up), _p(w_down), _p(y), _p(ws),
+                                      ws.numel(), _stream()))
     return y
 
 

@@ -57,6 +57,7 @@ struct RowsParams {
   uint32_t zrow_off; // shared-memory offset of 256 zero bytes (x rows of absent tokens)
   unsigned long long red_wait_ns;  // bound of rank 0's wait for its peers' partial sums
   int withhold;      // test hook: the reduction barrier expects one arrival nobody makes
+  const uint8_t* w_up;   // GLU: the up matrix (w is the gate); y receives h = silu(gate) * up
 };
 
 // CTA c owns units [unit_begin(c), unit_begin(c+1)); cta_of_unit inverts it.
@@ -210,6 +211,86 @@ __device__ __forceinline__ void cluster_reduce(const RowsParams& p, int T, int r
 // a cluster sharing a row tile (its range lies inside that tile, group slot
 // = unit index in the range, no tile boundaries); otherwise a stream-K range
 // that may cross row tiles, finished through the ticket hand-off.
+// GLU (the gate/up half of a decode MLP block, M <= 8, cluster mode): each
+// stage holds the gate and the up super-block of one (row tile, group) and
+// that group's x rows; two folded sums per row; rank 0 of the cluster adds
+// the ranks' gate and up sums in rank order and stores h = silu(gate) * up.
+__device__ __forceinline__ void glu_reduce(const RowsParams& p, int T, int rank, int warp, int lane,
+                                           const float (&tg)[4], const float (&tu)[4], uint64_t* red_bar,
+                                           float* red_buf) {
+  constexpr int V = 8;
+  if (rank > 0) {
+    float* dst = cluster_map_rank0(red_buf) + ((static_cast<size_t>(rank - 1) * kConsumerWarps + warp) * 32 + lane) * V;
+    *reinterpret_cast<float4*>(dst) = make_float4(tg[0], tg[1], tg[2], tg[3]);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(tu[0], tu[1], tu[2], tu[3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_remote_rank0(red_bar);
+    return;
+  }
+  if (!mbar_wait_cluster(red_bar, 0, p.red_wait_ns)) {
+    if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 6);
+    if (p.withhold && warp == 0 && lane == 0) mbar_arrive(red_bar);
+    mbar_wait_cluster(red_bar, 0);
+    return;
+  }
+  float g[4], u[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) g[e] = tg[e], u[e] = tu[e];
+  for (int rr = 1; rr < p.csize; ++rr) {
+    const float* src = red_buf + ((static_cast<size_t>(rr - 1) * kConsumerWarps + warp) * 32 + lane) * V;
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    const float4 b = *reinterpret_cast<const float4*>(src + 4);
+    g[0] += a.x, g[1] += a.y, g[2] += a.z, g[3] += a.w;
+    u[0] += b.x, u[1] += b.y, u[2] += b.z, u[3] += b.w;
+  }
+  const int gid = lane >> 2, tig = lane & 3;
+  const int rbase = T * kRowTile + warp * 16;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int n = rbase + gid + (e >> 1) * 8;
+    const int m = 2 * tig + (e & 1);
+    if (n < p.N && m < p.M) p.y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(g[e] / (1.f + expf(-g[e])) * u[e]);
+  }
+}
+
+__device__ __forceinline__ void rows_consume_glu(const RowsParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                                 const float* xsum, int u0, int nstage, int rank, int warp, int lane,
+                                                 uint64_t* red_bar, float* red_buf) {
+  constexpr int Mp = 8;
+  const uint32_t xoff = 2 * kSbBytes;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int r0 = warp * 16 + gid;
+  const uint8_t* xzero = smem + p.zrow_off;
+  float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
+  int s = 0;
+  uint32_t ph = 0;
+  for (int k = 0; k < nstage; ++k) {
+    if (!mbar_wait(&full[s], ph)) {
+      if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 2);
+      if (rank == 0) mbar_wait_cluster(red_bar, 0);
+      return;
+    }
+    const uint8_t* sb = smem + static_cast<size_t>(s) * p.stage_bytes;
+    float ag[1][4], au[1][4];
+    float sg0, sg1, su0, su1;
+    uint32_t zg0, zg1, zu0, zu1;
+    unit_dot<1, true, true>(sb, sb + xoff, p.M, r0, gid, tig, ag, sg0, sg1, zg0, zg1, 1, xzero);
+    unit_dot<1, true, true>(sb + kSbBytes, sb + xoff, p.M, r0, gid, tig, au, su0, su1, zu0, zu1, 1, xzero);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    const float2 xs = *reinterpret_cast<const float2*>(xsum + k * Mp + 2 * tig);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float xv = (e & 1) ? xs.y : xs.x;
+      const uint32_t zg = (e >> 1) ? zg1 : zg0, zu = (e >> 1) ? zu1 : zu0;
+      tg[e] = fmaf((e >> 1) ? sg1 : sg0, fmaf(-__uint_as_float(0x43000000u + (zg << 16)), xv, ag[0][e]), tg[e]);
+      tu[e] = fmaf((e >> 1) ? su1 : su0, fmaf(-__uint_as_float(0x43000000u + (zu << 16)), xv, au[0][e]), tu[e]);
+    }
+    if (++s == p.stages) s = 0, ph ^= 1u;
+  }
+  glu_reduce(p, u0 / p.G, rank, warp, lane, tg, tu, red_bar, red_buf);
+}
+
 template <int NT, int UPS, bool CL, bool G64>
 __device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                              const float* xsum, int u0, int u1, int g0, int nslot, int nstage,
@@ -316,8 +397,9 @@ __device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem,
 // 2 (M <= 8, ~100 KB of stages each), 3 (M <= 8 when the row tiles' clusters
 // would fill the GPU's cluster capacity at 2: smaller stages, fewer
 // registers, so that every cluster is resident in one wave) or 1 (M > 8).
-template <int NT, int UPS, int MINB, bool G64>
+template <int NT, int UPS, int MINB, bool G64, bool GLU = false>
 __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams p) {
+  static_assert(!GLU || (NT == 1 && UPS == 2 && !G64), "GLU: one token tile, the gate and up super-blocks per stage");
   constexpr bool FOLD = NT <= 2;
   constexpr int Mp = 8 * NT;
   constexpr int XS = G64 ? 2 : 1;
@@ -340,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
   }
   uint64_t* red_bar = reinterpret_cast<uint64_t*>(smem + p.red_off);
   float* red_buf = reinterpret_cast<float*>(smem + p.red_off + 16);   // [csize-1][warp][lane][4*NT]
-  const int nstage = (u1 - u0 + UPS - 1) / UPS;   // stages this CTA fills, in order
+  const int nstage = GLU ? u1 - u0 : (u1 - u0 + UPS - 1) / UPS;   // stages this CTA fills, in order
   const uint32_t xoff = UPS * kSbBytes;           // x slices follow the super-blocks
   const int g0 = u0 % p.G;
   const int nslot = (u1 - u0) < p.G ? (u1 - u0) : p.G;   // distinct groups, from g0 on (mod G)
@@ -364,6 +446,16 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
     // ---------------- producer warp
     const uint64_t pol = policy_evict_first();
     auto issue_w = [&](int k, int slot) {   // weights of stage k (contiguous super-blocks, and side entries)
+      if (GLU) {   // the gate and the up super-block of unit u0 + k
+        if (lane == 0) {
+          uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
+          const size_t off = static_cast<size_t>(u0 + k) * kSbBytes;
+          mbar_arrive_expect_tx(&full[slot], 2u * kSbBytes + p.M * 256u);
+          bulk_g2s_hint(st, p.w + off, kSbBytes, &full[slot], pol);
+          bulk_g2s_hint(st + kSbBytes, p.w_up + off, kSbBytes, &full[slot], pol);
+        }
+        return;
+      }
       const int ua = u0 + k * UPS, n = min(UPS, u1 - ua);
       if (lane == 0) {
         uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
@@ -376,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
       }
     };
     auto issue_x = [&](int k, int slot) {   // the M token rows' slices of stage k's groups
-      const int ua = u0 + k * UPS, n = min(UPS, u1 - ua);
+      const int ua = GLU ? u0 + k : u0 + k * UPS, n = GLU ? 1 : min(UPS, u1 - ua);
       uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes + xoff;
       for (int idx = lane; idx < n * p.M; idx += 32) {
         const int i = idx / p.M, m = idx - i * p.M;
@@ -462,6 +554,10 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
     }
     named_bar(1, kConsumerWarps * 32);
   }
+  if constexpr (GLU) {
+    rows_consume_glu(p, smem, full, empty, xsum, u0, nstage, rank, warp, lane, red_bar, red_buf);
+    return;
+  }
   if (p.csize > 1)
     rows_consume<NT, UPS, true, G64>(p, smem, full, empty, xsum, u0, u1, g0, nslot, nstage, c, rank, warp, lane,
                                      red_bar, red_buf);
@@ -481,7 +577,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // minb: CTAs per SM the kernel is built for (0 = the default for M); g64:
 // groups of 64 (side entries in the stages, two token sums per group).
-bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bool g64 = false) {
+bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bool g64 = false, bool glu = false) {
   if (M < 1 || M > kMaxTokens || N < 1 || K < kGroup || K % kGroup || sms < 1) return false;
   if ((N + kRowTile - 1) / kRowTile > kMaxRowTiles) return false;
   pl->T = (N + kRowTile - 1) / kRowTile;
@@ -509,10 +605,15 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bo
     pl->P = pl->T * pl->csize;
   else
     pl->P = static_cast<int>(U < slots ? U : slots);
+  if (glu && (pl->NT != 1 || pl->csize < 2 || g64)) return false;   // GLU: cluster mode, M <= 8
   const size_t red_bytes =
-      pl->csize > 1 ? 16 + static_cast<size_t>(pl->csize - 1) * kConsumerWarps * 32 * 4 * pl->NT * sizeof(float) : 0;
+      pl->csize > 1
+          ? 16 + static_cast<size_t>(pl->csize - 1) * kConsumerWarps * 32 * 4 * pl->NT * (glu ? 2 : 1) * sizeof(float)
+          : 0;
   pl->stage_bytes = static_cast<uint32_t>(align_up(
-      static_cast<size_t>(pl->ups) * (kSbBytes + static_cast<size_t>(M) * kXRowStride + (g64 ? kSbSide : 0)), 128));
+      glu ? 2 * static_cast<size_t>(kSbBytes) + static_cast<size_t>(M) * kXRowStride
+          : static_cast<size_t>(pl->ups) * (kSbBytes + static_cast<size_t>(M) * kXRowStride + (g64 ? kSbSide : 0)),
+      128));
   const size_t budget = (pl->minb == 3 ? 66u * 1024u : pl->minb == 2 ? 100u * 1024u : 200u * 1024u) - red_bytes;
   int stages = static_cast<int>(budget / pl->stage_bytes);
   pl->stages = stages > 12 ? 12 : (stages < 2 ? 2 : stages);
@@ -530,12 +631,12 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bo
   return true;
 }
 
-template <int NT, int UPS, int MINB, bool G64>
+template <int NT, int UPS, int MINB, bool G64, bool GLU = false>
 bool rows_attr(int dev) {
   static bool attr_done[64] = {false};
   if (dev < 0 || dev >= 64) return false;
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(k_linear_rows<NT, UPS, MINB, G64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_linear_rows<NT, UPS, MINB, G64, GLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              227 * 1024) != cudaSuccess)
       return false;
     attr_done[dev] = true;
@@ -577,11 +678,11 @@ int rows_cluster_capacity(const RowsPlan& pl) {
   return cap;
 }
 
-template <int NT, int UPS, int MINB, bool G64>
+template <int NT, int UPS, int MINB, bool G64, bool GLU = false>
 int launch_rows(const RowsPlan& pl, const RowsParams& prm, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (!rows_attr<NT, UPS, MINB, G64>(dev)) return FL_ERR_CUDA;
+  if (!rows_attr<NT, UPS, MINB, G64, GLU>(dev)) return FL_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.P);
   cfg.blockDim = dim3(kThreads);
@@ -596,7 +697,7 @@ int launch_rows(const RowsPlan& pl, const RowsParams& prm, cudaStream_t s) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pl.csize > 1 ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, k_linear_rows<NT, UPS, MINB, G64>, prm) != cudaSuccess) return FL_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, k_linear_rows<NT, UPS, MINB, G64, GLU>, prm) != cudaSuccess) return FL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
 
@@ -638,6 +739,7 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   RowsParams prm;
   prm.w = static_cast<const uint8_t*>(w);
   prm.side = g64 ? static_cast<const uint8_t*>(w) + static_cast<size_t>(pl.U) * kSbBytes : nullptr;
+  prm.w_up = nullptr;
   prm.x = static_cast<const __nv_bfloat16*>(x);
   prm.y = static_cast<__nv_bfloat16*>(y);
   prm.status = static_cast<int32_t*>(ws);
@@ -674,6 +776,44 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
     case 3: return launch_rows<3, 1, 1, false>(pl, prm, stream);
     default: return launch_rows<4, 1, 1, false>(pl, prm, stream);
   }
+}
+
+// Gate/up half of a decode MLP block (M <= 8): h[m, i] = silu(G x)[m, i] *
+// (U x)[m, i] as bf16, G and U interleaved [I, H].  Returns FL_ERR_UNSUPPORTED
+// when the shape does not take the cluster split (the caller then uses
+// another path).  ws: the linear workspace of (M, I, H).
+int fl_linear_glu(const void* x, int M, int H, const void* w_gate, const void* w_up, int I, void* h, void* ws,
+                  size_t ws_bytes, cudaStream_t stream) {
+  RowsPlan pl;
+  if (!make_rows_plan(M, I, H, flh::sm_count(), &pl, 0, false, true)) return FL_ERR_UNSUPPORTED;
+  if (ws_bytes < pl.ws_bytes) return FL_ERR_WORKSPACE;
+  const int cap = rows_cluster_capacity(pl);
+  if (cap > 0 && pl.T > cap - 2) return FL_ERR_UNSUPPORTED;   // a second wave of clusters: not worth it
+  RowsParams prm;
+  prm.w = static_cast<const uint8_t*>(w_gate);
+  prm.w_up = static_cast<const uint8_t*>(w_up);
+  prm.side = nullptr;
+  prm.x = static_cast<const __nv_bfloat16*>(x);
+  prm.y = static_cast<__nv_bfloat16*>(h);
+  prm.status = static_cast<int32_t*>(ws);
+  prm.cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + pl.cnt_off);
+  prm.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.part_off);
+  prm.U = pl.U;
+  prm.M = M;
+  prm.K = H;
+  prm.N = I;
+  prm.T = pl.T;
+  prm.G = pl.G;
+  prm.P = pl.P;
+  prm.stages = pl.stages;
+  prm.stage_bytes = pl.stage_bytes;
+  prm.csize = pl.csize;
+  prm.red_off = pl.red_off;
+  prm.zrow_off = pl.zrow_off;
+  const long long hook = g_withhold_ns.load();
+  prm.withhold = hook >= 0 ? 1 : 0;
+  prm.red_wait_ns = prm.withhold ? static_cast<unsigned long long>(hook) : kWaitLimitNs;
+  return launch_rows<1, 2, 2, false, true>(pl, prm, stream);
 }
 
 static bool linear_args_ok(const void* x, int M, int K, const void* w, int N, const void* y, const void* ws) {

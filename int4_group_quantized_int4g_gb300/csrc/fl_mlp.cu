@@ -27,6 +27,7 @@
 // fp16 scale applied to each fp32 group sum).  The grid counter is reset by
 // the last CTA to exit, the tickets by each tile's finisher, so a successful
 // call leaves the workspace's counters zero.
+#include <algorithm>
 #include <mutex>
 
 #include "fl_common.cuh"
@@ -611,15 +612,59 @@ bool make_mlp_plan(int M, int H, int I, int ctas, MlpPlan* pl) {
 
 }  // namespace
 
+int fl_linear_rows_workspace(int M, int N, int K, size_t* out);
+int fl_linear_decode_workspace(int M, int N, int K, size_t* out);
+int fl_linear_decode(const void* x, int M, int K, const void* w, int N, void* y, void* ws, size_t ws_bytes,
+                     cudaStream_t s);
+int fl_linear_glu(const void* x, int M, int H, const void* w_gate, const void* w_up, int I, void* h, void* ws,
+                  size_t ws_bytes, cudaStream_t stream);
+
+// Two-launch form: its workspace is the two decode linears' (shared, used in
+// turn) and h after it.
+static bool two_launch_layout(int M, int H, int I, size_t* h_off, size_t* total) {
+  size_t a = 0, b = 0;
+  if (fl_linear_rows_workspace(M, I, H, &a) != FL_OK || fl_linear_decode_workspace(M, H, I, &b) != FL_OK)
+    return false;
+  *h_off = (std::max(a, b) + 255) / 256 * 256;
+  *total = *h_off + 2ull * M * I;
+  return true;
+}
+
 extern "C" int fl_int4g_mlp_workspace(int M, int H, int I, size_t* out) {
   MlpPlan pl;
-  if (!out || !make_mlp_plan(M, H, I, 2 * flh::sm_count(), &pl)) return FL_ERR_ARG;
-  *out = pl.total;
+  size_t h_off = 0, two = 0;
+  if (!out || !make_mlp_plan(M, H, I, 2 * flh::sm_count(), &pl) || !two_launch_layout(M, H, I, &h_off, &two))
+    return FL_ERR_ARG;
+  *out = std::max(pl.total, two);
   return FL_OK;
 }
 
+extern "C" int fl_int4g_mlp_fused(const void* x, int M, int H, int I, const void* w_gate, const void* w_up,
+                                  const void* w_down, void* y, void* ws, size_t ws_bytes, fl_stream_t stream);
+
 extern "C" int fl_int4g_mlp(const void* x, int M, int H, int I, const void* w_gate, const void* w_up,
                             const void* w_down, void* y, void* ws, size_t ws_bytes, fl_stream_t stream) {
+  if (!x || !w_gate || !w_up || !w_down || !y || !ws) return FL_ERR_ARG;
+  if (!flh::aligned16(x) || !flh::aligned16(w_gate) || !flh::aligned16(w_up) || !flh::aligned16(w_down) ||
+      !flh::aligned16(y) || !flh::aligned16(ws))
+    return FL_ERR_ARG;
+  if (M > kMaxTok && M >= 1) return FL_ERR_UNSUPPORTED;
+  size_t need = 0, h_off = 0, two = 0;
+  if (fl_int4g_mlp_workspace(M, H, I, &need) != FL_OK || !two_launch_layout(M, H, I, &h_off, &two))
+    return FL_ERR_ARG;
+  if (ws_bytes < need) return FL_ERR_WORKSPACE;
+  // gate/up with SwiGLU, then down, chained by programmatic launch; shapes
+  // without the cluster split take the one-launch kernel
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* h = static_cast<uint8_t*>(ws) + h_off;
+  const int rc = fl_linear_glu(x, M, H, w_gate, w_up, I, h, ws, h_off, s);
+  if (rc == FL_ERR_UNSUPPORTED) return fl_int4g_mlp_fused(x, M, H, I, w_gate, w_up, w_down, y, ws, ws_bytes, stream);
+  if (rc != FL_OK) return rc;
+  return fl_linear_decode(h, M, I, w_down, H, y, ws, h_off, s);
+}
+
+extern "C" int fl_int4g_mlp_fused(const void* x, int M, int H, int I, const void* w_gate, const void* w_up,
+                                  const void* w_down, void* y, void* ws, size_t ws_bytes, fl_stream_t stream) {
   if (!x || !w_gate || !w_up || !w_down || !y || !ws) return FL_ERR_ARG;
   if (!flh::aligned16(x) || !flh::aligned16(w_gate) || !flh::aligned16(w_up) || !flh::aligned16(w_down) ||
       !flh::aligned16(y) || !flh::aligned16(ws))

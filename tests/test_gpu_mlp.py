@@ -57,23 +57,25 @@ def check(y, ref, tol):
     assert rel <= 1e-2, f"relative RMS error {rel:.3e}"
 
 
+@pytest.mark.parametrize("one_launch", [False, True])
 @pytest.mark.parametrize("M", [1, 3, 8])
-@pytest.mark.parametrize("HI", [(256, 256), (384, 640), (1024, 384), (128, 128)])
-def test_mlp_small_every_output(M, HI):
+@pytest.mark.parametrize("HI", [(256, 256), (384, 640), (1024, 384), (128, 128), (4096, 1408)])
+def test_mlp_small_every_output(M, HI, one_launch):
     H, I = HI
     G, U, D, (g, u, d) = mlp_case(H, I, layer=1200 + H + I)
     xb = inputs.activations(M, H, stream=1200 + M)
     ws = torch.zeros(fl.fl_int4g_mlp_workspace(M, H, I), dtype=torch.uint8, device=DEV)
     x = to_dev(xb.view(np.int16)).view(torch.bfloat16)
-    y = fl.fl_int4g_mlp(x, g, u, d, I, ws=ws)
+    y = fl.fl_int4g_mlp(x, g, u, d, I, ws=ws, one_launch=one_launch)
     torch.cuda.synchronize()
     assert fl.fl_int4g_status(ws) == 0
     ref, tol = oracle_mlp(xb, G, U, D)
     check(y, ref, tol)
 
 
+@pytest.mark.parametrize("one_launch", [False, True])
 @pytest.mark.parametrize("M", [1, 8])
-def test_mlp_llama_full(M):
+def test_mlp_llama_full(M, one_launch):
     """Llama-7B MLP block (H=4096, I=11008) at M in {1, 8}, every output;
     two calls on one workspace give the same bits (the counters are left
     zero, the reduction order is fixed)."""
@@ -82,8 +84,8 @@ def test_mlp_llama_full(M):
     xb = inputs.activations(M, H, stream=1300 + M)
     x = to_dev(xb.view(np.int16)).view(torch.bfloat16)
     ws = torch.zeros(fl.fl_int4g_mlp_workspace(M, H, I), dtype=torch.uint8, device=DEV)
-    y1 = fl.fl_int4g_mlp(x, g, u, d, I, ws=ws).clone()
-    y2 = fl.fl_int4g_mlp(x, g, u, d, I, ws=ws).clone()
+    y1 = fl.fl_int4g_mlp(x, g, u, d, I, ws=ws, one_launch=one_launch).clone()
+    y2 = fl.fl_int4g_mlp(x, g, u, d, I, ws=ws, one_launch=one_launch).clone()
     torch.cuda.synchronize()
     assert fl.fl_int4g_status(ws) == 0
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
@@ -91,8 +93,10 @@ def test_mlp_llama_full(M):
     check(y1, ref, tol)
 
 
-def test_mlp_in_a_cuda_graph():
-    """The cooperative launch captured in a CUDA graph and replayed."""
+@pytest.mark.parametrize("one_launch", [False, True])
+def test_mlp_in_a_cuda_graph(one_launch):
+    """Both forms (the cooperative launch among them) captured in a CUDA
+    graph and replayed."""
     M, H, I = 2, 512, 384
     G, U, D, (g, u, d) = mlp_case(H, I, layer=1400)
     xb = inputs.activations(M, H, stream=1400)
@@ -101,11 +105,11 @@ def test_mlp_in_a_cuda_graph():
     y = torch.empty((M, H), dtype=torch.bfloat16, device=DEV)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        fl.fl_int4g_mlp(x, g, u, d, I, y=y, ws=ws)
+        fl.fl_int4g_mlp(x, g, u, d, I, y=y, ws=ws, one_launch=one_launch)
     s.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=s):
-        fl.fl_int4g_mlp(x, g, u, d, I, y=y, ws=ws)
+        fl.fl_int4g_mlp(x, g, u, d, I, y=y, ws=ws, one_launch=one_launch)
     y.zero_()
     for _ in range(3):
         graph.replay()
@@ -120,5 +124,29 @@ def test_mlp_rejects_bad_arguments():
     L = fl.lib()
     fake = ctypes.c_void_p(0x10000)
     assert L.fl_int4g_mlp(fake, 9, 256, 256, fake, fake, fake, fake, fake, 1 << 30, None) == 3   # M > 8
+    assert L.fl_int4g_mlp_fused(fake, 9, 256, 256, fake, fake, fake, fake, fake, 1 << 30, None) == 3
     assert L.fl_int4g_mlp(fake, 1, 200, 256, fake, fake, fake, fake, fake, 1 << 30, None) == 1   # H % 128
     assert L.fl_int4g_mlp(fake, 1, 256, 256, fake, fake, fake, fake, fake, 16, None) == 2        # workspace
+
+
+def test_mlp_glu_timeout_is_reported():
+    """The gate/up launch reduces row tiles across thread-block clusters: the
+    test hook makes that bounded wait run out (FL_ERR_TIMEOUT reported, no
+    hang, no fault), and the next call on the workspace is correct."""
+    M, H, I = 2, 512, 256
+    G, U, D, (g, u, d) = mlp_case(H, I, layer=1500)
+    xb = inputs.activations(M, H, stream=1500)
+    x = to_dev(xb.view(np.int16)).view(torch.bfloat16)
+    ws = torch.zeros(fl.fl_int4g_mlp_workspace(M, H, I), dtype=torch.uint8, device=DEV)
+    fl.fl_int4g_test_withhold_cluster_arrival(1_000_000)
+    try:
+        fl.fl_int4g_mlp(x, g, u, d, I, ws=ws)
+        torch.cuda.synchronize()
+    finally:
+        fl.fl_int4g_test_withhold_cluster_arrival(-1)
+    assert fl.fl_int4g_status(ws) == 5
+    y = fl.fl_int4g_mlp(x, g, u, d, I, ws=ws)
+    torch.cuda.synchronize()
+    assert fl.fl_int4g_status(ws) == 0
+    ref, tol = oracle_mlp(xb, G, U, D)
+    check(y, ref, tol)
