@@ -31,8 +31,7 @@ using namespace fl;
 
 namespace {
 
-constexpr int kSegRows = 32;          // tokens per segment (4 token tiles of 8)
-constexpr int kNT = 4;
+constexpr int kNT = 4;                // token tiles of 8 per segment (decode, M <= 8: 1)
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxE = 1024;
@@ -70,8 +69,9 @@ __global__ void k_moe_route(const float* __restrict__ logits, int M, int E, int 
     v[i] = x;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, FL_ERR_DEVICE_CHECK, t);
-  float selv[32];   // k <= 32 handled per token (checked on the host)
-  int sele[32];
+  // slot j's choice is kept by lane j (k <= 32, checked on the host)
+  float myv = -INFINITY, v0 = -INFINITY;
+  int mye = 0;
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
     int be = 0x7fffffff;
@@ -87,15 +87,16 @@ __global__ void k_moe_route(const float* __restrict__ logits, int M, int E, int 
       if (better(ov, oe, bv, be)) bv = ov, be = oe;
     }
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    selv[j] = bv;
-    sele[j] = be;
+    if (lane == j) myv = bv, mye = be;
+    if (j == 0) v0 = bv;
   }
-  // gate weights in fp32
-  float den = 0.f;
+  // gate weights in fp32; sums over the slots in slot order
+  float den = 0.f, num = 0.f;
   if (scoring == FL_SOFTMAX) {
-    const float lmax = selv[0];
+    const float lmax = v0;
+    num = expf(myv - lmax);
     if (renorm) {
-      for (int j = 0; j < k; ++j) den += expf(selv[j] - lmax);
+      for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, num, j);
     } else {
       float part = 0.f;
 #pragma unroll
@@ -106,17 +107,15 @@ __global__ void k_moe_route(const float* __restrict__ logits, int M, int E, int 
       den = part;
     }
   } else {
+    num = 1.f / (1.f + expf(-myv));
     if (renorm)
-      for (int j = 0; j < k; ++j) den += 1.f / (1.f + expf(-selv[j]));
+      for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, num, j);
     else
       den = 1.f;
   }
-  if (lane == 0) {
-    for (int j = 0; j < k; ++j) {
-      const float num = scoring == FL_SOFTMAX ? expf(selv[j] - selv[0]) : 1.f / (1.f + expf(-selv[j]));
-      ids[static_cast<size_t>(t) * k + j] = sele[j];
-      wts[static_cast<size_t>(t) * k + j] = num / den * scale;
-    }
+  if (lane < k) {
+    ids[static_cast<size_t>(t) * k + lane] = mye;
+    wts[static_cast<size_t>(t) * k + lane] = num / den * scale;
   }
 }
 
@@ -288,20 +287,34 @@ __global__ void __launch_bounds__(1024, 1) k_moe_permute(const PermuteArgs a) {
     tot[e] = s;
   }
   __syncthreads();
-  if (tid == 0) {
+  if (warp == 0) {
+    // exclusive scans of the counts (-> offsets) and of the segment counts
+    // (-> first segment of each expert): lane l takes experts [l*per, (l+1)*per)
+    const int per = (E + 31) / 32, e0 = lane * per, e1 = min(E, e0 + per);
     int run = 0, seg = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = tot[e];
-      tot[e] = run;                              // exclusive scan -> offsets
-      nch[e] = seg;                              // first segment of expert e
-      run += c;
-      seg += (c + a.seg_rows - 1) / a.seg_rows;
+    for (int e = e0; e < e1; ++e) run += tot[e], seg += (tot[e] + a.seg_rows - 1) / a.seg_rows;
+    int xr = run, xs = seg;   // inclusive warp scan, then shifted to exclusive
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yr = __shfl_up_sync(0xffffffffu, xr, o), ys = __shfl_up_sync(0xffffffffu, xs, o);
+      if (lane >= o) xr += yr, xs += ys;
     }
-    tot[E] = run;
-    nch[E] = seg;
-    const int nshared = a.has_shared ? (a.M + a.seg_rows - 1) / a.seg_rows : 0;
-    a.plan->nseg = seg + nshared;
-    a.plan->U = (seg + nshared) * a.TT13 * a.G13;   // == (seg + nshared) * TT2 * G2
+    int rbase = xr - run, sbase = xs - seg;
+    for (int e = e0; e < e1; ++e) {
+      const int c = tot[e];
+      tot[e] = rbase;
+      nch[e] = sbase;
+      rbase += c;
+      sbase += (c + a.seg_rows - 1) / a.seg_rows;
+    }
+    const int all_r = __shfl_sync(0xffffffffu, xr, 31), all_s = __shfl_sync(0xffffffffu, xs, 31);
+    if (lane == 0) {
+      tot[E] = all_r;
+      nch[E] = all_s;
+      const int nshared = a.has_shared ? (a.M + a.seg_rows - 1) / a.seg_rows : 0;
+      a.plan->nseg = all_s + nshared;
+      a.plan->U = (all_s + nshared) * a.TT13 * a.G13;   // == (all_s + nshared) * TT2 * G2
+    }
   }
   __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) {
@@ -402,7 +415,7 @@ __device__ __forceinline__ int cta_of_unit_d(int u, int U, int P) {
 }
 
 // Output of one finished (segment, tile) for the warp's 16 rows.
-template <int MODE>
+template <int MODE, int kNT>
 __device__ __forceinline__ void emit(const MoeRowsParams& p, int seg, int tile, int warp, int lane,
                                      const float (&tg)[kNT][4], const float (&tu)[kNT][4]) {
   const int gid = lane >> 2, tig = lane & 3;
@@ -424,14 +437,14 @@ __device__ __forceinline__ void emit(const MoeRowsParams& p, int seg, int tile, 
     }
 }
 
-template <int MODE>
+template <int MODE, int kNT>
 __device__ __forceinline__ float* slot_ptr(const MoeRowsParams& p, int c, bool second, int warp) {
   constexpr size_t kSlot = static_cast<size_t>(kRowTile) * (8 * kNT) * MoeIO<MODE>::kVals;
   return p.part + (static_cast<size_t>(2 * c + (second ? 1 : 0))) * kSlot +
          static_cast<size_t>(warp) * 16 * (8 * kNT) * MoeIO<MODE>::kVals;
 }
 
-template <int MODE>
+template <int MODE, int kNT>
 __device__ __forceinline__ void ticket(const MoeRowsParams& p, int U, int Pe, int gt, int warp, int lane) {
   constexpr int Mp = 8 * kNT;
   constexpr int V = MoeIO<MODE>::kVals;
@@ -455,7 +468,7 @@ __device__ __forceinline__ void ticket(const MoeRowsParams& p, int U, int Pe, in
     for (int e = 0; e < 4; ++e) tg[nt][e] = 0.f, tu[nt][e] = 0.f;
   for (int cc = cf; cc <= cl; ++cc) {   // CTA order: deterministic
     const bool second = gt != unit_begin_d(cc, U, Pe) / p.G;
-    const float* sp = slot_ptr<MODE>(p, cc, second, warp);
+    const float* sp = slot_ptr<MODE, kNT>(p, cc, second, warp);
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
@@ -471,11 +484,11 @@ __device__ __forceinline__ void ticket(const MoeRowsParams& p, int U, int Pe, in
       }
     }
   }
-  emit<MODE>(p, seg, tile, warp, lane, tg, tu);
+  emit<MODE, kNT>(p, seg, tile, warp, lane, tg, tu);
   if (lane == 0) p.cnt[gt * kConsumerWarps + warp] = 0;
 }
 
-template <int MODE>
+template <int MODE, int kNT>
 __device__ __forceinline__ bool store(const MoeRowsParams& p, int gt, int c, int u0, int u1, int warp,
                                       int lane, const float (&tg)[kNT][4], const float (&tu)[kNT][4]) {
   constexpr int Mp = 8 * kNT;
@@ -483,11 +496,11 @@ __device__ __forceinline__ bool store(const MoeRowsParams& p, int gt, int c, int
   const int tu0 = gt * p.G, tu1 = (gt + 1) * p.G;
   if (tu0 >= u0 && tu1 <= u1) {
     const int seg = gt / p.TT;
-    emit<MODE>(p, seg, gt - seg * p.TT, warp, lane, tg, tu);
+    emit<MODE, kNT>(p, seg, gt - seg * p.TT, warp, lane, tg, tu);
     return false;
   }
   const int gid = lane >> 2, tig = lane & 3;
-  float* sp = slot_ptr<MODE>(p, c, gt != u0 / p.G, warp);
+  float* sp = slot_ptr<MODE, kNT>(p, c, gt != u0 / p.G, warp);
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
@@ -502,9 +515,13 @@ __device__ __forceinline__ bool store(const MoeRowsParams& p, int gt, int c, int
   return true;
 }
 
-template <int MODE, bool G64>
-__global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p) {
+// kNT token tiles of 8 per segment: 4 (segments of up to 32 positions, one
+// CTA per SM) or 1 (M <= 8: an expert never holds more than 8 positions; two
+// CTAs per SM).
+template <int MODE, bool G64, int kNT>
+__global__ void __launch_bounds__(kThreads, kNT == 1 ? 2 : 1) k_moe_rows(const MoeRowsParams p) {
   constexpr int SB = MoeIO<MODE>::kSB;
+  constexpr int kSegRowsK = 8 * kNT;
   constexpr int XS = G64 ? 2 : 1;   // accumulator chains per super-block: one per 64-column group
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
@@ -519,8 +536,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p)
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_launch_dependents();
-  pdl_wait();   // the plan, segments and x/h come from the previous kernels
+  // kEarly (segments of 8, decode): MODE 0 (gate/up) gets its plan, segments
+  // and x from the permute, the kernel just before it, and lets the next
+  // kernel start only once that wait is over.  So MODE 1 (down) starts after
+  // the permute has completed: it reads the plan at once (plain loads: written
+  // by a kernel that completed before this one started) and requests its first
+  // weights before its own wait; only h (from MODE 0) waits for the previous
+  // kernel.  Otherwise both modes wait at the top.
+  constexpr bool kEarly = kNT == 1;
+  if (kEarly && MODE == 0) {
+    pdl_wait();
+    pdl_launch_dependents();
+  } else if (kEarly) {
+    pdl_launch_dependents();
+  } else {
+    pdl_launch_dependents();
+    pdl_wait();
+  }
   const int U = p.plan->U;
   // the work is split over min(P, U) CTAs, so that every working CTA owns at
   // least one unit (the ticket hand-off counts on it); the rest retire
@@ -533,8 +565,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p)
   if (warp == kConsumerWarps) {
     // ---------------- producer: super-block(s) + the segment's x rows
     const uint64_t pol = policy_evict_first();
+    // kEarly MODE 1: the weights of the first stages before the wait (see above)
+    const int npre = kEarly && MODE == 1 ? min(u1 - u0, p.stages) : 0;
     int s = 0, fills = 0;
     uint32_t ph = 0;
+    // weights of (row tile, group) of expert e into stage `slot`, by lane 0
+    auto issue_w = [&](int e, int tile, int g, int nt_ok, int slot) {
+      // a bad table entry (recorded) skips the weight copy: the stage then
+      // completes on its activations alone and its result is garbage
+      const uint8_t* base = e == p.E ? p.w_shared : expert_base(p.w, p.wtab, p.wbytes, e, p.status);
+      uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
+      mbar_arrive_expect_tx(&full[slot],
+                            static_cast<uint32_t>((base ? SB * (kSbBytes + (G64 ? kSbSide : 0)) : 0) + nt_ok * 256));
+      if (base) {
+        const size_t u_a = static_cast<size_t>(tile) * p.G + g, u_b = static_cast<size_t>(tile + p.up_off) * p.G + g;
+        bulk_g2s_hint(st, base + u_a * kSbBytes, kSbBytes, &full[slot], pol);
+        if (SB == 2) bulk_g2s_hint(st + kSbBytes, base + u_b * kSbBytes, kSbBytes, &full[slot], pol);
+        if (G64) {   // side entries after the x rows
+          uint8_t* sd = st + xoff + kSegRowsK * kXRowStride;
+          bulk_g2s_hint(sd, base + p.side_off + u_a * kSbSide, kSbSide, &full[slot], pol);
+          if (SB == 2) bulk_g2s_hint(sd + kSbSide, base + p.side_off + u_b * kSbSide, kSbSide, &full[slot], pol);
+        }
+      }
+    };
+    if (npre > 0) {
+      if (lane == 0)
+        for (int k = 0; k < npre; ++k) {
+          const int u = u0 + k, seg = u / TG, rem = u - seg * TG, tile = rem / p.G;
+          issue_w(p.seg_e[seg], tile, rem - tile * p.G, p.seg_n[seg], k);
+        }
+      __syncwarp();
+    }
+    if (kEarly && MODE == 1) pdl_wait();   // h comes from the gate/up kernel
     for (int u = u0; u < u1; ++u) {
       if (fills >= p.stages && !mbar_wait(&empty[s], ph ^ 1u)) {
         if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 11);
@@ -547,23 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p)
       const int seg = u / TG, rem = u - seg * TG, tile = rem / p.G, g = rem - tile * p.G;
       const int e = p.seg_e[seg], pos0 = p.seg_pos[seg], nt_ok = p.seg_n[seg];
       uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-      if (lane == 0) {
-        // a bad table entry (recorded) skips the weight copy: the stage then
-        // completes on its activations alone and its result is garbage
-        const uint8_t* base = e == p.E ? p.w_shared : expert_base(p.w, p.wtab, p.wbytes, e, p.status);
-        mbar_arrive_expect_tx(&full[s],
-                              static_cast<uint32_t>((base ? SB * (kSbBytes + (G64 ? kSbSide : 0)) : 0) + nt_ok * 256));
-        if (base) {
-          const size_t u_a = static_cast<size_t>(tile) * p.G + g, u_b = static_cast<size_t>(tile + p.up_off) * p.G + g;
-          bulk_g2s_hint(st, base + u_a * kSbBytes, kSbBytes, &full[s], pol);
-          if (SB == 2) bulk_g2s_hint(st + kSbBytes, base + u_b * kSbBytes, kSbBytes, &full[s], pol);
-          if (G64) {   // side entries after the x rows
-            uint8_t* sd = st + xoff + kSegRows * kXRowStride;
-            bulk_g2s_hint(sd, base + p.side_off + u_a * kSbSide, kSbSide, &full[s], pol);
-            if (SB == 2) bulk_g2s_hint(sd + kSbSide, base + p.side_off + u_b * kSbSide, kSbSide, &full[s], pol);
-          }
-        }
-      }
+      if (lane == 0 && fills >= npre) issue_w(e, tile, g, nt_ok, s);
       __syncwarp();
       if (lane < nt_ok) {
         const int row = MODE == 0 ? p.tok_of_pos[pos0 + lane] : pos0 + lane;
@@ -574,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p)
     }
     return;
   }
+  if (kEarly && MODE == 1) pdl_wait();   // the consumers write out[] and the tickets only after the gate/up kernel
 
   // ---------------- consumers
   const int gid = lane >> 2, tig = lane & 3;
@@ -598,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p)
     float s0g[XS], s1g[XS], s0u[XS], s1u[XS];
     const int ntiles = (nt_ok + 7) / 8;
     if constexpr (G64) {
-      const uint8_t* sd = sb + xoff + kSegRows * kXRowStride;
+      const uint8_t* sd = sb + xoff + kSegRowsK * kXRowStride;
       uint32_t z0[2], z1[2];
       unit_dot64<kNT, false>(sb, sd, sb + xoff, nt_ok, r0, gid, tig, ag, s0g, s1g, z0, z1, ntiles);
       if (SB == 2)
@@ -623,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p)
       }
     if (++s == p.stages) s = 0, ph ^= 1u;
     if ((u + 1) % p.G == 0 && u + 1 < u1) {
-      if (store<MODE>(p, gt, c, u0, u1, warp, lane, tg, tu)) owed0 = gt;
+      if (store<MODE, kNT>(p, gt, c, u0, u1, warp, lane, tg, tu)) owed0 = gt;
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
@@ -631,9 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p)
       ++gt;
     }
   }
-  const bool owed1 = store<MODE>(p, gt, c, u0, u1, warp, lane, tg, tu);
-  if (owed0 >= 0) ticket<MODE>(p, U, Pe, owed0, warp, lane);
-  if (owed1) ticket<MODE>(p, U, Pe, gt, warp, lane);
+  const bool owed1 = store<MODE, kNT>(p, gt, c, u0, u1, warp, lane, tg, tu);
+  if (owed0 >= 0) ticket<MODE, kNT>(p, U, Pe, owed0, warp, lane);
+  if (owed1) ticket<MODE, kNT>(p, U, Pe, gt, warp, lane);
 }
 
 // ------------------------------------------------------------------ combine
@@ -684,6 +731,7 @@ struct MoeLayout {
   size_t plan, ids, wts, offsets, perm, inv, tok, wpos, sege, segp, segn, h, out, cnt13, cnt2, part13, part2, xp, gu,
       total;
   int nseg_max, P, stages13, stages2, gemm;
+  int nt;   // token tiles of 8 per segment of the grouped rows kernels (1 for M <= 8, else 4)
   uint32_t stage13, stage2;
 };
 
@@ -701,8 +749,11 @@ bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeL
     return false;
   if (static_cast<long long>(M) * k > kMaxAssign) return false;
   const int n = M * k, npos = n + (has_shared ? M : 0);
-  L->nseg_max = std::min(E, n) + (n + kSegRows - 1) / kSegRows + (has_shared ? (M + kSegRows - 1) / kSegRows : 0);
-  L->P = sms;
+  // M <= 8: an expert holds at most M positions, so segments of 8 suffice
+  L->nt = M <= 8 ? 1 : kNT;
+  const int seg_rows = 8 * L->nt;
+  L->nseg_max = std::min(E, n) + (n + seg_rows - 1) / seg_rows + (has_shared ? (M + seg_rows - 1) / seg_rows : 0);
+  L->P = L->nt == 1 ? 2 * sms : sms;
   const int TT13 = I / kRowTile, TT2 = H / kRowTile;
   // everything after the counter region that the linear kernels keep zero
   // between calls: one workspace can serve calls of every entry point
@@ -722,17 +773,18 @@ bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeL
   L->out = o; o = al(o + 4ull * npos * H);
   L->cnt13 = o; o = al(o + 4ull * L->nseg_max * TT13 * kConsumerWarps);
   L->cnt2 = o; o = al(o + 4ull * L->nseg_max * TT2 * kConsumerWarps);
-  L->part13 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * kNT * 2);
-  L->part2 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * kNT);
+  L->part13 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * L->nt * 2);
+  L->part2 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * L->nt);
   L->gemm = moe_uses_gemm(M, E, k, H) ? 1 : 0;
   L->xp = o; o = al(o + (L->gemm ? 2ull * npos * H : 0));
   L->gu = o; o = al(o + (L->gemm ? 4ull * npos * 2 * I : 0));
   L->total = o;
   const int side = g64 ? kSbSide : 0;
-  L->stage13 = static_cast<uint32_t>((2 * (kSbBytes + side) + kSegRows * kXRowStride + 127) / 128 * 128);
-  L->stage2 = static_cast<uint32_t>((kSbBytes + side + kSegRows * kXRowStride + 127) / 128 * 128);
-  L->stages13 = std::min(8, static_cast<int>((200u * 1024u) / L->stage13));
-  L->stages2 = std::min(12, static_cast<int>((200u * 1024u) / L->stage2));
+  L->stage13 = static_cast<uint32_t>((2 * (kSbBytes + side) + seg_rows * kXRowStride + 127) / 128 * 128);
+  L->stage2 = static_cast<uint32_t>((kSbBytes + side + seg_rows * kXRowStride + 127) / 128 * 128);
+  const unsigned budget = L->nt == 1 ? 100u * 1024u : 200u * 1024u;   // two CTAs per SM for nt = 1
+  L->stages13 = std::min(8, static_cast<int>(budget / L->stage13));
+  L->stages2 = std::min(12, static_cast<int>(budget / L->stage2));
   return true;
 }
 
@@ -839,7 +891,7 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     a.G13 = H / kGroup;
     a.G2 = I / kGroup;
     a.has_shared = has_shared;
-    a.seg_rows = L.gemm ? 128 : kSegRows;
+    a.seg_rows = L.gemm ? 128 : 8 * L.nt;
     a.offsets = reinterpret_cast<int32_t*>(W + L.offsets);
     a.perm = reinterpret_cast<int32_t*>(W + L.perm);
     a.inv = reinterpret_cast<int32_t*>(W + L.inv);
@@ -919,12 +971,15 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     p.stages = mode == 0 ? L.stages13 : L.stages2;
     p.stage_bytes = mode == 0 ? L.stage13 : L.stage2;
     const size_t smem = static_cast<size_t>(p.stages) * p.stage_bytes + 2 * p.stages * sizeof(uint64_t);
-    static bool attr_done[4][64] = {{false}};
+    static bool attr_done[8][64] = {{false}};
     int dev = 0;
     cudaGetDevice(&dev);
-    auto kern = g64 ? (mode == 0 ? k_moe_rows<0, true> : k_moe_rows<1, true>)
-                    : (mode == 0 ? k_moe_rows<0, false> : k_moe_rows<1, false>);
-    const int ki = 2 * (g64 ? 1 : 0) + mode;
+    using KFn = void (*)(MoeRowsParams);
+    static const KFn kerns[8] = {k_moe_rows<0, false, kNT>, k_moe_rows<1, false, kNT>, k_moe_rows<0, true, kNT>,
+                                 k_moe_rows<1, true, kNT>,  k_moe_rows<0, false, 1>,   k_moe_rows<1, false, 1>,
+                                 k_moe_rows<0, true, 1>,    k_moe_rows<1, true, 1>};
+    const int ki = 4 * (L.nt == 1 ? 1 : 0) + 2 * (g64 ? 1 : 0) + mode;
+    const KFn kern = kerns[ki];
     if (dev >= 0 && dev < 64 && !attr_done[ki][dev]) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
         return FL_ERR_CUDA;

@@ -98,7 +98,7 @@ def small():
                 sw13_d=repack_dev(*sw13[0], 2 * I, H), sw2_d=repack_dev(*sw2[0], H, I))
 
 
-@pytest.mark.parametrize("M", [1, 5, 37, 70])
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 37, 70])
 @pytest.mark.parametrize("mode", ["softmax", "sigmoid_shared", "softmax_norenorm"])
 def test_moe_small_parity(small, M, mode):
     E, H, I = small["E"], small["H"], small["I"]
@@ -128,6 +128,25 @@ def test_moe_routing_ties_and_all_experts(small):
         check_routing(logits, k, fl.FL_SOFTMAX, True, ids, wts, offs, perm)
         ref, tol, _, _ = O.moe(O.bf16_value(xb), logits, k, small["w13"], small["w2"], O.SOFTMAX, True)
         check_y(y, ref, tol)
+
+
+@pytest.mark.parametrize("M", [8, 9])
+def test_moe_full_segments(small, M):
+    """Every token routed to the same k experts: at M = 8 each of them holds
+    one full segment of 8 positions (the decode build), at M = 9 one segment
+    of 9 (the 32-position build)."""
+    E, H, I = small["E"], small["H"], small["I"]
+    k = 3
+    row = inputs.router_logits(1, E, stream=630)
+    logits = np.repeat(row, M, axis=0)
+    xb = inputs.activations(M, H, stream=630 + M)
+    y, ids, wts, offs, perm = run_moe(xb, logits, k, I, small["w13_d"], small["w2_d"], fl.FL_SIGMOID, True,
+                                      small["sw13_d"], small["sw2_d"])
+    check_routing(logits, k, fl.FL_SIGMOID, True, ids, wts, offs, perm)
+    assert sorted(np.diff(offs.cpu().numpy()).tolist())[-k:] == [M] * k
+    ref, tol, _, _ = O.moe(O.bf16_value(xb), logits, k, small["w13"], small["w2"], O.SIGMOID, True,
+                           small["sw13"], small["sw2"])
+    check_y(y, ref, tol)
 
 
 def test_moe_deterministic(small):
