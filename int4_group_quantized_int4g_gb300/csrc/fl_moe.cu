@@ -24,6 +24,8 @@
 //   fl_moe_gemm    gate/up rows, fp32 [pos, 2I]
 //   k_moe_swiglu   h = silu(gate) * up, bf16 [pos, I]
 //   fl_moe_gemm    out = w_pos * (W2 h), fp32 [pos, H]
+#include <climits>
+
 #include "fl_common.cuh"
 #include "fl_rows.cuh"
 
@@ -45,18 +47,23 @@ struct MoePlan {
 
 // ------------------------------------------------------------------ route
 // Order used by the selection: larger logit first, equal logits -> lower index.
-__device__ __forceinline__ bool better(float v, int e, float bv, int be) { return v > bv || (v == bv && e < be); }
 
-__global__ void k_moe_route(const float* __restrict__ logits, int M, int E, int k, int scoring, int renorm,
-                            float scale, int32_t* __restrict__ ids, float* __restrict__ wts,
-                            int32_t* __restrict__ status) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= M) return;
-  constexpr int kPer = kMaxE / 32;
+// A float's order as a signed integer (NaN excluded; -0 taken as +0).
+__device__ __forceinline__ int order_key(float x) {
+  const int b = __float_as_int(x == 0.f ? 0.f : x);
+  return b ^ ((b >> 31) & 0x7fffffff);
+}
+
+// The routing of one token by one warp: the top k of the E logits at l
+// (E <= 32 * kPer; a NaN counts as -inf and is reported through the return
+// value), then the gate weights in fp32.  Lane j < k ends with slot j:
+// expert `mye`, weight `myw`.  Each pick takes the warp maximum of the
+// untaken keys and, among the lanes holding it, the lowest expert index.
+template <int kPer>
+__device__ __forceinline__ bool route_token(const float* __restrict__ l, int E, int k, int scoring, int renorm,
+                                            float scale, int lane, int& mye, float& myw) {
   float v[kPer];
-  uint32_t taken = 0;
-  const float* l = logits + static_cast<size_t>(t) * E;
+  int key[kPer];
   int bad = 0;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
@@ -67,25 +74,20 @@ __global__ void k_moe_route(const float* __restrict__ logits, int M, int E, int 
       if (isnan(x)) bad = 1, x = -INFINITY;
     }
     v[i] = x;
+    key[i] = e < E ? order_key(x) : INT_MIN;   // a real -inf still beats an absent slot
   }
-  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, FL_ERR_DEVICE_CHECK, t);
-  // slot j's choice is kept by lane j (k <= 32, checked on the host)
+  uint32_t taken = 0;
   float myv = -INFINITY, v0 = -INFINITY;
-  int mye = 0;
+  mye = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
+    int lk = INT_MIN, li = 0;
+    float lv = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, be)) bv = v[i], be = e;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (better(ov, oe, bv, be)) bv = ov, be = oe;
-    }
+    for (int i = 0; i < kPer; ++i)
+      if (!((taken >> i) & 1u) && key[i] > lk) lk = key[i], li = i, lv = v[i];
+    const int m = __reduce_max_sync(0xffffffffu, lk);
+    const int be = __reduce_min_sync(0xffffffffu, lk == m ? li * 32 + lane : INT_MAX);
+    const float bv = __shfl_sync(0xffffffffu, lv, be & 31);
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
     if (lane == j) myv = bv, mye = be;
     if (j == 0) v0 = bv;
@@ -113,9 +115,24 @@ __global__ void k_moe_route(const float* __restrict__ logits, int M, int E, int 
     else
       den = 1.f;
   }
+  myw = num / den * scale;
+  return __any_sync(0xffffffffu, bad) != 0;
+}
+
+template <int kPer>
+__global__ void k_moe_route(const float* __restrict__ logits, int M, int E, int k, int scoring, int renorm,
+                            float scale, int32_t* __restrict__ ids, float* __restrict__ wts,
+                            int32_t* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= M) return;
+  int mye;
+  float myw;
+  const bool bad = route_token<kPer>(logits + static_cast<size_t>(t) * E, E, k, scoring, renorm, scale, lane, mye, myw);
+  if (bad && lane == 0) set_status(status, FL_ERR_DEVICE_CHECK, t);
   if (lane < k) {
     ids[static_cast<size_t>(t) * k + lane] = mye;
-    wts[static_cast<size_t>(t) * k + lane] = num / den * scale;
+    wts[static_cast<size_t>(t) * k + lane] = myw;
   }
 }
 
@@ -399,7 +416,128 @@ struct MoeRowsParams {
   int32_t* status;
   int P, stages;
   uint32_t stage_bytes;
+  // Decode (segments of 8) with plain routing: `logits` non-null.  Every CTA
+  // then routes the M <= 8 tokens and builds the plan itself, in shared
+  // memory at `sr_off` (no route or permute launch); the gate/up kernel's
+  // CTAs also write the routing outputs below, each a slice of them.
+  const float* logits;
+  int M, k, scoring, renorm, has_shared;
+  float scale;
+  uint32_t sr_off;
+  int32_t* ids;
+  float* wts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv;
+  int32_t* user_offsets;
+  int32_t* user_perm;
+  MoePlan* plan_out;
 };
+
+// Shared-memory words of the self-routed plan for n = M*k assignments.
+__host__ __device__ constexpr int sr_words(int M, int k) { return 4 * (M * k) + 3 * (M * k + 1) + 2 * (M * k + M) + 4; }
+
+// The plan of the decode build computed in every CTA (see MoeRowsParams):
+// the routing of each token (one warp per token, the route kernel's
+// arithmetic), then what the permute kernel builds for segments of 8.  An
+// expert holds at most M <= 8 positions, so each chosen expert is one
+// segment of its positions in assignment order, ascending by expert, and
+// the shared expert's M positions are the last segment.  Returns the
+// number of segments; `pv` receives the plan's arrays in shared memory.
+struct PlanView {
+  const int32_t* seg_e;
+  const int32_t* seg_pos;
+  const int32_t* seg_n;
+  const int32_t* tok_of_pos;
+  const float* wpos;
+};
+
+template <int kPer>
+__device__ __forceinline__ int self_plan(const MoeRowsParams& p, int32_t* sm, bool write_outputs, PlanView& pv) {
+  const int M = p.M, k = p.k, n = M * k, npos = n + (p.has_shared ? M : 0);
+  const int tid = threadIdx.x, nth = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  int32_t* sids = sm;
+  float* swts = reinterpret_cast<float*>(sids + n);
+  int32_t* sexp = reinterpret_cast<int32_t*>(swts + n);   // expert of each position
+  int32_t* spos = sexp + n;                              // position of each assignment
+  int32_t* seg_e = spos + n;
+  int32_t* seg_pos = seg_e + (n + 1);
+  int32_t* seg_n = seg_pos + (n + 1);
+  int32_t* tok = seg_n + (n + 1);
+  float* wpos = reinterpret_cast<float*>(tok + (n + M));
+  int32_t* misc = reinterpret_cast<int32_t*>(wpos + (n + M));
+  if (warp < M) {
+    int mye;
+    float myw;
+    const bool bad = route_token<kPer>(p.logits + static_cast<size_t>(warp) * p.E, p.E, k, p.scoring, p.renorm,
+                                       p.scale, lane, mye, myw);
+    if (bad && lane == 0 && blockIdx.x == 0) set_status(p.status, FL_ERR_DEVICE_CHECK, warp);
+    if (lane < k) sids[warp * k + lane] = mye, swts[warp * k + lane] = myw;
+  }
+  __syncthreads();
+  // stable counting sort by expert: position = assignments of smaller
+  // experts + earlier assignments of the same expert
+  for (int i = tid; i < n; i += nth) {
+    const int e = sids[i];
+    int pos = 0;
+    for (int j = 0; j < n; ++j) {
+      const int ej = sids[j];
+      pos += (ej < e) | ((ej == e) & (j < i));
+    }
+    spos[i] = pos;
+    sexp[pos] = e;
+    tok[pos] = i / k;
+    wpos[pos] = swts[i];
+  }
+  for (int t = tid; t < (p.has_shared ? M : 0); t += nth) tok[n + t] = t, wpos[n + t] = 1.f;
+  __syncthreads();
+  for (int q = tid; q < n; q += nth) {
+    if (q > 0 && sexp[q] == sexp[q - 1]) continue;
+    int si = 0;
+    for (int r = 1; r <= q; ++r) si += sexp[r] != sexp[r - 1];
+    int cnt = 1;
+    while (q + cnt < n && sexp[q + cnt] == sexp[q]) ++cnt;
+    seg_e[si] = sexp[q];
+    seg_pos[si] = q;
+    seg_n[si] = cnt;
+  }
+  if (tid == 0) {
+    int nr = n > 0 ? 1 : 0;
+    for (int r = 1; r < n; ++r) nr += sexp[r] != sexp[r - 1];
+    if (p.has_shared) seg_e[nr] = p.E, seg_pos[nr] = n, seg_n[nr] = M;
+    misc[0] = nr + (p.has_shared ? 1 : 0);
+  }
+  if (write_outputs) {
+    // each CTA writes a slice of the routing outputs
+    const int g0 = blockIdx.x * nth + tid, gs = gridDim.x * nth;
+    for (int i = g0; i < n; i += gs) {
+      p.ids[i] = sids[i];
+      p.wts[i] = swts[i];
+      p.inv[i] = spos[i];
+      p.perm[spos[i]] = i;
+      if (p.user_perm) p.user_perm[spos[i]] = i;
+    }
+    for (int e = g0; e <= p.E; e += gs) {
+      int off = 0;
+      for (int j = 0; j < n; ++j) off += sids[j] < e;
+      p.offsets[e] = off;
+      if (p.user_offsets) p.user_offsets[e] = off;
+    }
+  }
+  __syncthreads();
+  const int nseg = misc[0];
+  if (write_outputs && blockIdx.x == 0 && tid == 0) {
+    p.plan_out->nseg = nseg;
+    p.plan_out->U = nseg * p.TT * p.G;
+  }
+  pv.seg_e = seg_e;
+  pv.seg_pos = seg_pos;
+  pv.seg_n = seg_n;
+  pv.tok_of_pos = tok;
+  pv.wpos = wpos;
+  (void)npos;
+  return nseg;
+}
 
 template <int MODE>
 struct MoeIO {
@@ -518,42 +656,17 @@ __device__ __forceinline__ bool store(const MoeRowsParams& p, int gt, int c, int
 // kNT token tiles of 8 per segment: 4 (segments of up to 32 positions, one
 // CTA per SM) or 1 (M <= 8: an expert never holds more than 8 positions; two
 // CTAs per SM).
+// Everything after the plan: the unit range of this CTA, the producer warp
+// and the consumer warps.
 template <int MODE, bool G64, int kNT>
-__global__ void __launch_bounds__(kThreads, kNT == 1 ? 2 : 1) k_moe_rows(const MoeRowsParams p) {
+__device__ __forceinline__ void rows_run(const MoeRowsParams& p, const int U, uint8_t* smem, uint64_t* full,
+                                         uint64_t* empty) {
   constexpr int SB = MoeIO<MODE>::kSB;
   constexpr int kSegRowsK = 8 * kNT;
   constexpr int XS = G64 ? 2 : 1;   // accumulator chains per super-block: one per 64-column group
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
-  uint64_t* empty = full + p.stages;
+  constexpr bool kEarly = kNT == 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-  // kEarly (segments of 8, decode): MODE 0 (gate/up) gets its plan, segments
-  // and x from the permute, the kernel just before it, and lets the next
-  // kernel start only once that wait is over.  So MODE 1 (down) starts after
-  // the permute has completed: it reads the plan at once (plain loads: written
-  // by a kernel that completed before this one started) and requests its first
-  // weights before its own wait; only h (from MODE 0) waits for the previous
-  // kernel.  Otherwise both modes wait at the top.
-  constexpr bool kEarly = kNT == 1;
-  if (kEarly && MODE == 0) {
-    pdl_wait();
-    pdl_launch_dependents();
-  } else if (kEarly) {
-    pdl_launch_dependents();
-  } else {
-    pdl_launch_dependents();
-    pdl_wait();
-  }
-  const int U = p.plan->U;
   // the work is split over min(P, U) CTAs, so that every working CTA owns at
   // least one unit (the ticket hand-off counts on it); the rest retire
   const int Pe = U < p.P ? U : p.P;
@@ -681,6 +794,55 @@ __global__ void __launch_bounds__(kThreads, kNT == 1 ? 2 : 1) k_moe_rows(const M
   const bool owed1 = store<MODE, kNT>(p, gt, c, u0, u1, warp, lane, tg, tu);
   if (owed0 >= 0) ticket<MODE, kNT>(p, U, Pe, owed0, warp, lane);
   if (owed1) ticket<MODE, kNT>(p, U, Pe, gt, warp, lane);
+}
+
+template <int MODE, bool G64, int kNT>
+__global__ void __launch_bounds__(kThreads, kNT == 1 ? 2 : 1) k_moe_rows(const MoeRowsParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
+  uint64_t* empty = full + p.stages;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // kEarly (segments of 8, decode): MODE 0 (gate/up) gets its plan (or,
+  // self-routed, the logits), segments and x from the kernels before it, and
+  // lets the next kernel start only once that wait is over.  So MODE 1 (down)
+  // starts after those have completed: it reads the plan or the logits at
+  // once (plain loads: written by kernels that completed before this one
+  // started) and requests its first weights before its own wait; only h
+  // (from MODE 0) waits for the previous kernel.  Otherwise both modes wait
+  // at the top.
+  constexpr bool kEarly = kNT == 1;
+  if (kEarly && MODE == 0) {
+    pdl_wait();
+    pdl_launch_dependents();
+  } else if (kEarly) {
+    pdl_launch_dependents();
+  } else {
+    pdl_launch_dependents();
+    pdl_wait();
+  }
+  if constexpr (kEarly) {
+    if (p.logits) {
+      PlanView pv;
+      int32_t* sm = reinterpret_cast<int32_t*>(smem + p.sr_off);
+      const int nseg = p.E <= 128 ? self_plan<4>(p, sm, MODE == 0, pv) : self_plan<8>(p, sm, MODE == 0, pv);
+      MoeRowsParams q = p;   // the plan arrays in shared memory
+      q.seg_e = pv.seg_e;
+      q.seg_pos = pv.seg_pos;
+      q.seg_n = pv.seg_n;
+      q.tok_of_pos = pv.tok_of_pos;
+      q.wpos = pv.wpos;
+      rows_run<MODE, G64, kNT>(q, nseg * p.TT * p.G, smem, full, empty);
+      return;
+    }
+  }
+  rows_run<MODE, G64, kNT>(p, p.plan->U, smem, full, empty);
 }
 
 // ------------------------------------------------------------------ combine
@@ -864,8 +1026,16 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
   const size_t b13 = n13 * (kSbBytes + (g64 ? kSbSide : 0));
   const size_t b2 = n2 * (kSbBytes + (g64 ? kSbSide : 0));
 
+  // Decode with plain routing (segments of 8, E <= 256): the grouped kernels
+  // route the tokens themselves, so neither route nor permute is launched.
+  // Their ticket counters then live in the counter region, which is zero
+  // between calls, since no kernel before them can clear them.
+  const size_t sr_cnt13 = 4ull * L.nseg_max * (I / kRowTile) * kConsumerWarps;
+  const size_t sr_cnt2 = 4ull * L.nseg_max * (H / kRowTile) * kConsumerWarps;
+  const bool sr = !keyed && !L.gemm && L.nt == 1 && E <= 256 && M <= 8 &&
+                  kTicketOff + sr_cnt13 + sr_cnt2 <= kScratchOff;
   // route
-  {
+  if (!sr) {
     // plain launches: the logits come from whatever ran before this call
     if (keyed) {
       const size_t smem = static_cast<size_t>(kRouteWarps) * (E + n_group) * sizeof(double);
@@ -873,13 +1043,20 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
           logits, routing->score_bias, M, E, k, renorm, n_group, topk_group, scale, ids, wts, status);
     } else {
       const int warps = 8;
-      k_moe_route<<<dim3((M + warps - 1) / warps), dim3(32 * warps), 0, s>>>(logits, M, E, k, scoring, renorm,
-                                                                              scale, ids, wts, status);
+      const dim3 grid((M + warps - 1) / warps), block(32 * warps);
+      if (E <= 128)
+        k_moe_route<4><<<grid, block, 0, s>>>(logits, M, E, k, scoring, renorm, scale, ids, wts, status);
+      else if (E <= 256)
+        k_moe_route<8><<<grid, block, 0, s>>>(logits, M, E, k, scoring, renorm, scale, ids, wts, status);
+      else if (E <= 512)
+        k_moe_route<16><<<grid, block, 0, s>>>(logits, M, E, k, scoring, renorm, scale, ids, wts, status);
+      else
+        k_moe_route<32><<<grid, block, 0, s>>>(logits, M, E, k, scoring, renorm, scale, ids, wts, status);
     }
     if (cudaGetLastError() != cudaSuccess) return FL_ERR_CUDA;
   }
   // permute
-  {
+  if (!sr) {
     PermuteArgs a;
     a.ids = ids;
     a.wts = wts;
@@ -965,12 +1142,30 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     p.h = reinterpret_cast<__nv_bfloat16*>(W + L.h);
     p.out = reinterpret_cast<float*>(W + L.out);
     p.part = reinterpret_cast<float*>(W + (mode == 0 ? L.part13 : L.part2));
-    p.cnt = reinterpret_cast<int32_t*>(W + (mode == 0 ? L.cnt13 : L.cnt2));
+    p.cnt = reinterpret_cast<int32_t*>(sr ? W + kTicketOff + (mode == 0 ? 0 : sr_cnt13)
+                                          : W + (mode == 0 ? L.cnt13 : L.cnt2));
     p.status = status;
     p.P = L.P;
     p.stages = mode == 0 ? L.stages13 : L.stages2;
     p.stage_bytes = mode == 0 ? L.stage13 : L.stage2;
-    const size_t smem = static_cast<size_t>(p.stages) * p.stage_bytes + 2 * p.stages * sizeof(uint64_t);
+    size_t smem = static_cast<size_t>(p.stages) * p.stage_bytes + 2 * p.stages * sizeof(uint64_t);
+    p.logits = sr ? logits : nullptr;
+    p.M = M;
+    p.k = k;
+    p.scoring = scoring;
+    p.renorm = renorm;
+    p.has_shared = has_shared;
+    p.scale = scale;
+    p.sr_off = static_cast<uint32_t>((smem + 15) / 16 * 16);
+    p.ids = ids;
+    p.wts = wts;
+    p.offsets = reinterpret_cast<int32_t*>(W + L.offsets);
+    p.perm = reinterpret_cast<int32_t*>(W + L.perm);
+    p.inv = reinterpret_cast<int32_t*>(W + L.inv);
+    p.user_offsets = expert_offsets;
+    p.user_perm = perm;
+    p.plan_out = plan;
+    if (sr) smem = p.sr_off + 4ull * sr_words(M, k);
     static bool attr_done[8][64] = {{false}};
     int dev = 0;
     cudaGetDevice(&dev);
