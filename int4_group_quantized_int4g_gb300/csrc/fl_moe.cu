@@ -591,9 +591,20 @@ __device__ __forceinline__ void ticket(const MoeRowsParams& p, int U, int Pe, in
   const int cf = cta_of_unit_d(tu0, U, Pe), cl = cta_of_unit_d(tu1 - 1, U, Pe);
   int last = 0;
   if (lane == 0) {
-    fence_acq_rel_gpu();
-    last = atomicAdd(&p.cnt[gt * kConsumerWarps + warp], 1) == cl - cf;
-    if (last) fence_acq_rel_gpu();
+    if constexpr (kNT == 1) {
+      // one acq_rel atomic: release of the warp's partials (ordered before
+      // it by the __syncwarp), acquire of everyone else's by the last arriver
+      int old;
+      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                   : "=r"(old)
+                   : "l"(&p.cnt[gt * kConsumerWarps + warp])
+                   : "memory");
+      last = old == cl - cf;
+    } else {
+      fence_acq_rel_gpu();
+      last = atomicAdd(&p.cnt[gt * kConsumerWarps + warp], 1) == cl - cf;
+      if (last) fence_acq_rel_gpu();
+    }
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
@@ -604,20 +615,64 @@ __device__ __forceinline__ void ticket(const MoeRowsParams& p, int U, int Pe, in
   for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) tg[nt][e] = 0.f, tu[nt][e] = 0.f;
-  for (int cc = cf; cc <= cl; ++cc) {   // CTA order: deterministic
-    const bool second = gt != unit_begin_d(cc, U, Pe) / p.G;
-    const float* sp = slot_ptr<MODE, kNT>(p, cc, second, warp);
+  if constexpr (kNT == 1) {
+    // the sharers' partials, added in CTA order (deterministic); the loads of
+    // a batch of kB sharers are all issued before the first add, so the last
+    // arriver pays about one L2 round trip per batch, not one per sharer
+    constexpr int kB = 4;
+    for (int cb = cf; cb <= cl; cb += kB) {
+      float4 buf[kB][kNT][2];
+  #pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        const int cc = cb + b;
+        if (cc > cl) break;
+        const bool second = gt != unit_begin_d(cc, U, Pe) / p.G;
+        const float* sp = slot_ptr<MODE, kNT>(p, cc, second, warp);
+  #pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+  #pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float* q = sp + ((gid + 8 * hh) * Mp + nt * 8 + 2 * tig) * V;
+            if (V == 2) {
+              buf[b][nt][hh] = __ldcg(reinterpret_cast<const float4*>(q));
+            } else {
+              const float2 v = __ldcg(reinterpret_cast<const float2*>(q));
+              buf[b][nt][hh] = make_float4(v.x, v.y, 0.f, 0.f);
+            }
+          }
+      }
+  #pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        if (cb + b > cl) break;
+  #pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+  #pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float4 v = buf[b][nt][hh];
+            if (V == 2) {
+              tg[nt][2 * hh] += v.x, tu[nt][2 * hh] += v.y, tg[nt][2 * hh + 1] += v.z, tu[nt][2 * hh + 1] += v.w;
+            } else {
+              tg[nt][2 * hh] += v.x, tg[nt][2 * hh + 1] += v.y;
+            }
+          }
+      }
+    }
+  } else {
+    for (int cc = cf; cc <= cl; ++cc) {   // CTA order: deterministic
+      const bool second = gt != unit_begin_d(cc, U, Pe) / p.G;
+      const float* sp = slot_ptr<MODE, kNT>(p, cc, second, warp);
 #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
+      for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const float* q = sp + ((gid + 8 * hh) * Mp + nt * 8 + 2 * tig) * V;
-        if (V == 2) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(q));
-          tg[nt][2 * hh] += v.x, tu[nt][2 * hh] += v.y, tg[nt][2 * hh + 1] += v.z, tu[nt][2 * hh + 1] += v.w;
-        } else {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(q));
-          tg[nt][2 * hh] += v.x, tg[nt][2 * hh + 1] += v.y;
+        for (int hh = 0; hh < 2; ++hh) {
+          const float* q = sp + ((gid + 8 * hh) * Mp + nt * 8 + 2 * tig) * V;
+          if (V == 2) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(q));
+            tg[nt][2 * hh] += v.x, tu[nt][2 * hh] += v.y, tg[nt][2 * hh + 1] += v.z, tu[nt][2 * hh + 1] += v.w;
+          } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(q));
+            tg[nt][2 * hh] += v.x, tg[nt][2 * hh + 1] += v.y;
+          }
         }
       }
     }
@@ -653,11 +708,10 @@ __device__ __forceinline__ bool store(const MoeRowsParams& p, int gt, int c, int
   return true;
 }
 
-// kNT token tiles of 8 per segment: 4 (segments of up to 32 positions, one
-// CTA per SM) or 1 (M <= 8: an expert never holds more than 8 positions; two
-// CTAs per SM).
 // Everything after the plan: the unit range of this CTA, the producer warp
-// and the consumer warps.
+// and the consumer warps.  kNT token tiles of 8 per segment: 4 (segments of
+// up to 32 positions, one CTA per SM) or 1 (M <= 8: an expert never holds
+// more than 8 positions; two CTAs per SM).
 template <int MODE, bool G64, int kNT>
 __device__ __forceinline__ void rows_run(const MoeRowsParams& p, const int U, uint8_t* smem, uint64_t* full,
                                          uint64_t* empty) {
@@ -797,7 +851,7 @@ __device__ __forceinline__ void rows_run(const MoeRowsParams& p, const int U, ui
 }
 
 template <int MODE, bool G64, int kNT>
-__global__ void __launch_bounds__(kThreads, kNT == 1 ? 2 : 1) k_moe_rows(const MoeRowsParams p) {
+__device__ __forceinline__ void rows_kernel(const MoeRowsParams& p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
   uint64_t* empty = full + p.stages;
@@ -843,6 +897,18 @@ __global__ void __launch_bounds__(kThreads, kNT == 1 ? 2 : 1) k_moe_rows(const M
     }
   }
   rows_run<MODE, G64, kNT>(p, p.plan->U, smem, full, empty);
+}
+
+// Segments of up to 32 positions: one CTA per SM.
+template <int MODE, bool G64>
+__global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p) {
+  rows_kernel<MODE, G64, kNT>(p);
+}
+
+// Decode (M <= 8, segments of 8): two CTAs per SM.
+template <int MODE, bool G64>
+__global__ void __launch_bounds__(kThreads, 2) k_moe_rows_dec(const MoeRowsParams p) {
+  rows_kernel<MODE, G64, 1>(p);
 }
 
 // ------------------------------------------------------------------ combine
@@ -1170,9 +1236,9 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     int dev = 0;
     cudaGetDevice(&dev);
     using KFn = void (*)(MoeRowsParams);
-    static const KFn kerns[8] = {k_moe_rows<0, false, kNT>, k_moe_rows<1, false, kNT>, k_moe_rows<0, true, kNT>,
-                                 k_moe_rows<1, true, kNT>,  k_moe_rows<0, false, 1>,   k_moe_rows<1, false, 1>,
-                                 k_moe_rows<0, true, 1>,    k_moe_rows<1, true, 1>};
+    static const KFn kerns[8] = {k_moe_rows<0, false>,     k_moe_rows<1, false>,     k_moe_rows<0, true>,
+                                 k_moe_rows<1, true>,      k_moe_rows_dec<0, false>, k_moe_rows_dec<1, false>,
+                                 k_moe_rows_dec<0, true>,  k_moe_rows_dec<1, true>};
     const int ki = 4 * (L.nt == 1 ? 1 : 0) + 2 * (g64 ? 1 : 0) + mode;
     const KFn kern = kerns[ki];
     if (dev >= 0 && dev < 64 && !attr_done[ki][dev]) {
