@@ -156,6 +156,12 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
 // GPU-scope acquire/release fence (lighter than the sequentially consistent
 // fence behind __threadfence) for ticket hand-offs between CTAs.
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// atomic add at GPU scope with acquire-release semantics; returns the old value
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

@@ -802,11 +802,8 @@ __device__ __forceinline__ void td_ticket(const TdParams& p, int T, int q, int l
   __syncwarp();
   const int cf = td_cta_of_unit(T * p.G, p.U, p.P), cl = td_cta_of_unit((T + 1) * p.G - 1, p.U, p.P);
   int last = 0;
-  if (lane == 0) {
-    fence_acq_rel_gpu();
-    last = atomicAdd(&p.cnt[T * 8 + q], 1) == cl - cf;
-    if (last) fence_acq_rel_gpu();
-  }
+  // release of this warp's partials, acquire of the others' for the last arriver
+  if (lane == 0) last = atom_add_acq_rel_gpu(&p.cnt[T * 8 + q], 1) == cl - cf;
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   __syncwarp();
@@ -815,13 +812,23 @@ __device__ __forceinline__ void td_ticket(const TdParams& p, int T, int q, int l
   float acc[NB];
 #pragma unroll
   for (int m = 0; m < NB; ++m) acc[m] = 0.f;
-  for (int cc = cf; cc <= cl; ++cc) {   // CTA order: deterministic
+  // CTA order (deterministic); two sharers' loads in flight at a time
+  for (int cc = cf; cc <= cl; cc += 2) {
+    const bool two = cc + 1 <= cl;
     const float* pp = p.part + static_cast<size_t>(cc + T) * kRowTile * NB + r;
-    float v[NB];
+    float v[2][NB];
 #pragma unroll
-    for (int m = 0; m < NB; ++m) v[m] = __ldcg(pp + m * kRowTile);
+    for (int m = 0; m < NB; ++m) v[0][m] = __ldcg(pp + m * kRowTile);
+    if (two) {
 #pragma unroll
-    for (int m = 0; m < NB; ++m) acc[m] += v[m];
+      for (int m = 0; m < NB; ++m) v[1][m] = __ldcg(pp + kRowTile * NB + m * kRowTile);
+    }
+#pragma unroll
+    for (int m = 0; m < NB; ++m) acc[m] += v[0][m];
+    if (two) {
+#pragma unroll
+      for (int m = 0; m < NB; ++m) acc[m] += v[1][m];
+    }
   }
   if (n < p.N) {
 #pragma unroll

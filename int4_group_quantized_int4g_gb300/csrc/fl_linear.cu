@@ -113,15 +113,12 @@ __device__ __forceinline__ void ticket_tile(const RowsParams& p, int T, int warp
   constexpr size_t kSlot = static_cast<size_t>(kRowTile) * Mp;
   const int tu0 = T * p.G, tu1 = (T + 1) * p.G;
   // the warp's partial stores are ordered before lane 0's ticket by the warp
-  // barrier and published at GPU scope by lane 0's release fence
+  // barrier and published at GPU scope by the release half of lane 0's
+  // acq_rel atomic; its acquire half gives the last arriver everyone else's
   __syncwarp();
   const int cf = cta_of_unit(tu0, p.U, p.P), cl = cta_of_unit(tu1 - 1, p.U, p.P);
   int last = 0;
-  if (lane == 0) {
-    fence_acq_rel_gpu();
-    last = atomicAdd(&p.cnt[T * kConsumerWarps + warp], 1) == cl - cf;
-    if (last) fence_acq_rel_gpu();
-  }
+  if (lane == 0) last = atom_add_acq_rel_gpu(&p.cnt[T * kConsumerWarps + warp], 1) == cl - cf;
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   const int np = cl - cf + 1;

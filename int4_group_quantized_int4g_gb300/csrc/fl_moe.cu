@@ -594,12 +594,7 @@ __device__ __forceinline__ void ticket(const MoeRowsParams& p, int U, int Pe, in
     if constexpr (kNT == 1) {
       // one acq_rel atomic: release of the warp's partials (ordered before
       // it by the __syncwarp), acquire of everyone else's by the last arriver
-      int old;
-      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
-                   : "=r"(old)
-                   : "l"(&p.cnt[gt * kConsumerWarps + warp])
-                   : "memory");
-      last = old == cl - cf;
+      last = atom_add_acq_rel_gpu(&p.cnt[gt * kConsumerWarps + warp], 1) == cl - cf;
     } else {
       fence_acq_rel_gpu();
       last = atomicAdd(&p.cnt[gt * kConsumerWarps + warp], 1) == cl - cf;
