@@ -155,6 +155,14 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
 
 // GPU-scope acquire/release fence (lighter than the sequentially consistent
 // fence behind __threadfence) for ticket hand-offs between CTAs.
+// Block barrier after code in which the lanes of a warp took different paths
+// (a lane-0 producer or MMA loop, a thread-0 setup block): each warp first
+// reconverges, so that the aligned barrier is always reached by whole warps.
+__device__ __forceinline__ void cta_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 // atomic add at GPU scope with acquire-release semantics; returns the old value
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {

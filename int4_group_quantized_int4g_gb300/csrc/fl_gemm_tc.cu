@@ -123,6 +123,15 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
 // Read NC chunks of 16 columns starting at taddr, keeping the next chunk's
 // load in flight while the current one is consumed; `release` runs as soon as
 // the last load has completed (the accumulator may then be overwritten).
+// 4-byte asynchronous copy global -> shared (generic proxy), and the wait for
+// all of this thread's copies.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
 template <int NC, typename Rel, typename Use>
 __device__ __forceinline__ void pf_drain(uint32_t taddr, Rel&& release, Use&& use) {
   static_assert(NC % 2 == 0, "chunks come in pairs");
@@ -309,6 +318,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
   uint64_t* dempty = dfull + 1;                                       // accumulator read out (8 epilogue warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + 1);
   int* epi_abort = reinterpret_cast<int*>(tmem_slot + 1);
+  int* done_flag = epi_abort + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -338,7 +348,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem_d = *tmem_slot;          // accumulator: columns [0, BN)
   const uint32_t tmem_a = tmem_d + BN;         // A ring: columns [BN, BN + 64 * RA)
@@ -570,10 +580,70 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
         return p.part + static_cast<size_t>(2 * cc + (td_unit_begin(cc, p.U, p.P) / p.G == T ? 0 : 1)) * kRowTile * BN;
       };
       int done = 0;
-      if (last_of_cta) {   // the accumulator is not needed afterwards: combine in place if all others are in
-        if (lane == 0) done = ld_acquire_gpu(cnt) == cl - cf;
-        done = __shfl_sync(0xffffffffu, done, 0);
-        __syncwarp();   // orders every lane's reads after lane 0's acquire
+      if (last_of_cta) {
+        // The accumulator is not needed afterwards: combine in place if all
+        // other sharers are in, one decision for the 8 epilogue warps (every
+        // warp's counter full), shared through the named barrier, which also
+        // orders every thread's reads after the acquiring loads.
+        if (e == 0) {   // lanes 0..7 acquire one warp's counter each, in parallel
+          const bool in = lane >= 8 || ld_acquire_gpu(p.cnt + T * 8 + lane) == cl - cf;
+          const bool all = __all_sync(0xffffffffu, in);
+          if (lane == 0) *done_flag = all ? 1 : 0;
+        }
+        named_bar(1, 256);
+        done = *reinterpret_cast<volatile int*>(done_flag);
+      }
+      if (done && p.tma_y && cl - cf == 1) {
+        // The CTA's MMAs are over, so its x stages hold nothing: each thread
+        // copies its elements of the other sharer's partial into them (all
+        // copies in flight at once), then the tile goes out like a whole one:
+        // accumulator + partial in CTA order, bf16 through the staging tile,
+        // one TMA store per half.
+        constexpr int kWarpFloats = (BN / 2) * 32;   // a warp's rows x columns of one slot
+        static_assert(8 * kWarpFloats * 4 <= NBS * C::kBBox, "partial staging");
+        float* stage = reinterpret_cast<float*>(smem);
+        const int co = cf == c ? cl : cf;
+        const bool other_first = co < c;
+        {
+          fence_proxy_async();   // the stages were last written by TMA
+          const float* src = slot_of(co) + static_cast<size_t>(col0) * kRowTile + r;
+          float* dst = stage + static_cast<size_t>(e) * kWarpFloats + lane;
+#pragma unroll 8
+          for (int j = 0; j < BN / 2; ++j) cp_async4(dst + j * 32, src + j * kRowTile);
+          cp_async_wait_all();
+        }
+        named_bar(1, 256);   // every warp's part of the partial is in
+        __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem + C::kStgOff);
+#pragma unroll 1
+        for (int rho = 0; rho < 2; ++rho) {
+          const int lt0 = (e >> 2) * (BN / 4);
+          const float* sp = stage + static_cast<size_t>(q + 4 * rho) * kWarpFloats + lane;
+          pf_drain<BN / 64>(
+              tmem_d + (static_cast<uint32_t>(q * 32) << 16) + rho * (BN / 2) + lt0,
+              [&]() {
+                if (rho == 1) release_d();
+              },
+              [&](int k, const float (&v)[16]) {
+                __nv_bfloat16* dst = stg + static_cast<size_t>(lt0 + 16 * k) * kRowTile + r;
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                  const float o = sp[(lt0 + 16 * k + t) * 32];
+                  const float sum = other_first ? (0.f + o) + v[t] : (0.f + v[t]) + o;   // CTA order
+                  dst[t * kRowTile] = __float2bfloat16_rn(sum);
+                }
+              });
+          fence_proxy_async();
+          named_bar(1, 256);
+          if (e == 0 && lane == 0) {
+            tma_store_2d(&ymap, stg, nt * kRowTile, mt * BN + rho * (BN / 2));
+            bulk_commit();
+            bulk_wait_read0();   // the staging tile has been read
+          }
+          named_bar(1, 256);
+        }
+        __syncwarp();
+        if (lane == 0) *cnt = 0;
+        continue;
       }
       if (done) {
         pf_drain<BN / 32>(tcol, release_d, [&](int k, const float (&v)[16]) {
@@ -629,7 +699,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_gemm_tc(const __grid_constant
     if (e == 0 && lane == 0) bulk_wait0();   // y stores complete before the CTA exits
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_d, C::kTmemCols);
@@ -887,7 +957,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem_d = *tmem_slot;
   pdl_launch_dependents();
@@ -1052,7 +1122,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
     }
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_d, C::kTmemCols);
@@ -1192,7 +1262,7 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem_d = *tmem_slot;
   const uint32_t tmem_a = tmem_d + BN;
@@ -1401,7 +1471,7 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
     }
   }
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_d, C::kTmemCols);

@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
     fence_mbar_init();
   }
   if (threadIdx.x < 16) reinterpret_cast<uint4*>(smem + p.zrow_off)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
-  __syncthreads();
+  cta_sync();
   // rank 0's reduction barrier is initialised before any peer can arrive on it
   if (p.csize > 1) cluster_sync_all();
   // the next kernel in the stream may start prefetching its weights now

@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_mlp_block(const MlpParams p) {
     fence_mbar_init();
   }
   if (threadIdx.x < 16) reinterpret_cast<uint4*>(smem + p.zrow_off)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
-  __syncthreads();
+  cta_sync();
 
   if (warp == kCW) {
     // ------------------------------------------------ producer warp
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_mlp_block(const MlpParams p) {
     }
   }
   // ---------------- the last CTA to finish resets the grid counters
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) {
     fence_acq_rel_gpu();
     if (atomicAdd(p.bar + 1, 1) == p.P - 1) {

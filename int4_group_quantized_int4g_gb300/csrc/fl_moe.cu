@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(1024, 1) k_moe_permute(const PermuteArgs a) {
   int32_t* nch = tot + (E + 1);                // [E + 1] segment starts
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < 32 * E; i += blockDim.x) counts[i] = 0;
-  __syncthreads();
+  cta_sync();
   // per-warp stable ranks: warp w owns assignments [w*C, (w+1)*C)
   const int C = (n + 31) / 32;
   const int i0 = warp * C, i1 = min(n, i0 + C);
@@ -296,14 +296,14 @@ __global__ void __launch_bounds__(1024, 1) k_moe_permute(const PermuteArgs a) {
     }
     __syncwarp();
   }
-  __syncthreads();
+  cta_sync();
   // totals, then per-expert base offsets for every warp
   for (int e = tid; e < E; e += blockDim.x) {
     int s = 0;
     for (int w = 0; w < 32; ++w) s += counts[w * E + e];
     tot[e] = s;
   }
-  __syncthreads();
+  cta_sync();
   if (warp == 0) {
     // exclusive scans of the counts (-> offsets) and of the segment counts
     // (-> first segment of each expert): lane l takes experts [l*per, (l+1)*per)
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(1024, 1) k_moe_permute(const PermuteArgs a) {
       a.plan->U = (all_s + nshared) * a.TT13 * a.G13;   // == (all_s + nshared) * TT2 * G2
     }
   }
-  __syncthreads();
+  cta_sync();
   for (int e = tid; e < E; e += blockDim.x) {
     int run = tot[e];
     for (int w = 0; w < 32; ++w) {
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(1024, 1) k_moe_permute(const PermuteArgs a) {
     a.offsets[e] = tot[e];
     if (a.user_offsets) a.user_offsets[e] = tot[e];
   }
-  __syncthreads();
+  cta_sync();
   for (int i = tid; i < n; i += blockDim.x) {
     const int w = i / C;
     const int e = a.ids[i];
@@ -474,7 +474,7 @@ __device__ __forceinline__ int self_plan(const MoeRowsParams& p, int32_t* sm, bo
     if (bad && lane == 0 && blockIdx.x == 0) set_status(p.status, FL_ERR_DEVICE_CHECK, warp);
     if (lane < k) sids[warp * k + lane] = mye, swts[warp * k + lane] = myw;
   }
-  __syncthreads();
+  cta_sync();
   // stable counting sort by expert: position = assignments of smaller
   // experts + earlier assignments of the same expert
   for (int i = tid; i < n; i += nth) {
@@ -490,7 +490,7 @@ __device__ __forceinline__ int self_plan(const MoeRowsParams& p, int32_t* sm, bo
     wpos[pos] = swts[i];
   }
   for (int t = tid; t < (p.has_shared ? M : 0); t += nth) tok[n + t] = t, wpos[n + t] = 1.f;
-  __syncthreads();
+  cta_sync();
   for (int q = tid; q < n; q += nth) {
     if (q > 0 && sexp[q] == sexp[q - 1]) continue;
     int si = 0;
@@ -524,7 +524,7 @@ __device__ __forceinline__ int self_plan(const MoeRowsParams& p, int32_t* sm, bo
       if (p.user_offsets) p.user_offsets[e] = off;
     }
   }
-  __syncthreads();
+  cta_sync();
   const int nseg = misc[0];
   if (write_outputs && blockIdx.x == 0 && tid == 0) {
     p.plan_out->nseg = nseg;
@@ -857,7 +857,7 @@ __device__ __forceinline__ void rows_kernel(const MoeRowsParams& p) {
     }
     fence_mbar_init();
   }
-  __syncthreads();
+  cta_sync();
   // kEarly (segments of 8, decode): MODE 0 (gate/up) gets its plan (or,
   // self-routed, the logits), segments and x from the kernels before it, and
   // lets the next kernel start only once that wait is over.  So MODE 1 (down)
