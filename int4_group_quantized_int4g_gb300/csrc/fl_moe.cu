@@ -8,15 +8,20 @@
 // Pipeline, one stream, no host synchronisation:
 //   k_moe_route    one warp per token: top-k of the fp32 logits, gate weights
 //   k_moe_permute  one CTA: stable counting sort of the M*k assignments by
-//                  expert, token segments of <= 32 rows per expert (the shared
-//                  expert is one more expert holding every token with weight
-//                  1), the device-side work plan, zeroed ticket counters
+//                  expert, token segments of <= 32 (or <= 8) rows per expert
+//                  (the shared expert is one more expert holding every token
+//                  with weight 1), the device-side work plan, zeroed ticket
+//                  counters
 //   k_moe_rows<0>  grouped gate/up: h = silu(G x) * (U x), bf16 [pos, I]
 //   k_moe_rows<1>  grouped down: out = w_pos * (W2 h), fp32 [pos, H]
 //   k_moe_combine  y[t] = sum_j out[slot (t,j)] + shared out[t], bf16
 // The grouped kernels stream each active expert's super-blocks once per
-// 32-token segment, with the same register-dequant mma.sync consumer as the
-// decode linear, split over K across all SMs with a ticket hand-off.
+// segment, with the same register-dequant mma.sync consumer as the decode
+// linear, split over K across all SMs with a ticket hand-off.  With at most 4
+// positions per expert on average (and for M <= 8) they run as
+// k_moe_rows_dec: segments of 8, two CTAs per SM.  For M <= 8 with plain
+// routing, k_moe_rows_dec routes the tokens itself in every CTA and neither
+// k_moe_route nor k_moe_permute is launched.
 //
 // With many tokens per expert (see moe_uses_gemm) the two grouped steps run on the
 // tensor-memory GEMM instead (fl_moe_gemm, segments of up to 128 positions):
@@ -959,11 +964,12 @@ struct MoeLayout {
 };
 
 // Many tokens per expert: the grouped steps run on the tensor-memory GEMM
-// (from 8 tokens per expert on average, or from 2 with large experts, where
-// the GEMM's per-super-block cost wins over its extra launches).
+// (from 8 positions per expert on average, or from more than 4 with large
+// experts, where the GEMM's per-super-block cost wins over the rows
+// kernels' segments of 32; up to 4 the rows kernels' segments of 8 win).
 bool moe_uses_gemm(int M, int E, int k, int H) {
   const long long n = static_cast<long long>(M) * k;
-  return n >= 8LL * E || (n >= 2LL * E && H >= 4096);
+  return n >= 8LL * E || (n > 4LL * E && H >= 4096);
 }
 
 bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeLayout* L, bool g64 = false) {
@@ -972,8 +978,10 @@ bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeL
     return false;
   if (static_cast<long long>(M) * k > kMaxAssign) return false;
   const int n = M * k, npos = n + (has_shared ? M : 0);
-  // M <= 8: an expert holds at most M positions, so segments of 8 suffice
-  L->nt = M <= 8 ? 1 : kNT;
+  // Segments of 8 (two CTAs per SM) when M <= 8, where an expert holds at
+  // most M positions, and when the experts hold 4 positions or fewer on
+  // average (an expert with more than 8 streams its weights once per 8)
+  L->nt = (M <= 8 || static_cast<long long>(M) * k <= 4LL * E) ? 1 : kNT;
   const int seg_rows = 8 * L->nt;
   L->nseg_max = std::min(E, n) + (n + seg_rows - 1) / seg_rows + (has_shared ? (M + seg_rows - 1) / seg_rows : 0);
   L->P = L->nt == 1 ? 2 * sms : sms;

@@ -149,6 +149,24 @@ def test_moe_full_segments(small, M):
     check_y(y, ref, tol)
 
 
+@pytest.mark.parametrize("M", [12, 24])
+def test_moe_segments_of_8_past_decode(M):
+    """Up to 4 positions per expert on average, M > 8: segments of 8 built by
+    the permute kernel (an expert with more than 8 positions spans two)."""
+    E, H, I, k = 32, 256, 256, 4
+    w13, w2 = host_experts(E, H, I, layer=640)
+    sw13, sw2 = host_experts(1, H, I, layer=641)
+    xb = inputs.activations(M, H, stream=640 + M)
+    logits = inputs.router_logits(M, E, stream=640 + M)
+    logits[:, 3] += 4.0   # one expert chosen by every token: M > 8 positions
+    y, ids, wts, offs, perm = run_moe(xb, logits, k, I, stack_dev(w13, 2 * I, H), stack_dev(w2, H, I),
+                                      fl.FL_SIGMOID, True, repack_dev(*sw13[0], 2 * I, H), repack_dev(*sw2[0], H, I))
+    check_routing(logits, k, fl.FL_SIGMOID, True, ids, wts, offs, perm)
+    assert np.diff(offs.cpu().numpy())[3] == M
+    ref, tol, _, _ = O.moe(O.bf16_value(xb), logits, k, w13, w2, O.SIGMOID, True, sw13[0], sw2[0])
+    check_y(y, ref, tol)
+
+
 def test_moe_deterministic(small):
     M = 37
     xb = inputs.activations(M, small["H"], stream=620)
