@@ -8,20 +8,17 @@
 // Pipeline, one stream, no host synchronisation:
 //   k_moe_route    one warp per token: top-k of the fp32 logits, gate weights
 //   k_moe_permute  one CTA: stable counting sort of the M*k assignments by
-//                  expert, token segments of <= 32 (or <= 8) rows per expert
-//                  (the shared expert is one more expert holding every token
-//                  with weight 1), the device-side work plan, zeroed ticket
-//                  counters
+//                  expert, token segments of <= 8 rows per expert (the shared
+//                  expert is one more expert holding every token with weight
+//                  1), the device-side work plan, zeroed ticket counters
 //   k_moe_rows<0>  grouped gate/up: h = silu(G x) * (U x), bf16 [pos, I]
 //   k_moe_rows<1>  grouped down: out = w_pos * (W2 h), fp32 [pos, H]
 //   k_moe_combine  y[t] = sum_j out[slot (t,j)] + shared out[t], bf16
 // The grouped kernels stream each active expert's super-blocks once per
 // segment, with the same register-dequant mma.sync consumer as the decode
-// linear, split over K across all SMs with a ticket hand-off.  With at most 4
-// positions per expert on average (and for M <= 8) they run as
-// k_moe_rows_dec: segments of 8, two CTAs per SM.  For M <= 8 with plain
-// routing, k_moe_rows_dec routes the tokens itself in every CTA and neither
-// k_moe_route nor k_moe_permute is launched.
+// linear, split over K across all SMs with a ticket hand-off, two CTAs per
+// SM.  For M <= 8 with plain routing, k_moe_rows routes the tokens itself in
+// every CTA and neither k_moe_route nor k_moe_permute is launched.
 //
 // With many tokens per expert (see moe_uses_gemm) the two grouped steps run on the
 // tensor-memory GEMM instead (fl_moe_gemm, segments of up to 128 positions):
@@ -38,7 +35,7 @@ using namespace fl;
 
 namespace {
 
-constexpr int kNT = 4;                // token tiles of 8 per segment (decode, M <= 8: 1)
+constexpr int kNT = 1;                // token tiles of 8 per segment: segments of 8 positions
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxE = 1024;
@@ -596,15 +593,9 @@ __device__ __forceinline__ void ticket(const MoeRowsParams& p, int U, int Pe, in
   const int cf = cta_of_unit_d(tu0, U, Pe), cl = cta_of_unit_d(tu1 - 1, U, Pe);
   int last = 0;
   if (lane == 0) {
-    if constexpr (kNT == 1) {
-      // one acq_rel atomic: release of the warp's partials (ordered before
-      // it by the __syncwarp), acquire of everyone else's by the last arriver
-      last = atom_add_acq_rel_gpu(&p.cnt[gt * kConsumerWarps + warp], 1) == cl - cf;
-    } else {
-      fence_acq_rel_gpu();
-      last = atomicAdd(&p.cnt[gt * kConsumerWarps + warp], 1) == cl - cf;
-      if (last) fence_acq_rel_gpu();
-    }
+    // one acq_rel atomic: release of the warp's partials (ordered before it
+    // by the __syncwarp), acquire of everyone else's by the last arriver
+    last = atom_add_acq_rel_gpu(&p.cnt[gt * kConsumerWarps + warp], 1) == cl - cf;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
@@ -615,66 +606,45 @@ __device__ __forceinline__ void ticket(const MoeRowsParams& p, int U, int Pe, in
   for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) tg[nt][e] = 0.f, tu[nt][e] = 0.f;
-  if constexpr (kNT == 1) {
-    // the sharers' partials, added in CTA order (deterministic); the loads of
-    // a batch of kB sharers are all issued before the first add, so the last
-    // arriver pays about one L2 round trip per batch, not one per sharer
-    constexpr int kB = 4;
-    for (int cb = cf; cb <= cl; cb += kB) {
-      float4 buf[kB][kNT][2];
-  #pragma unroll
-      for (int b = 0; b < kB; ++b) {
-        const int cc = cb + b;
-        if (cc > cl) break;
-        const bool second = gt != unit_begin_d(cc, U, Pe) / p.G;
-        const float* sp = slot_ptr<MODE, kNT>(p, cc, second, warp);
-  #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-  #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const float* q = sp + ((gid + 8 * hh) * Mp + nt * 8 + 2 * tig) * V;
-            if (V == 2) {
-              buf[b][nt][hh] = __ldcg(reinterpret_cast<const float4*>(q));
-            } else {
-              const float2 v = __ldcg(reinterpret_cast<const float2*>(q));
-              buf[b][nt][hh] = make_float4(v.x, v.y, 0.f, 0.f);
-            }
-          }
-      }
-  #pragma unroll
-      for (int b = 0; b < kB; ++b) {
-        if (cb + b > cl) break;
-  #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-  #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const float4 v = buf[b][nt][hh];
-            if (V == 2) {
-              tg[nt][2 * hh] += v.x, tu[nt][2 * hh] += v.y, tg[nt][2 * hh + 1] += v.z, tu[nt][2 * hh + 1] += v.w;
-            } else {
-              tg[nt][2 * hh] += v.x, tg[nt][2 * hh + 1] += v.y;
-            }
-          }
-      }
-    }
-  } else {
-    for (int cc = cf; cc <= cl; ++cc) {   // CTA order: deterministic
+  // the sharers' partials, added in CTA order (deterministic); the loads of
+  // a batch of kB sharers are all issued before the first add, so the last
+  // arriver pays about one L2 round trip per batch, not one per sharer
+  constexpr int kB = 4;
+  for (int cb = cf; cb <= cl; cb += kB) {
+    float4 buf[kB][kNT][2];
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int cc = cb + b;
+      if (cc > cl) break;
       const bool second = gt != unit_begin_d(cc, U, Pe) / p.G;
       const float* sp = slot_ptr<MODE, kNT>(p, cc, second, warp);
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
+      for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const float* q = sp + ((gid + 8 * hh) * Mp + nt * 8 + 2 * tig) * V;
           if (V == 2) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(q));
-            tg[nt][2 * hh] += v.x, tu[nt][2 * hh] += v.y, tg[nt][2 * hh + 1] += v.z, tu[nt][2 * hh + 1] += v.w;
+            buf[b][nt][hh] = __ldcg(reinterpret_cast<const float4*>(q));
           } else {
             const float2 v = __ldcg(reinterpret_cast<const float2*>(q));
+            buf[b][nt][hh] = make_float4(v.x, v.y, 0.f, 0.f);
+          }
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      if (cb + b > cl) break;
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const float4 v = buf[b][nt][hh];
+          if (V == 2) {
+            tg[nt][2 * hh] += v.x, tu[nt][2 * hh] += v.y, tg[nt][2 * hh + 1] += v.z, tu[nt][2 * hh + 1] += v.w;
+          } else {
             tg[nt][2 * hh] += v.x, tg[nt][2 * hh + 1] += v.y;
           }
         }
-      }
     }
   }
   emit<MODE, kNT>(p, seg, tile, warp, lane, tg, tu);
@@ -709,16 +679,13 @@ __device__ __forceinline__ bool store(const MoeRowsParams& p, int gt, int c, int
 }
 
 // Everything after the plan: the unit range of this CTA, the producer warp
-// and the consumer warps.  kNT token tiles of 8 per segment: 4 (segments of
-// up to 32 positions, one CTA per SM) or 1 (M <= 8: an expert never holds
-// more than 8 positions; two CTAs per SM).
+// and the consumer warps.
 template <int MODE, bool G64, int kNT>
 __device__ __forceinline__ void rows_run(const MoeRowsParams& p, const int U, uint8_t* smem, uint64_t* full,
                                          uint64_t* empty) {
   constexpr int SB = MoeIO<MODE>::kSB;
   constexpr int kSegRowsK = 8 * kNT;
   constexpr int XS = G64 ? 2 : 1;   // accumulator chains per super-block: one per 64-column group
-  constexpr bool kEarly = kNT == 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   // the work is split over min(P, U) CTAs, so that every working CTA owns at
@@ -732,8 +699,8 @@ __device__ __forceinline__ void rows_run(const MoeRowsParams& p, const int U, ui
   if (warp == kConsumerWarps) {
     // ---------------- producer: super-block(s) + the segment's x rows
     const uint64_t pol = policy_evict_first();
-    // kEarly MODE 1: the weights of the first stages before the wait (see above)
-    const int npre = kEarly && MODE == 1 ? min(u1 - u0, p.stages) : 0;
+    // MODE 1: the weights of the first stages before the wait (see rows_kernel)
+    const int npre = MODE == 1 ? min(u1 - u0, p.stages) : 0;
     int s = 0, fills = 0;
     uint32_t ph = 0;
     // weights of (row tile, group) of expert e into stage `slot`, by lane 0
@@ -763,7 +730,7 @@ __device__ __forceinline__ void rows_run(const MoeRowsParams& p, const int U, ui
         }
       __syncwarp();
     }
-    if (kEarly && MODE == 1) pdl_wait();   // h comes from the gate/up kernel
+    if (MODE == 1) pdl_wait();   // h comes from the gate/up kernel
     for (int u = u0; u < u1; ++u) {
       if (fills >= p.stages && !mbar_wait(&empty[s], ph ^ 1u)) {
         if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 11);
@@ -787,7 +754,7 @@ __device__ __forceinline__ void rows_run(const MoeRowsParams& p, const int U, ui
     }
     return;
   }
-  if (kEarly && MODE == 1) pdl_wait();   // the consumers write out[] and the tickets only after the gate/up kernel
+  if (MODE == 1) pdl_wait();   // the consumers write out[] and the tickets only after the gate/up kernel
 
   // ---------------- consumers
   const int gid = lane >> 2, tig = lane & 3;
@@ -863,52 +830,39 @@ __device__ __forceinline__ void rows_kernel(const MoeRowsParams& p) {
     fence_mbar_init();
   }
   cta_sync();
-  // kEarly (segments of 8, decode): MODE 0 (gate/up) gets its plan (or,
-  // self-routed, the logits), segments and x from the kernels before it, and
-  // lets the next kernel start only once that wait is over.  So MODE 1 (down)
-  // starts after those have completed: it reads the plan or the logits at
-  // once (plain loads: written by kernels that completed before this one
-  // started) and requests its first weights before its own wait; only h
-  // (from MODE 0) waits for the previous kernel.  Otherwise both modes wait
-  // at the top.
-  constexpr bool kEarly = kNT == 1;
-  if (kEarly && MODE == 0) {
+  // MODE 0 (gate/up) gets its plan (or, self-routed, the logits), segments
+  // and x from the kernels before it, and lets the next kernel start only
+  // once that wait is over.  So MODE 1 (down) starts after those have
+  // completed: it reads the plan or the logits at once (plain loads: written
+  // by kernels that completed before this one started) and requests its
+  // first weights before its own wait; only h (from MODE 0) waits for the
+  // previous kernel.
+  if (MODE == 0) {
     pdl_wait();
-    pdl_launch_dependents();
-  } else if (kEarly) {
     pdl_launch_dependents();
   } else {
     pdl_launch_dependents();
-    pdl_wait();
   }
-  if constexpr (kEarly) {
-    if (p.logits) {
-      PlanView pv;
-      int32_t* sm = reinterpret_cast<int32_t*>(smem + p.sr_off);
-      const int nseg = p.E <= 128 ? self_plan<4>(p, sm, MODE == 0, pv) : self_plan<8>(p, sm, MODE == 0, pv);
-      MoeRowsParams q = p;   // the plan arrays in shared memory
-      q.seg_e = pv.seg_e;
-      q.seg_pos = pv.seg_pos;
-      q.seg_n = pv.seg_n;
-      q.tok_of_pos = pv.tok_of_pos;
-      q.wpos = pv.wpos;
-      rows_run<MODE, G64, kNT>(q, nseg * p.TT * p.G, smem, full, empty);
-      return;
-    }
+  if (p.logits) {
+    PlanView pv;
+    int32_t* sm = reinterpret_cast<int32_t*>(smem + p.sr_off);
+    const int nseg = p.E <= 128 ? self_plan<4>(p, sm, MODE == 0, pv) : self_plan<8>(p, sm, MODE == 0, pv);
+    MoeRowsParams q = p;   // the plan arrays in shared memory
+    q.seg_e = pv.seg_e;
+    q.seg_pos = pv.seg_pos;
+    q.seg_n = pv.seg_n;
+    q.tok_of_pos = pv.tok_of_pos;
+    q.wpos = pv.wpos;
+    rows_run<MODE, G64, kNT>(q, nseg * p.TT * p.G, smem, full, empty);
+    return;
   }
   rows_run<MODE, G64, kNT>(p, p.plan->U, smem, full, empty);
 }
 
-// Segments of up to 32 positions: one CTA per SM.
+// Two CTAs per SM.
 template <int MODE, bool G64>
-__global__ void __launch_bounds__(kThreads, 1) k_moe_rows(const MoeRowsParams p) {
+__global__ void __launch_bounds__(kThreads, 2) k_moe_rows(const MoeRowsParams p) {
   rows_kernel<MODE, G64, kNT>(p);
-}
-
-// Decode (M <= 8, segments of 8): two CTAs per SM.
-template <int MODE, bool G64>
-__global__ void __launch_bounds__(kThreads, 2) k_moe_rows_dec(const MoeRowsParams p) {
-  rows_kernel<MODE, G64, 1>(p);
 }
 
 // ------------------------------------------------------------------ combine
@@ -959,17 +913,18 @@ struct MoeLayout {
   size_t plan, ids, wts, offsets, perm, inv, tok, wpos, sege, segp, segn, h, out, cnt13, cnt2, part13, part2, xp, gu,
       total;
   int nseg_max, P, stages13, stages2, gemm;
-  int nt;   // token tiles of 8 per segment of the grouped rows kernels (1 for M <= 8, else 4)
   uint32_t stage13, stage2;
 };
 
 // Many tokens per expert: the grouped steps run on the tensor-memory GEMM
-// (from 8 positions per expert on average, or from more than 4 with large
-// experts, where the GEMM's per-super-block cost wins over the rows
-// kernels' segments of 32; up to 4 the rows kernels' segments of 8 win).
+// above 8 positions per expert on average.  Up to 8 the rows kernels win,
+// although an expert with more than 8 positions streams its weights once per
+// segment of 8 (measured on the Qwen3- and DeepSeek-V3-shaped layers: at 8
+// positions per expert the rows kernels take 0.75-0.9 of the GEMM's time, at
+// 16 about 1.1-1.5 times it).
 bool moe_uses_gemm(int M, int E, int k, int H) {
   const long long n = static_cast<long long>(M) * k;
-  return n >= 8LL * E || (n > 4LL * E && H >= 4096);
+  return n > 8LL * E;
 }
 
 bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeLayout* L, bool g64 = false) {
@@ -978,13 +933,11 @@ bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeL
     return false;
   if (static_cast<long long>(M) * k > kMaxAssign) return false;
   const int n = M * k, npos = n + (has_shared ? M : 0);
-  // Segments of 8 (two CTAs per SM) when M <= 8, where an expert holds at
-  // most M positions, and when the experts hold 4 positions or fewer on
-  // average (an expert with more than 8 streams its weights once per 8)
-  L->nt = (M <= 8 || static_cast<long long>(M) * k <= 4LL * E) ? 1 : kNT;
-  const int seg_rows = 8 * L->nt;
+  // segments of 8 positions (an expert with more streams its weights once
+  // per segment)
+  const int seg_rows = 8 * kNT;
   L->nseg_max = std::min(E, n) + (n + seg_rows - 1) / seg_rows + (has_shared ? (M + seg_rows - 1) / seg_rows : 0);
-  L->P = L->nt == 1 ? 2 * sms : sms;
+  L->P = 2 * sms;   // two CTAs per SM
   const int TT13 = I / kRowTile, TT2 = H / kRowTile;
   // everything after the counter region that the linear kernels keep zero
   // between calls: one workspace can serve calls of every entry point
@@ -1004,8 +957,8 @@ bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeL
   L->out = o; o = al(o + 4ull * npos * H);
   L->cnt13 = o; o = al(o + 4ull * L->nseg_max * TT13 * kConsumerWarps);
   L->cnt2 = o; o = al(o + 4ull * L->nseg_max * TT2 * kConsumerWarps);
-  L->part13 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * L->nt * 2);
-  L->part2 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * L->nt);
+  L->part13 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * kNT * 2);
+  L->part2 = o; o = al(o + 4ull * 2 * L->P * kRowTile * 8 * kNT);
   L->gemm = moe_uses_gemm(M, E, k, H) ? 1 : 0;
   L->xp = o; o = al(o + (L->gemm ? 2ull * npos * H : 0));
   L->gu = o; o = al(o + (L->gemm ? 4ull * npos * 2 * I : 0));
@@ -1013,7 +966,7 @@ bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeL
   const int side = g64 ? kSbSide : 0;
   L->stage13 = static_cast<uint32_t>((2 * (kSbBytes + side) + seg_rows * kXRowStride + 127) / 128 * 128);
   L->stage2 = static_cast<uint32_t>((kSbBytes + side + seg_rows * kXRowStride + 127) / 128 * 128);
-  const unsigned budget = L->nt == 1 ? 100u * 1024u : 200u * 1024u;   // two CTAs per SM for nt = 1
+  const unsigned budget = 100u * 1024u;   // two CTAs per SM
   L->stages13 = std::min(8, static_cast<int>(budget / L->stage13));
   L->stages2 = std::min(12, static_cast<int>(budget / L->stage2));
   return true;
@@ -1101,7 +1054,7 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
   // between calls, since no kernel before them can clear them.
   const size_t sr_cnt13 = 4ull * L.nseg_max * (I / kRowTile) * kConsumerWarps;
   const size_t sr_cnt2 = 4ull * L.nseg_max * (H / kRowTile) * kConsumerWarps;
-  const bool sr = !keyed && !L.gemm && L.nt == 1 && E <= 256 && M <= 8 &&
+  const bool sr = !keyed && !L.gemm && E <= 256 && M <= 8 &&
                   kTicketOff + sr_cnt13 + sr_cnt2 <= kScratchOff;
   // route
   if (!sr) {
@@ -1137,7 +1090,7 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     a.G13 = H / kGroup;
     a.G2 = I / kGroup;
     a.has_shared = has_shared;
-    a.seg_rows = L.gemm ? 128 : 8 * L.nt;
+    a.seg_rows = L.gemm ? 128 : 8 * kNT;
     a.offsets = reinterpret_cast<int32_t*>(W + L.offsets);
     a.perm = reinterpret_cast<int32_t*>(W + L.perm);
     a.inv = reinterpret_cast<int32_t*>(W + L.inv);
@@ -1235,14 +1188,13 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     p.user_perm = perm;
     p.plan_out = plan;
     if (sr) smem = p.sr_off + 4ull * sr_words(M, k);
-    static bool attr_done[8][64] = {{false}};
+    static bool attr_done[4][64] = {{false}};
     int dev = 0;
     cudaGetDevice(&dev);
     using KFn = void (*)(MoeRowsParams);
-    static const KFn kerns[8] = {k_moe_rows<0, false>,     k_moe_rows<1, false>,     k_moe_rows<0, true>,
-                                 k_moe_rows<1, true>,      k_moe_rows_dec<0, false>, k_moe_rows_dec<1, false>,
-                                 k_moe_rows_dec<0, true>,  k_moe_rows_dec<1, true>};
-    const int ki = 4 * (L.nt == 1 ? 1 : 0) + 2 * (g64 ? 1 : 0) + mode;
+    static const KFn kerns[4] = {k_moe_rows<0, false>, k_moe_rows<1, false>, k_moe_rows<0, true>,
+                                 k_moe_rows<1, true>};
+    const int ki = 2 * (g64 ? 1 : 0) + mode;
     const KFn kern = kerns[ki];
     if (dev >= 0 && dev < 64 && !attr_done[ki][dev]) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)

@@ -133,8 +133,7 @@ def test_moe_routing_ties_and_all_experts(small):
 @pytest.mark.parametrize("M", [8, 9])
 def test_moe_full_segments(small, M):
     """Every token routed to the same k experts: at M = 8 each of them holds
-    one full segment of 8 positions (the decode build), at M = 9 one segment
-    of 9 (the 32-position build)."""
+    one full segment of 8 positions, at M = 9 two segments (8 and 1)."""
     E, H, I = small["E"], small["H"], small["I"]
     k = 3
     row = inputs.router_logits(1, E, stream=630)
