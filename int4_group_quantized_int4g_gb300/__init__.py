@@ -108,8 +108,12 @@ def _check(where, rc):
 
 def _stream(stream=None):
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:   # the current stream's handle without building a Stream object
+        return ctypes.c_void_p(raw(torch.cuda.current_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _p(t):
@@ -208,9 +212,8 @@ def fl_int4g_linear(x, w, N, y=None, ws=None, group=GROUP):
     M, K = x.shape
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    nb = fl_int4g_linear_workspace(M, N, K)
-    if ws is None:
-        ws = _workspace(nb, x.device)
+    if ws is None:   # (a caller's workspace is checked for size by the library)
+        ws = _workspace(fl_int4g_linear_workspace(M, N, K), x.device)
     if group == GROUP:
         _check("fl_int4g_linear",
                lib().fl_int4g_linear(_p(x), M, K, _p(w), N, _p(y), _p(ws), ws.numel(), _stream()))
