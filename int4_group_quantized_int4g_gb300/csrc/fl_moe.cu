@@ -468,46 +468,88 @@ __device__ __forceinline__ int self_plan(const MoeRowsParams& p, int32_t* sm, bo
   int32_t* tok = seg_n + (n + 1);
   float* wpos = reinterpret_cast<float*>(tok + (n + M));
   int32_t* misc = reinterpret_cast<int32_t*>(wpos + (n + M));
+  int mye = 0;
+  float myw = 0.f;
   if (warp < M) {
-    int mye;
-    float myw;
     const bool bad = route_token<kPer>(p.logits + static_cast<size_t>(warp) * p.E, p.E, k, p.scoring, p.renorm,
                                        p.scale, lane, mye, myw);
     if (bad && lane == 0 && blockIdx.x == 0) set_status(p.status, FL_ERR_DEVICE_CHECK, warp);
     if (lane < k) sids[warp * k + lane] = mye, swts[warp * k + lane] = myw;
   }
-  cta_sync();
-  // stable counting sort by expert: position = assignments of smaller
-  // experts + earlier assignments of the same expert
-  for (int i = tid; i < n; i += nth) {
-    const int e = sids[i];
-    int pos = 0;
-    for (int j = 0; j < n; ++j) {
-      const int ej = sids[j];
-      pos += (ej < e) | ((ej == e) & (j < i));
+  // n <= 32: warp 0 sorts and cuts the segments in registers (for M = 1 from
+  // its own picks, without waiting for the block); otherwise the block does
+  // it through shared memory
+  const bool one_warp = n <= 32;
+  if (!(one_warp && M == 1)) cta_sync();
+  if (one_warp) {
+    if (warp == 0) {
+      const bool act = lane < n;
+      const int e = act ? (M == 1 ? mye : sids[lane]) : INT_MAX;
+      const float w = act ? (M == 1 ? myw : swts[lane]) : 0.f;
+      // stable counting sort: position = assignments of smaller experts +
+      // earlier assignments of the same expert; segment = the number of
+      // smaller chosen experts (each expert's first assignment counts them)
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(same & ((1u << lane) - 1u));
+      const bool first = act && rank == 0;
+      const unsigned firsts = __ballot_sync(0xffffffffu, first);
+      int less = 0, si = 0;
+      for (int j = 0; j < n; ++j) {
+        const int ej = __shfl_sync(0xffffffffu, e, j);
+        less += ej < e;
+        si += ((firsts >> j) & 1u) && ej < e;
+      }
+      const int pos = less + rank;
+      if (act) {
+        sids[lane] = e;
+        swts[lane] = w;
+        spos[lane] = pos;
+        sexp[pos] = e;
+        tok[pos] = lane / k;
+        wpos[pos] = w;
+        if (first) seg_e[si] = e, seg_pos[si] = pos, seg_n[si] = __popc(same);
+      }
+      if (lane < (p.has_shared ? M : 0)) tok[n + lane] = lane, wpos[n + lane] = 1.f;
+      if (lane == 0) {
+        const int nr = __popc(firsts);
+        if (p.has_shared) seg_e[nr] = p.E, seg_pos[nr] = n, seg_n[nr] = M;
+        misc[0] = nr + (p.has_shared ? 1 : 0);
+      }
     }
-    spos[i] = pos;
-    sexp[pos] = e;
-    tok[pos] = i / k;
-    wpos[pos] = swts[i];
-  }
-  for (int t = tid; t < (p.has_shared ? M : 0); t += nth) tok[n + t] = t, wpos[n + t] = 1.f;
-  cta_sync();
-  for (int q = tid; q < n; q += nth) {
-    if (q > 0 && sexp[q] == sexp[q - 1]) continue;
-    int si = 0;
-    for (int r = 1; r <= q; ++r) si += sexp[r] != sexp[r - 1];
-    int cnt = 1;
-    while (q + cnt < n && sexp[q + cnt] == sexp[q]) ++cnt;
-    seg_e[si] = sexp[q];
-    seg_pos[si] = q;
-    seg_n[si] = cnt;
-  }
-  if (tid == 0) {
-    int nr = n > 0 ? 1 : 0;
-    for (int r = 1; r < n; ++r) nr += sexp[r] != sexp[r - 1];
-    if (p.has_shared) seg_e[nr] = p.E, seg_pos[nr] = n, seg_n[nr] = M;
-    misc[0] = nr + (p.has_shared ? 1 : 0);
+    cta_sync();
+  } else {
+    // stable counting sort by expert: position = assignments of smaller
+    // experts + earlier assignments of the same expert
+    for (int i = tid; i < n; i += nth) {
+      const int e = sids[i];
+      int pos = 0;
+      for (int j = 0; j < n; ++j) {
+        const int ej = sids[j];
+        pos += (ej < e) | ((ej == e) & (j < i));
+      }
+      spos[i] = pos;
+      sexp[pos] = e;
+      tok[pos] = i / k;
+      wpos[pos] = swts[i];
+    }
+    for (int t = tid; t < (p.has_shared ? M : 0); t += nth) tok[n + t] = t, wpos[n + t] = 1.f;
+    cta_sync();
+    for (int q = tid; q < n; q += nth) {
+      if (q > 0 && sexp[q] == sexp[q - 1]) continue;
+      int si = 0;
+      for (int r = 1; r <= q; ++r) si += sexp[r] != sexp[r - 1];
+      int cnt = 1;
+      while (q + cnt < n && sexp[q + cnt] == sexp[q]) ++cnt;
+      seg_e[si] = sexp[q];
+      seg_pos[si] = q;
+      seg_n[si] = cnt;
+    }
+    if (tid == 0) {
+      int nr = n > 0 ? 1 : 0;
+      for (int r = 1; r < n; ++r) nr += sexp[r] != sexp[r - 1];
+      if (p.has_shared) seg_e[nr] = p.E, seg_pos[nr] = n, seg_n[nr] = M;
+      misc[0] = nr + (p.has_shared ? 1 : 0);
+    }
   }
   if (write_outputs) {
     // each CTA writes a slice of the routing outputs
@@ -526,7 +568,7 @@ __device__ __forceinline__ int self_plan(const MoeRowsParams& p, int32_t* sm, bo
       if (p.user_offsets) p.user_offsets[e] = off;
     }
   }
-  cta_sync();
+  if (!one_warp) cta_sync();   // (the one-warp plan was published by its barrier)
   const int nseg = misc[0];
   if (write_outputs && blockIdx.x == 0 && tid == 0) {
     p.plan_out->nseg = nseg;
