@@ -574,7 +574,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // minb: CTAs per SM the kernel is built for (0 = the default for M); g64:
 // groups of 64 (side entries in the stages, two token sums per group).
-bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bool g64 = false, bool glu = false) {
+bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bool g64 = false, bool glu = false,
+                    int max_cs = 8) {
   if (M < 1 || M > kMaxTokens || N < 1 || K < kGroup || K % kGroup || sms < 1) return false;
   if ((N + kRowTile - 1) / kRowTile > kMaxRowTiles) return false;
   pl->T = (N + kRowTile - 1) / kRowTile;
@@ -594,7 +595,7 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bo
   pl->csize = 1;
   if (2LL * pl->T <= slots) {
     long long cs = slots / pl->T;
-    if (cs > 8) cs = 8;
+    if (cs > max_cs) cs = max_cs;
     // every rank streams at least one full stage (ups super-blocks): with a
     // single super-block a rank, the reduction over more ranks costs more
     // than the split saves (K=1024, N=3072, M=1: 4.04 us at 8 ranks, 3.28 us
@@ -732,10 +733,16 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   if (ws_bytes < pl.ws_bytes) return FL_ERR_WORKSPACE;
   // Clusters that would fill the GPU's cluster capacity leave some of them
   // waiting for a second wave whenever the previous kernel's exits fragment
-  // the free slots: such shapes run three smaller CTAs per SM instead (same
-  // grid, same workspace), which has capacity to spare.
+  // the free slots.  Such shapes take smaller clusters first (fused QKV,
+  // K=4096 N=12288 at M=1: 9.7 us with clusters of 2 against 11.2 us for the
+  // three-per-SM build), and three smaller CTAs per SM (same grid, same
+  // workspace) only if that is not enough.
   if (pl.NT == 1 && pl.csize > 1) {
-    const int cap = rows_cluster_capacity(pl);
+    int cap = rows_cluster_capacity(pl);
+    while (cap > 0 && pl.T > cap - 2 && pl.csize > 2) {
+      if (!make_rows_plan(M, N, K, flh::sm_count(), &pl, 0, g64, false, pl.csize - 1)) return FL_ERR_ARG;
+      cap = rows_cluster_capacity(pl);
+    }
     if (cap > 0 && pl.T > cap - 2 && !make_rows_plan(M, N, K, flh::sm_count(), &pl, 3, g64)) return FL_ERR_ARG;
   }
   RowsParams prm;
