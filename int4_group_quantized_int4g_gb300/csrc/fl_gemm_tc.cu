@@ -187,6 +187,17 @@ __device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// One thread of the (converged) warp, chosen by elect.sync.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // TMA 2-D tile load global -> shared, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile(
@@ -810,20 +821,28 @@ int launch_tc(const void* x, int M, int K, const void* w, int N, void* y, void* 
 }
 
 // ======================================================================
-// Decode (M <= 32) on tcgen05: the stream of super-blocks of the decode
-// linear, split over K across the SMs exactly like the mma.sync kernel (CTA c
-// owns units [c*U/P, (c+1)*U/P) in layout order, a row tile split across CTAs
-// is finished by the last CTA to take its ticket, partials summed in CTA
-// order), but the dot products run on tcgen05:
-//   warp 0        producer: super-block by 1-D bulk copy, the x tile (NB token
-//                 rows x 128 k, rows past M read as zero) by TMA
-//   warp 1        TMEM allocation; lane 0 issues 8 MMAs per super-block into
-//                 one of two accumulator buffers (N = NB tokens)
-//   warps 4..11   dequantize: exact (q - z) bf16 into the swizzled A tile
-//   warps 12..15  epilogue: per super-block, read the accumulator (row r =
-//                 lane of the warp's TMEM quadrant) and add s16 * D into
-//                 register sums; at a row tile's end, write or hand off.
-// The fp16 scale is applied to the fp32 group sum (no rounding of s*(q-z)).
+// Decode (8 < M <= 32) on tcgen05: the stream of super-blocks of the decode
+// linear, split over K across the SMs like the mma.sync kernel (CTA c owns
+// units [c*U/P, (c+1)*U/P) in layout order, a row tile split across CTAs is
+// finished by the last CTA to take its ticket, partials summed in CTA order),
+// but the dot products run on tcgen05.  One CTA per SM (a kernel that
+// allocates tensor memory gets one CTA per SM), so the work runs in three
+// independent chains: super-block i goes to MMA issuer i % 3 and dequant group
+// i % 3.
+//   warp 0        super-block producer (1-D bulk copies)
+//   warp 1        x producer: the x tile (NB token rows x 128 k, rows past M
+//                 read as zero) by TMA
+//   warps 2..4    MMA issuers: 8 MMAs per super-block (M = 128 rows, N = NB
+//                 tokens, K = 16), each issuer into its own accumulator per
+//                 row tile (two tile buffers)
+//   warps 5..16   dequant, three groups of four warps (one per tensor-memory
+//                 quadrant): the correctly rounded bf16(s16 * (q - z)) into
+//                 the group's A slot, so the accumulators hold scaled sums
+//   warps 17..20  epilogue, once per row tile: the issuers' accumulators added
+//                 in issuer order, then y written or the split tile handed off
+// The dequant is bound by the ALU (five instructions per pair of weights, three
+// of them on the bf16 pipe); one issuing thread reaches only about one
+// tcgen05.mma per 65 cycles.  Both are why the work runs in three chains.
 struct TdParams {
   const uint8_t* w;
   __nv_bfloat16* y;
@@ -836,18 +855,24 @@ struct TdParams {
 template <int NB>
 struct TdCfg {
   static constexpr int kXBytes = NB * 256;                        // NB rows x 128 k bf16 (two swizzled halves)
-  static constexpr int kSbRing = 16;                              // super-blocks in flight per CTA
-  static constexpr int kARing = 4;                                // dequantized A tiles (tensor memory)
-  static constexpr int kXRing = 8;                                // x tiles (one per super-block's group)
-  static constexpr int kDRing = 8;                                // accumulators in tensor memory
+  static constexpr int kChains = 3;                               // super-block i goes to issuer and dequant group i % 3
+  // ring sizes are multiples of kChains: every slot, and so every barrier,
+  // then has exactly one waiter chain (a parity wait is only sound when its
+  // waiter cannot be two phases behind)
+  static constexpr int kSbRing = 12;                              // super-blocks in flight per CTA
+  static constexpr int kARing = 3;                                // dequantized A tiles (tensor memory)
+  static constexpr int kXRing = 6;                                // x tiles (one per super-block's group)
   static constexpr int kSmem = kXRing * kXBytes + kSbRing * kSbBytes + 1024 /*align slack*/ + 1024 /*barriers*/;
-  static_assert((2 * kSbRing + 2 * kXRing + 2 * kARing + 2 * kDRing) * 8 + 8 <= 1024, "barrier area");
+  static_assert(kSbRing % kChains == 0 && kARing % kChains == 0 && kXRing % kChains == 0, "one chain per slot");
+  static_assert((2 * kSbRing + 2 * kXRing + 2 * kARing + 4 * kChains) * 8 + 8 <= 1024, "barrier area");
   static_assert(kSmem <= 232448, "shared memory");
-  static constexpr uint32_t kTmemCols = 512;                      // A ring 4 x 64 columns, D ring 8 x NB
+  static constexpr uint32_t kDCol = kARing * 64;                  // accumulators [issuer][tile buffer] of NB columns
+  static_assert(kDCol + 2 * kChains * NB + 32 - NB <= 512, "tensor memory");
+  static constexpr uint32_t kTmemCols = 512;
 };
 
-constexpr int kTdThreads = 16 * 32;
-constexpr int kTdDeq0 = 4, kTdEpi0 = 12;
+constexpr int kTdThreads = 21 * 32;
+constexpr int kTdIss0 = 2, kTdDeq0 = 5, kTdEpi0 = 17;
 
 
 // Final sums of row tile T for this epilogue thread's row: write them or hand
@@ -882,31 +907,36 @@ __device__ __forceinline__ void td_ticket(const TdParams& p, int T, int q, int l
   __syncwarp();
   const int r = q * 32 + lane;
   const int n = T * kRowTile + r;
-  float acc[NB];
+  // in halves of the tokens (registers); CTA order (deterministic); two
+  // sharers' loads in flight at a time
+  constexpr int H = NB / 2;
 #pragma unroll
-  for (int m = 0; m < NB; ++m) acc[m] = 0.f;
-  // CTA order (deterministic); two sharers' loads in flight at a time
-  for (int cc = cf; cc <= cl; cc += 2) {
-    const bool two = cc + 1 <= cl;
-    const float* pp = p.part + static_cast<size_t>(cc + T) * kRowTile * NB + r;
-    float v[2][NB];
+  for (int hh = 0; hh < 2; ++hh) {
+    float acc[H];
 #pragma unroll
-    for (int m = 0; m < NB; ++m) v[0][m] = __ldcg(pp + m * kRowTile);
-    if (two) {
+    for (int m = 0; m < H; ++m) acc[m] = 0.f;
+    for (int cc = cf; cc <= cl; cc += 2) {
+      const bool two = cc + 1 <= cl;
+      const float* pp = p.part + static_cast<size_t>(cc + T) * kRowTile * NB + r + hh * H * kRowTile;
+      float v[2][H];
 #pragma unroll
-      for (int m = 0; m < NB; ++m) v[1][m] = __ldcg(pp + kRowTile * NB + m * kRowTile);
+      for (int m = 0; m < H; ++m) v[0][m] = __ldcg(pp + m * kRowTile);
+      if (two) {
+#pragma unroll
+        for (int m = 0; m < H; ++m) v[1][m] = __ldcg(pp + kRowTile * NB + m * kRowTile);
+      }
+#pragma unroll
+      for (int m = 0; m < H; ++m) acc[m] += v[0][m];
+      if (two) {
+#pragma unroll
+        for (int m = 0; m < H; ++m) acc[m] += v[1][m];
+      }
     }
+    if (n < p.N) {
 #pragma unroll
-    for (int m = 0; m < NB; ++m) acc[m] += v[0][m];
-    if (two) {
-#pragma unroll
-      for (int m = 0; m < NB; ++m) acc[m] += v[1][m];
+      for (int m = 0; m < H; ++m)
+        if (hh * H + m < p.M) p.y[static_cast<size_t>(hh * H + m) * p.N + n] = __float2bfloat16_rn(acc[m]);
     }
-  }
-  if (n < p.N) {
-#pragma unroll
-    for (int m = 0; m < NB; ++m)
-      if (m < p.M) p.y[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(acc[m]);
   }
   __syncwarp();
   if (lane == 0) p.cnt[T * 8 + q] = 0;
@@ -915,47 +945,48 @@ __device__ __forceinline__ void td_ticket(const TdParams& p, int T, int q, int l
 template <int NB>
 __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_constant__ CUtensorMap xmap, const TdParams p) {
   using C = TdCfg<NB>;
-  constexpr int RS = C::kSbRing, RA = C::kARing, RX = C::kXRing;
+  constexpr int RS = C::kSbRing, RA = C::kARing, RX = C::kXRing, NC = C::kChains;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* xbuf = smem;                                    // [RX][NB*256] (1 KB aligned)
   uint8_t* sbuf = xbuf + RX * C::kXBytes;                  // [RS][8512]
   uint64_t* sb_full = reinterpret_cast<uint64_t*>(sbuf + RS * kSbBytes);
-  uint64_t* sb_empty = sb_full + RS;   // dequant (8 warps) + epilogue (4 warps)
+  uint64_t* sb_empty = sb_full + RS;   // the super-block's dequant group (4 warps)
   uint64_t* x_full = sb_empty + RS;    // [RX] x tile landed
   uint64_t* x_empty = x_full + RX;     // [RX] MMAs reading the x tile done
-  uint64_t* a_full = x_empty + RX;     // A tile dequantized (8 warps)
+  uint64_t* a_full = x_empty + RX;     // A tile dequantized (4 warps)
   uint64_t* a_empty = a_full + RA;     // MMAs on the A slot done
-  constexpr int RD = C::kDRing;
-  uint64_t* dfull = a_empty + RA;      // [RD]
-  uint64_t* dempty = dfull + RD;       // [RD]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + RD);
+  uint64_t* dfull = a_empty + RA;      // [issuer][tile buffer]: the issuer's last MMA of the tile done
+  uint64_t* dempty = dfull + 2 * NC;   // [issuer][tile buffer]: the epilogue has read that accumulator
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + 2 * NC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   const int u0 = td_unit_begin(c, p.U, p.P), u1 = td_unit_begin(c + 1, p.U, p.P);
   const int nu = u1 - u0;
+  // local end of the CTA's first row-tile segment
+  const int seg0_end = min(nu, (u0 / p.G + 1) * p.G - u0);
 
   if (threadIdx.x == 0) {
     for (int j = 0; j < RS; ++j) {
       mbar_init(&sb_full[j], 1);
-      mbar_init(&sb_empty[j], 8 + 4);
+      mbar_init(&sb_empty[j], 4);
     }
     for (int xs = 0; xs < RX; ++xs) {
       mbar_init(&x_full[xs], 1);
       mbar_init(&x_empty[xs], 1);
     }
     for (int a = 0; a < RA; ++a) {
-      mbar_init(&a_full[a], 8);
+      mbar_init(&a_full[a], 4);
       mbar_init(&a_empty[a], 1);
     }
-    for (int b = 0; b < RD; ++b) {
+    for (int b = 0; b < 2 * NC; ++b) {
       mbar_init(&dfull[b], 1);
       mbar_init(&dempty[b], 4);
     }
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kTdIss0) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
@@ -983,7 +1014,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
         bulk_g2s_hint(sbuf + j * kSbBytes, p.w + static_cast<size_t>(u0 + i) * kSbBytes, kSbBytes, &sb_full[j], pol);
       }
     }
-  } else if (warp == 2) {
+  } else if (warp == 1) {
     // ---------------- x producer: the tile of x for each super-block's group
     if (lane == 0) {
       pdl_wait();
@@ -1000,62 +1031,86 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
         tma_load_2d(xbuf + xs * C::kXBytes + NB * 128, &xmap, g * kGroup + 64, 0, &x_full[xs]);
       }
     }
-  } else if (warp == 1 || warp == 3) {
-    // ---------------- MMA issuers: warp 1 takes the even super-blocks, warp 3
-    // the odd ones.  One thread issues tcgen05.mma at only about one per 65
-    // cycles, and at N = NB the tensor pipe is far from full, so two issuers
-    // double the rate (each commit tracks only its own thread's MMAs).
-    // Each issuer probes its super-block's A slot, x tile and accumulator.
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16<NB>();
-      for (int i = warp == 1 ? 0 : 1; i < nu; i += 2) {
-        const int a = i % RA, b = i % RD;
-        const int xs = i % RX;
-        if (!mbar_wait(&a_full[a], static_cast<uint32_t>(i / RA) & 1u) ||
-            !mbar_wait(&x_full[xs], static_cast<uint32_t>(i / RX) & 1u) ||
-            (i >= RD && !mbar_wait(&dempty[b], static_cast<uint32_t>(i / RD - 1) & 1u))) {
-          set_status(p.status, FL_ERR_TIMEOUT, 32);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t x0 = smem_u32(xbuf + xs * C::kXBytes);
+  } else if (warp < kTdDeq0) {
+    // ---------------- MMA issuers: issuer e takes super-blocks e, e + 3, ...,
+    // each into its own accumulator per row tile (two tile buffers, so that
+    // the epilogue of one tile overlaps the next tile's MMAs).  One thread
+    // issues tcgen05.mma at only about one per 65 cycles, and at N = NB the
+    // tensor pipe is far from full, so three issuers triple the rate.  The
+    // whole warp runs the loop (its addresses and descriptors are warp
+    // uniform); one elected thread issues.
+    const int e = warp - kTdIss0;
+    const uint32_t idesc = idesc_bf16<NB>();
+    int sa = 0, se = seg0_end, tl = 0;   // current row-tile segment [sa, se) and its ordinal
+    uint32_t uses = 0;                   // bit tb: parity of this issuer's uses of tile buffer tb so far
+    for (int i = e; i < nu; i += NC) {
+      while (i >= se) {
+        sa = se;
+        se = min(nu, se + p.G);
+        ++tl;
+      }
+      const int tb = tl & 1;
+      const bool first = i - NC < sa, last = i + NC >= se;
+      const int a = i % RA, xs = i % RX;
+      // before the first MMA of a tile: the epilogue has read this issuer's
+      // previous tile in the same buffer (if any)
+      bool ok = true;
+      if (first) {
+        if (uses & (4u << tb)) ok = mbar_wait(&dempty[e * 2 + tb], ((uses >> tb) & 1u) ^ 1u);
+        uses = (uses ^ (1u << tb)) | (4u << tb);
+      }
+      ok = ok && mbar_wait(&a_full[a], static_cast<uint32_t>(i / RA) & 1u) &&
+           mbar_wait(&x_full[xs], static_cast<uint32_t>(i / RX) & 1u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 32);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t x0 = smem_u32(xbuf + xs * C::kXBytes);
+      const uint32_t dcol = tmem_d + C::kDCol + (e * 2 + tb) * NB;
+      if (elect_one()) {
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ta(tmem_d + 256 + b * NB, tmem_d + a * 64 + h * 32 + kk * 8,
-                         sw128_desc(x0 + h * NB * 128 + kk * 32), idesc, (h | kk) != 0);
+            umma_bf16_ta(dcol, tmem_d + a * 64 + h * 32 + kk * 8, sw128_desc(x0 + h * NB * 128 + kk * 32), idesc,
+                         (!first || (h | kk) != 0) ? 1u : 0u);
         umma_commit(&x_empty[xs]);
         umma_commit(&a_empty[a]);
-        umma_commit(&dfull[b]);
+        if (last) umma_commit(&dfull[e * 2 + tb]);
       }
+      __syncwarp();
     }
-  } else if (warp >= kTdDeq0 && warp < kTdEpi0) {
-    // ---------------- dequant: thread = (row r, K half h) -> exact (q - z) bf16 into the A ring in
-    // tensor memory: row r = lane of the warp's quadrant, column c holds k = 2c, 2c+1 of the half
-    const int q = warp & 3, h = (warp - kTdDeq0) >> 2;
+  } else if (warp < kTdEpi0) {
+    // ---------------- dequant: group grp takes super-blocks grp, grp + 3, ...;
+    // thread = row r (lane of the warp's quadrant), both K halves -> the
+    // correctly rounded bf16(s16 * (q - z)) into the A slot, column c holding
+    // k = 2c, 2c+1.  s16 = s_hi + s_lo (both bf16, the split exact);
+    // s_lo * (q - z) is exact and fma(s_hi, q - z, s_lo * (q - z)) rounds once.
+    const int q = warp & 3, grp = (warp - kTdDeq0) >> 2;
     const int r = q * 32 + lane;
     const uint32_t trow = static_cast<uint32_t>(q * 32) << 16;
-    // the super-block is read into registers and released, unpacked, then
-    // stored to its A slot once the MMAs of the slot's previous use are done
-    for (int i = 0; i < nu; ++i) {
+    for (int i = grp; i < nu; i += NC) {
       const int j = i % RS, a = i % RA;
       if (!mbar_wait(&sb_full[j], (i / RS) & 1u)) {
         set_status(p.status, FL_ERR_TIMEOUT, 33);
         break;
       }
       const uint8_t* sb = sbuf + j * kSbBytes;
+      const float sf = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
       const uint32_t z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
-      const uint32_t zz = bf16_bias_pair(z);
-      // logical 8-column chunks wl = 8h .. 8h+7 live in word slot p = 4*(wl%4) + wl/4,
-      // i.e. in 16-byte chunk p/4 = wl%4, word p%4 = wl/4
       uint4 cv[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) cv[t] = *reinterpret_cast<const uint4*>(sb + r * 64 + ((t + (r >> 1)) & 3) * 16);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sb_empty[j]);
+      const __nv_bfloat16 shi = __float2bfloat16_rn(sf);
+      const __nv_bfloat16 slo = __float2bfloat16_rn(sf - __bfloat162float(shi));   // exact remainder
+      const uint32_t hi2 = static_cast<uint32_t>(__bfloat16_as_ushort(shi)) * 0x00010001u;
+      const uint32_t lo2 = static_cast<uint32_t>(__bfloat16_as_ushort(slo)) * 0x00010001u;
+      const uint32_t zz = bf16_bias_pair(z);
       uint32_t o[32];
-      // h is uniform across the warp: two static copies keep cv in registers
+      // logical 8-column chunks wl = 8h .. 8h+7 live in 16-byte chunk wl % 4, word wl / 4
       auto unpack = [&](auto H) {
         constexpr int hh = decltype(H)::value;
 #pragma unroll
@@ -1063,70 +1118,84 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_linear_tcdec(const __grid_con
           const int wl = 8 * hh + t;
           const uint32_t word = (&cv[wl & 3].x)[wl >> 2];
 #pragma unroll
-          for (int pi = 0; pi < 4; ++pi) o[4 * t + pi] = bf16x2_sub(nib_pair_bf16(word, pi), zz);
+          for (int pi = 0; pi < 4; ++pi) {
+            const uint32_t qz = bf16x2_sub(nib_pair_bf16(word, pi), zz);
+            o[4 * t + pi] = bfma2(hi2, qz, bmul2(lo2, qz));
+          }
         }
       };
-      if (h == 0)
-        unpack(std::integral_constant<int, 0>());
-      else
-        unpack(std::integral_constant<int, 1>());
+      unpack(std::integral_constant<int, 0>());
       if (i >= RA && !mbar_wait(&a_empty[a], ((i / RA) - 1) & 1u)) {
         set_status(p.status, FL_ERR_TIMEOUT, 36);
         break;
       }
       tc_fence_after();
-      tmem_st32(tmem_d + trow + a * 64 + h * 32, o);
+      tmem_st32(tmem_d + trow + a * 64, o);
+      tmem_wait_st();   // o is rewritten with the second half
+      unpack(std::integral_constant<int, 1>());
+      tmem_st32(tmem_d + trow + a * 64 + 32, o);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[a]);
     }
-  } else if (warp >= kTdEpi0) {
-    // ---------------- epilogue: row r of every super-block, all tokens
+  } else {
+    // ---------------- epilogue: once per row tile, the sum of the issuers'
+    // accumulators (in issuer order) for row r and every token.  A split tile
+    // other than the CTA's last is handed off at once, overlapping the rest of
+    // the stream; the last one at the end.
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    const uint32_t tq = tmem_d + (static_cast<uint32_t>(q * 32) << 16) + C::kDCol;
     pdl_wait();   // y and the workspace: only once the previous kernel is done
-    float tot[NB];
-#pragma unroll
-    for (int m = 0; m < NB; ++m) tot[m] = 0.f;
-    int T = u0 / p.G, owed0 = -1;
+    int T = u0 / p.G, sa = 0, se = seg0_end, owed = -1;
+    uint32_t dph = 0;   // bit b: parity of the next completion of accumulator barrier b
     bool ok = true;
-    for (int i = 0; i < nu; ++i) {
-      const int b = i % RD, j = i % RS;
-      if (!mbar_wait(&dfull[b], (i / RD) & 1u) || !mbar_wait(&sb_full[j], (i / RS) & 1u)) {
-        set_status(p.status, FL_ERR_TIMEOUT, 34);
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const float sc = __half2float(reinterpret_cast<const __half*>(sbuf + j * kSbBytes + kSbNib)[r]);
-      float v[32];
-      tmem_ld32(tmem_d + (static_cast<uint32_t>(q * 32) << 16) + 256 + b * NB, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&dempty[b]);
-        mbar_arrive(&sb_empty[j]);
-      }
+    for (int tl = 0; sa < nu; ++tl) {
+      const int tb = tl & 1, len = se - sa;
+      float tot[NB];
 #pragma unroll
-      for (int m = 0; m < NB; ++m) tot[m] = fmaf(sc, v[m], tot[m]);
-      const int u = u0 + i;
-      if ((u + 1) % p.G == 0 && u + 1 < u1) {
-        if (td_store<NB>(p, T, c, u0, u1, r, tot)) owed0 = T;
+      for (int m = 0; m < NB; ++m) tot[m] = 0.f;
+      for (int e = 0; e < NC; ++e) {
+        // issuer e has super-blocks in [sa, se) iff some i there has i % 3 == e
+        const int off = ((e - sa) % NC + NC) % NC;
+        if (off >= len) continue;
+        const int b = e * 2 + tb;
+        if (!mbar_wait(&dfull[b], (dph >> b) & 1u)) {
+          set_status(p.status, FL_ERR_TIMEOUT, 34);
+          ok = false;
+          break;
+        }
+        dph ^= 1u << b;
+        tc_fence_after();
 #pragma unroll
-        for (int m = 0; m < NB; ++m) tot[m] = 0.f;
-        ++T;
+        for (int hh = 0; hh < NB / 16; ++hh) {
+          uint32_t v[16];
+          tmem_ld16_issue(tq + b * NB + hh * 16, v);
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int m = 0; m < 16; ++m) tot[hh * 16 + m] += __uint_as_float(v[m]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty[b]);
       }
+      if (!ok) break;
+      if (td_store<NB>(p, T, c, u0, u1, r, tot)) {
+        if (se < nu)
+          td_ticket<NB>(p, T, q, lane);
+        else
+          owed = T;
+      }
+      sa = se;
+      se = min(nu, se + p.G);
+      ++T;
     }
-    if (ok && nu > 0) {
-      const bool owed1 = td_store<NB>(p, T, c, u0, u1, r, tot);
-      if (owed0 >= 0) td_ticket<NB>(p, owed0, q, lane);
-      if (owed1) td_ticket<NB>(p, T, q, lane);
-    }
+    if (ok && owed >= 0) td_ticket<NB>(p, owed, q, lane);
   }
   tc_fence_before();
   cta_sync();
-  if (warp == 1) {
+  if (warp == kTdIss0) {
     tc_fence_after();
     tmem_dealloc(tmem_d, C::kTmemCols);
   }
