@@ -237,6 +237,12 @@ __device__ __forceinline__ uint32_t idesc_bf16() {
          (static_cast<uint32_t>(128 >> 4) << 24);
 }
 
+// The same with N chosen at run time (a multiple of 16, 16..256).
+__device__ __forceinline__ uint32_t idesc_bf16_n(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
 // CTA c of P owns units [unit_begin(c), unit_begin(c + 1)) of U; cta_of_unit
 // inverts it.
 __host__ __device__ __forceinline__ int td_unit_begin(int c, int U, int P) {
@@ -1256,12 +1262,15 @@ int launch_tcdec(const void* x, int M, int K, const void* w, int N, void* y, voi
 // Grouped expert GEMM of the MoE layer on tcgen05 (token segments of up to
 // 128 positions of one expert, in expert order).  A tile is (segment s, 128
 // output rows nt); tiles are split over the CTAs as whole tiles (no split-K),
-// so every output element is one fp32 sum written once.  The roles are those
-// of k_gemm_tc with BN = 128: x producer (TMA boxes of the segment's 128
-// position rows, rows past the segment are computed and not stored), weight
-// producer (the segment's expert), MMA issuer, 8 dequant warps, 8 epilogue
-// warps.  Output: fp32 rows of the segment's positions, times wpos[pos] when
-// given (the down projection), else as they are (gate/up).
+// so every output element is one sum written once.  Unit i of a CTA (one
+// super-block of a tile) goes to MMA issuer i % 2 and dequant group i % 2,
+// each issuer accumulating into its own accumulator; the epilogue adds the
+// two in issuer order.  Roles: x producer (the segment's rows rounded up to
+// 32, 64 or 128 by TMA, one box per K half, so that short segments move and
+// multiply only their own rows), weight producer (the segment's expert), two
+// MMA issuers, two dequant groups of four warps, eight epilogue warps.
+// Output: fp32 rows of the segment's positions, times wpos[pos] when given
+// (the down projection), else as they are (gate/up).
 struct MgParams {
   const uint8_t* w;          // routed experts back to back (when wtab is null)
   const uint8_t* const* wtab;  // device table of E expert pointers, or null
@@ -1282,19 +1291,34 @@ constexpr int kMgThreads = 20 * 32;
 
 struct MgCfg {
   static constexpr int BN = 128;
-  static constexpr int kBBox = BN * 64 * 2;     // 16 KB
-  static constexpr int kBStages = 8;
+  static constexpr int kRows = 32;              // the smallest x box (positions)
+  static_assert((kRows << 2) == BN, "box heights 32, 64, 128");
+  static constexpr int kBBox = BN * 64 * 2;     // 16 KB: one K half of a unit's x tile (BN positions x 64 k)
+  static constexpr int kXStage = 2 * kBBox;     // a unit's x tile (its segment's rows), one barrier
+  static constexpr int kBStages = 4;
   static constexpr int kSStages = 8;
   static constexpr int kARing = 4;
-  static constexpr int kSOff = kBStages * kBBox;
+  static constexpr int kSOff = kBStages * kXStage;
   static constexpr int kBarOff = kSOff + kSStages * kSbBytes;
-  static constexpr int kNumBars = 2 * kBStages + 2 * kSStages + 2 * kARing + 2;
+  static constexpr int kNumBars = 2 * kBStages + 2 * kSStages + 2 * kARing + 4;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
-  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmemCols = 512;   // accumulators 2 x BN, A ring 4 x 64
+  static_assert(2 * BN + 64 * kARing <= 512, "tensor memory");
   static_assert(kSmem <= 232448, "shared memory");
+  // unit i goes to MMA issuer and dequant group i % 2: every ring size is
+  // even, so that each barrier has one waiter chain
+  static_assert(kARing % 2 == 0 && kSStages % 2 == 0 && kBStages % 2 == 0, "one chain per slot");
 };
 
-__global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constant__ CUtensorMap xmap, const MgParams p) {
+// x tiles: the segment's positions rounded up to 32, 64 or 128 rows, one TMA
+// box per K half from the tensor map of that box height (xm[0..2])
+struct MgMaps {
+  CUtensorMap xm[3];
+};
+
+__device__ __forceinline__ int mg_rows_kind(int n) { return n <= 32 ? 0 : n <= 64 ? 1 : 2; }
+
+__global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constant__ MgMaps maps, const MgParams p) {
   using C = MgCfg;
   constexpr int BN = C::BN, RA = C::kARing, NBS = C::kBStages, NSS = C::kSStages;
   extern __shared__ uint8_t smem_raw[];
@@ -1305,9 +1329,9 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
   uint64_t* sempty = sfull + NSS;
   uint64_t* afull = sempty + NSS;
   uint64_t* aempty = afull + RA;
-  uint64_t* dfull = aempty + RA;
-  uint64_t* dempty = dfull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + 1);
+  uint64_t* dfull = aempty + RA;   // [issuer]: the issuer's last MMA of the tile done
+  uint64_t* dempty = dfull + 2;    // [issuer]: the epilogue has read that accumulator
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dempty + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -1319,14 +1343,16 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
     }
     for (int i = 0; i < NSS; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sempty[i], 8);
+      mbar_init(&sempty[i], 4);
     }
     for (int i = 0; i < RA; ++i) {
-      mbar_init(&afull[i], 8);
+      mbar_init(&afull[i], 4);
       mbar_init(&aempty[i], 1);
     }
-    mbar_init(dfull, 1);
-    mbar_init(dempty, 8);
+    for (int e = 0; e < 2; ++e) {
+      mbar_init(&dfull[e], 1);
+      mbar_init(&dempty[e], 8);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -1337,7 +1363,7 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
   cta_sync();
   tc_fence_after();
   const uint32_t tmem_d = *tmem_slot;
-  const uint32_t tmem_a = tmem_d + BN;
+  const uint32_t tmem_a = tmem_d + 2 * BN;
   pdl_launch_dependents();
   // the segment plan, the weights' selection and x come from earlier kernels
   pdl_wait();
@@ -1352,18 +1378,21 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
       int j = 0;
       bool ok = true;
       for (int t = t0; t < t1 && ok; ++t) {
-        const int pos0 = p.seg_pos[t / p.TT];
-        for (int g = 0; g < p.G && ok; ++g) {
-          for (int h = 0; h < 2; ++h, ++j) {
-            const int b = j % NBS;
-            if (j >= NBS && !mbar_wait(&bempty[b], static_cast<uint32_t>(j / NBS - 1) & 1u)) {
-              set_status(p.status, FL_ERR_TIMEOUT, 41);
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&bfull[b], C::kBBox);
-            tma_load_2d(smem + b * C::kBBox, &xmap, g * kGroup + 64 * h, pos0, &bfull[b]);
+        const int sg = t / p.TT, pos0 = p.seg_pos[sg];
+        // the segment's rows rounded up to 32, 64 or 128 (the MMA's N)
+        const int kind = mg_rows_kind(p.seg_n[sg]);
+        const CUtensorMap* xmap = &maps.xm[kind];
+        const uint32_t bytes = static_cast<uint32_t>(2 * (C::kRows << kind) * 128);
+        for (int g = 0; g < p.G; ++g, ++j) {
+          const int b = j % NBS;
+          if (j >= NBS && !mbar_wait(&bempty[b], static_cast<uint32_t>(j / NBS - 1) & 1u)) {
+            set_status(p.status, FL_ERR_TIMEOUT, 41);
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(&bfull[b], bytes);
+          tma_load_2d(smem + b * C::kXStage, xmap, g * kGroup, pos0, &bfull[b]);
+          tma_load_2d(smem + b * C::kXStage + C::kBBox, xmap, g * kGroup + 64, pos0, &bfull[b]);
         }
       }
       if (!ok)
@@ -1399,60 +1428,76 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
       if (!ok)
         for (int ii = i > NSS ? i - NSS : 0; ii < i; ++ii) mbar_wait(&sfull[ii % NSS], static_cast<uint32_t>(ii / NSS) & 1u);
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer (one barrier probe per unit: afull certifies the x stages too)
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16<BN>();
-      int jt = 0, a = 0, b = 0;
-      uint32_t aph = 0;
-      for (int i = 0, g = 0; i < nu; ++i) {
-        const bool first = g == 0, last = g == p.G - 1;
-        if ((first && jt > 0 && !mbar_wait(dempty, static_cast<uint32_t>(jt - 1) & 1u)) || !mbar_wait(&afull[a], aph)) {
-          set_status(p.status, FL_ERR_TIMEOUT, 43);
-          break;
-        }
-        tc_fence_after();
+  } else if (warp == 1 || warp == 3) {
+    // ---------------- MMA issuers: issuer e takes units e, e + 2, ... into its
+    // own accumulator.  The whole warp runs the loop; one elected thread
+    // issues.
+    const int e = warp == 1 ? 0 : 1;
+    const uint32_t dcol = tmem_d + e * BN;
+    int g = e, t = t0;               // group of unit i within its tile, and the tile
+    while (g >= p.G) g -= p.G, ++t;
+    uint32_t uses = 0;               // bit 0: parity of the tiles this issuer took part in; bit 1: any
+    for (int i = e; i < nu; i += 2) {
+      const int a = i % RA;
+      const bool first = g < 2, last = g + 2 >= p.G;
+      bool ok = true;
+      if (first) {
+        // the epilogue has read this accumulator's previous tile
+        if (uses & 2u) ok = mbar_wait(&dempty[e], (uses & 1u) ^ 1u);
+        uses = (uses ^ 1u) | 2u;
+      }
+      const int b = i % NBS;
+      // N: the segment's positions rounded up to whole boxes (rows past the
+      // segment are computed and not stored)
+      const uint32_t idesc = idesc_bf16_n(C::kRows << mg_rows_kind(p.seg_n[t / p.TT]));
+      ok = ok && mbar_wait(&afull[a], static_cast<uint32_t>(i / RA) & 1u) &&
+           mbar_wait(&bfull[b], static_cast<uint32_t>(i / NBS) & 1u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) set_status(p.status, FL_ERR_TIMEOUT, 43);
+        break;
+      }
+      tc_fence_after();
+      if (elect_one()) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t b0 = smem_u32(smem + b * C::kBBox);
+          const uint32_t b0 = smem_u32(smem + b * C::kXStage + h * C::kBBox);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16_ta(tmem_d, tmem_a + a * 64 + h * 32 + kk * 8, sw128_desc(b0 + kk * 32), idesc,
+            umma_bf16_ta(dcol, tmem_a + a * 64 + h * 32 + kk * 8, sw128_desc(b0 + kk * 32), idesc,
                          (!first || h != 0 || kk != 0) ? 1u : 0u);
-          umma_commit(&bempty[b]);
-          if (++b == NBS) b = 0;
         }
+        umma_commit(&bempty[b]);
         umma_commit(&aempty[a]);
-        if (++a == RA) a = 0, aph ^= 1u;
-        if (last) {
-          umma_commit(dfull);
-          ++jt;
-        }
-        if (++g == p.G) g = 0;
+        if (last) umma_commit(&dfull[e]);
       }
+      __syncwarp();
+      g += 2;
+      while (g >= p.G) g -= p.G, ++t;
     }
   } else if (warp >= kPfDeq0 && warp < kPfEpi0) {
-    // ---------------- dequant (as k_gemm_tc): exact bf16(s16 * (q - z)) into the A ring
-    const int q = warp & 3, h = (warp - kPfDeq0) >> 2;
+    // ---------------- dequant: group grp takes units grp, grp + 2, ...;
+    // thread = row r, both K halves -> exact bf16(s16 * (q - z)) into the A
+    // ring (s16 = s_hi + s_lo, both bf16, the split exact; s_lo * (q - z) is
+    // exact and fma(s_hi, q - z, s_lo * (q - z)) rounds once)
+    const int q = warp & 3, grp = (warp - kPfDeq0) >> 2;
     const int r = q * 32 + lane;
     const uint32_t trow = static_cast<uint32_t>(q * 32) << 16;
-    for (int i = 0; i < nu; ++i) {
+    for (int i = grp; i < nu; i += 2) {
       const int sI = i % NSS, a = i % RA;
       // groups of 64: the upper K half takes the odd group's scale and zero
       // point from the expert's side entry (read before the wait)
-      const bool odd = p.side_off != 0 && h == 1;
-      float sf = 0.f;
-      uint32_t z = 0;
-      bool odd_ok = false;
-      if (odd) {
+      float sf1 = 0.f;
+      uint32_t z1 = 0;
+      bool side_ok = false;
+      if (p.side_off != 0) {
         const int t = t0 + i / p.G, g = i - (i / p.G) * p.G;
         const int sg = t / p.TT, nt = t - sg * p.TT, e = p.seg_e[sg];
         const uint8_t* base = e == p.E ? p.w_shared : expert_base(p.w, p.wtab, p.wbytes, e, p.status);
         if (base) {
           const uint8_t* sd = base + p.side_off + (static_cast<size_t>(nt) * p.G + g) * kSbSide;
-          sf = __half2float(__ldg(reinterpret_cast<const __half*>(sd) + r));
-          z = (__ldg(sd + kSbScale + (r >> 1)) >> ((r & 1) * 4)) & 15u;
-          odd_ok = true;
+          sf1 = __half2float(__ldg(reinterpret_cast<const __half*>(sd) + r));
+          z1 = (__ldg(sd + kSbScale + (r >> 1)) >> ((r & 1) * 4)) & 15u;
+          side_ok = true;
         }
       }
       if (!mbar_wait(&sfull[sI], static_cast<uint32_t>(i / NSS) & 1u)) {
@@ -1460,23 +1505,26 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
         break;
       }
       const uint8_t* sb = smem + C::kSOff + sI * kSbBytes;
-      if (!odd_ok) {
-        sf = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
-        z = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
+      const float sf0 = __half2float(reinterpret_cast<const __half*>(sb + kSbNib)[r]);
+      const uint32_t z0 = (sb[kSbNib + kSbScale + (r >> 1)] >> ((r & 1) * 4)) & 15u;
+      if (!side_ok) {
+        sf1 = sf0;
+        z1 = z0;
       }
       uint4 cv[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) cv[t] = *reinterpret_cast<const uint4*>(sb + r * 64 + ((t + (r >> 1)) & 3) * 16);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sI]);
-      const __nv_bfloat16 shi = __float2bfloat16_rn(sf);
-      const __nv_bfloat16 slo = __float2bfloat16_rn(sf - __bfloat162float(shi));
-      const uint32_t hi2 = static_cast<uint32_t>(__bfloat16_as_ushort(shi)) * 0x00010001u;
-      const uint32_t lo2 = static_cast<uint32_t>(__bfloat16_as_ushort(slo)) * 0x00010001u;
-      const uint32_t zz = bf16_bias_pair(z);
       uint32_t o[32];
-      auto unpack = [&](auto H) {
+      // half hh of the row with scale sf and zero point z
+      auto unpack = [&](auto H, float sf, uint32_t z) {
         constexpr int hh = decltype(H)::value;
+        const __nv_bfloat16 shi = __float2bfloat16_rn(sf);
+        const __nv_bfloat16 slo = __float2bfloat16_rn(sf - __bfloat162float(shi));
+        const uint32_t hi2 = static_cast<uint32_t>(__bfloat16_as_ushort(shi)) * 0x00010001u;
+        const uint32_t lo2 = static_cast<uint32_t>(__bfloat16_as_ushort(slo)) * 0x00010001u;
+        const uint32_t zz = bf16_bias_pair(z);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const int wl = 8 * hh + t;
@@ -1488,58 +1536,72 @@ __global__ void __launch_bounds__(kMgThreads, 1) k_moe_gemm(const __grid_constan
           }
         }
       };
-      if (h == 0)
-        unpack(std::integral_constant<int, 0>());
-      else
-        unpack(std::integral_constant<int, 1>());
+      unpack(std::integral_constant<int, 0>(), sf0, z0);
       if (i >= RA && !mbar_wait(&aempty[a], static_cast<uint32_t>(i / RA - 1) & 1u)) {
         set_status(p.status, FL_ERR_TIMEOUT, 45);
         break;
       }
       tc_fence_after();
-      tmem_st32(tmem_a + trow + a * 64 + h * 32, o);
+      tmem_st32(tmem_a + trow + a * 64, o);
+      tmem_wait_st();   // o is rewritten with the second half
+      unpack(std::integral_constant<int, 1>(), sf1, z1);
+      tmem_st32(tmem_a + trow + a * 64 + 32, o);
       tmem_wait_st();
-      if (!mbar_wait(&bfull[(2 * i) % NBS], static_cast<uint32_t>((2 * i) / NBS) & 1u) ||
-          !mbar_wait(&bfull[(2 * i + 1) % NBS], static_cast<uint32_t>((2 * i + 1) / NBS) & 1u)) {
-        set_status(p.status, FL_ERR_TIMEOUT, 46);
-        break;
-      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[a]);
     }
   } else if (warp >= kPfEpi0) {
-    // ---------------- epilogue: rows q*32+lane of the tile, one half of its 128 positions
-    const int e = warp - kPfEpi0, q = warp & 3;
+    // ---------------- epilogue: rows q*32+lane of the tile, one half of its
+    // 128 positions; the two issuers' accumulators added in issuer order
+    const int ew = warp - kPfEpi0, q = warp & 3;
     const int r = q * 32 + lane;
-    const int col0 = (e >> 2) * (BN / 2);
+    const int col0 = (ew >> 2) * (BN / 2);
     const uint32_t tcol = tmem_d + (static_cast<uint32_t>(q * 32) << 16) + col0;
-    auto release_d = [&]() {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dempty);
-    };
+    uint32_t dph = 0;   // bit e: parity of the next completion of dfull[e]
     int jt = 0;
     for (int t = t0; t < t1; ++t, ++jt) {
-      if (!mbar_wait(dfull, static_cast<uint32_t>(jt) & 1u)) {
+      // issuer e took part in the tile unless it has a single unit of the other parity
+      const bool has0 = p.G >= 2 || ((jt * p.G) & 1) == 0;
+      const bool has1 = p.G >= 2 || ((jt * p.G) & 1) == 1;
+      if ((has0 && !mbar_wait(&dfull[0], dph & 1u)) || (has1 && !mbar_wait(&dfull[1], (dph >> 1) & 1u))) {
         set_status(p.status, FL_ERR_TIMEOUT, 47);
         break;
       }
+      dph ^= (has0 ? 1u : 0u) | (has1 ? 2u : 0u);
       tc_fence_after();
       const int sg = t / p.TT, nt = t - sg * p.TT;
       const int pos0 = p.seg_pos[sg], n = p.seg_n[sg];
       const int col = nt * kRowTile + r;
-      pf_drain<BN / 32>(tcol, release_d, [&](int k, const float (&v)[16]) {
+#pragma unroll
+      for (int k = 0; k < BN / 32; ++k) {
+        uint32_t ra[16], rb[16];
+        const bool live = col0 + 16 * k < n;   // columns past the segment were not computed for this tile
+        if (live && has0) tmem_ld16_issue(tcol + 16 * k, ra);
+        if (live && has1) tmem_ld16_issue(tcol + BN + 16 * k, rb);
+        if (live && has0) tmem_ld_wait(ra);
+        if (live && has1) tmem_ld_wait(rb);
+        if (k == BN / 32 - 1) {
+          // every read of both accumulators is done: the next tile's MMAs may start
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (has0) mbar_arrive(&dempty[0]);
+            if (has1) mbar_arrive(&dempty[1]);
+          }
+        }
 #pragma unroll
         for (int tt = 0; tt < 16; ++tt) {
+          const float v = has0 ? (has1 ? __uint_as_float(ra[tt]) + __uint_as_float(rb[tt]) : __uint_as_float(ra[tt]))
+                               : __uint_as_float(rb[tt]);
           const int m = col0 + 16 * k + tt;
           if (m < n) {
             const int pos = pos0 + m;
             const float sc = p.wpos ? p.wpos[pos] : 1.f;
-            p.out[static_cast<size_t>(pos) * p.ldo + col] = sc * v[tt];
+            p.out[static_cast<size_t>(pos) * p.ldo + col] = sc * v;
           }
         }
-      });
+      }
     }
   }
   tc_fence_before();
@@ -1581,15 +1643,17 @@ int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* const
                 cudaStream_t s) {
   auto enc = encode_fn();
   if (!enc) return FL_ERR_CUDA;
-  CUtensorMap map;
+  MgMaps maps;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(npos)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(MgCfg::BN)};
   const cuuint32_t estr[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return FL_ERR_CUDA;
+  for (int kind = 0; kind < 3; ++kind) {
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(MgCfg::kRows << kind)};
+    if (enc(&maps.xm[kind], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FL_ERR_CUDA;
+  }
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1626,6 +1690,6 @@ int fl_moe_gemm(const void* x, int npos, int K, const void* w, const void* const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, k_moe_gemm, map, p) != cudaSuccess) return FL_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, k_moe_gemm, maps, p) != cudaSuccess) return FL_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FL_OK : FL_ERR_CUDA;
 }
