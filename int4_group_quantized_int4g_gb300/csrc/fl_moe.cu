@@ -908,43 +908,62 @@ __global__ void __launch_bounds__(kThreads, 2) k_moe_rows(const MoeRowsParams p)
 }
 
 // ------------------------------------------------------------------ combine
+// Four columns per thread; each output sums its slots in slot order.
 __global__ void k_moe_combine(const float* __restrict__ out, const int32_t* __restrict__ inv, int M, int k, int H,
                               int has_shared, __nv_bfloat16* __restrict__ y) {
   const int t = blockIdx.y;
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (t >= M || n >= H) return;
   pdl_wait();
-  float acc = 0.f;
-  for (int j = 0; j < k; ++j) acc += out[static_cast<size_t>(inv[t * k + j]) * H + n];
-  if (has_shared) acc += out[static_cast<size_t>(M * k + t) * H + n];
-  y[static_cast<size_t>(t) * H + n] = __float2bfloat16_rn(acc);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const float4 v = *reinterpret_cast<const float4*>(out + static_cast<size_t>(inv[t * k + j]) * H + n);
+    acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+  }
+  if (has_shared) {
+    const float4 v = *reinterpret_cast<const float4*>(out + static_cast<size_t>(M * k + t) * H + n);
+    acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+  }
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 st;
+  st.x = *reinterpret_cast<const uint32_t*>(&lo);
+  st.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(y + static_cast<size_t>(t) * H + n) = st;
 }
 
 // ------------------------------------------------------------------ gather / SwiGLU (grouped-GEMM path)
-// xp[pos] = x[token of pos], 16 bytes per thread.
+// xp[pos] = x[token of pos], 16 bytes per thread (32-bit indices: the host
+// checks npos * H / 8 < 2^31).
 __global__ void k_moe_gather(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ tok_of_pos, int npos,
                              int H, __nv_bfloat16* __restrict__ xp) {
   pdl_wait();
   const int per_row = H / 8;
-  const long long total = static_cast<long long>(npos) * per_row;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int pos = static_cast<int>(i / per_row), c = static_cast<int>(i - static_cast<long long>(pos) * per_row);
+  const int total = npos * per_row;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int pos = i / per_row, c = i - pos * per_row;
     const int t = tok_of_pos[pos];
     reinterpret_cast<uint4*>(xp + static_cast<size_t>(pos) * H)[c] =
         reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H)[c];
   }
 }
 
-// h[pos, i] = bf16(silu(gu[pos, i]) * gu[pos, I + i]), gate rows first.
+// h[pos, i] = bf16(silu(gu[pos, i]) * gu[pos, I + i]), gate rows first; four
+// columns per thread (32-bit indices: the host checks npos * I / 4 < 2^31).
 __global__ void k_moe_swiglu(const float* __restrict__ gu, int npos, int I, __nv_bfloat16* __restrict__ h) {
   pdl_wait();
-  const long long total = static_cast<long long>(npos) * I;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int pos = static_cast<int>(i / I), c = static_cast<int>(i - static_cast<long long>(pos) * I);
-    const float g = gu[static_cast<size_t>(pos) * 2 * I + c], u = gu[static_cast<size_t>(pos) * 2 * I + I + c];
-    h[i] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
+  const int q4 = I / 4;
+  const int total = npos * q4;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int pos = i / q4, c = (i - pos * q4) * 4;
+    const float* row = gu + static_cast<size_t>(pos) * 2 * I;
+    const float4 g = *reinterpret_cast<const float4*>(row + c);
+    const float4 u = *reinterpret_cast<const float4*>(row + I + c);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(g.x / (1.f + expf(-g.x)) * u.x, g.y / (1.f + expf(-g.y)) * u.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(g.z / (1.f + expf(-g.z)) * u.z, g.w / (1.f + expf(-g.w)) * u.w);
+    uint2 st;
+    st.x = *reinterpret_cast<const uint32_t*>(&lo);
+    st.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(h + static_cast<size_t>(pos) * I + c) = st;
   }
 }
 
@@ -1161,6 +1180,9 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
   }
   const int n = M * k, npos = n + (has_shared ? M : 0);
   if (L.gemm) {
+    // the element-wise kernels index with 32 bits
+    if (static_cast<long long>(npos) * (H / 8) >= (1LL << 31) || static_cast<long long>(npos) * (I / 4) >= (1LL << 31))
+      return FL_ERR_UNSUPPORTED;
     const int32_t* sege = reinterpret_cast<const int32_t*>(W + L.sege);
     const int32_t* segp = reinterpret_cast<const int32_t*>(W + L.segp);
     const int32_t* segn = reinterpret_cast<const int32_t*>(W + L.segn);
@@ -1246,7 +1268,7 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     if (launch_pdl(kern, dim3(L.P), dim3(kThreads), smem, s, p) != cudaSuccess) return FL_ERR_CUDA;
   }
   // combine
-  if (launch_pdl(k_moe_combine, dim3((H + 255) / 256, M), dim3(256), 0, s,
+  if (launch_pdl(k_moe_combine, dim3((H / 4 + 255) / 256, M), dim3(256), 0, s,
                  reinterpret_cast<const float*>(W + L.out), reinterpret_cast<const int32_t*>(W + L.inv), M, k, H,
                  has_shared, static_cast<__nv_bfloat16*>(y)) != cudaSuccess)
     return FL_ERR_CUDA;
