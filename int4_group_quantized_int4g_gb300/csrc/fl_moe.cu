@@ -383,10 +383,13 @@ __global__ void __launch_bounds__(1024, 1) k_moe_permute(const PermuteArgs a) {
       a.seg_n[si] = min(a.seg_rows, a.M - s * a.seg_rows);
     }
   }
-  // zero the ticket counters the grouped kernels will use
+  // zero the ticket counters the grouped rows kernels will use (the grouped
+  // GEMM takes none: null)
   const int nseg = nch[E] + (a.has_shared ? (a.M + a.seg_rows - 1) / a.seg_rows : 0);
-  for (int i = tid; i < nseg * a.TT13 * kConsumerWarps; i += blockDim.x) a.cnt13[i] = 0;
-  for (int i = tid; i < nseg * a.TT2 * kConsumerWarps; i += blockDim.x) a.cnt2[i] = 0;
+  if (a.cnt13) {
+    for (int i = tid; i < nseg * a.TT13 * kConsumerWarps; i += blockDim.x) a.cnt13[i] = 0;
+    for (int i = tid; i < nseg * a.TT2 * kConsumerWarps; i += blockDim.x) a.cnt2[i] = 0;
+  }
 }
 
 // ------------------------------------------------------------------ grouped rows
@@ -1161,8 +1164,8 @@ static int moe_layer(const void* x, const float* logits, int M, int H, int E, in
     a.seg_pos = reinterpret_cast<int32_t*>(W + L.segp);
     a.seg_n = reinterpret_cast<int32_t*>(W + L.segn);
     a.plan = plan;
-    a.cnt13 = reinterpret_cast<int32_t*>(W + L.cnt13);
-    a.cnt2 = reinterpret_cast<int32_t*>(W + L.cnt2);
+    a.cnt13 = L.gemm ? nullptr : reinterpret_cast<int32_t*>(W + L.cnt13);
+    a.cnt2 = L.gemm ? nullptr : reinterpret_cast<int32_t*>(W + L.cnt2);
     a.user_offsets = expert_offsets;
     a.user_perm = perm;
     const size_t smem = 4ull * (32 * E + M * k + 2 * (E + 1));
