@@ -10,7 +10,8 @@
 //   k_moe_permute  one CTA: stable counting sort of the M*k assignments by
 //                  expert, token segments of <= 8 rows per expert (the shared
 //                  expert is one more expert holding every token with weight
-//                  1), the device-side work plan, zeroed ticket counters
+//                  1), the device-side work plan, and (for the grouped
+//                  rows kernels) zeroed ticket counters
 //   k_moe_rows<0>  grouped gate/up: h = silu(G x) * (U x), bf16 [pos, I]
 //   k_moe_rows<1>  grouped down: out = w_pos * (W2 h), fp32 [pos, H]
 //   k_moe_combine  y[t] = sum_j out[slot (t,j)] + shared out[t], bf16
