@@ -982,14 +982,15 @@ struct MoeLayout {
 };
 
 // Many tokens per expert: the grouped steps run on the tensor-memory GEMM
-// above 8 positions per expert on average.  Up to 8 the rows kernels win,
-// although an expert with more than 8 positions streams its weights once per
-// segment of 8 (measured on the Qwen3- and DeepSeek-V3-shaped layers: at 8
-// positions per expert the rows kernels take 0.75-0.9 of the GEMM's time, at
-// 16 about 1.1-1.5 times it).
+// above 8 positions per expert on average, or from 4 when the hidden size is
+// at least 4096.  Below that the rows kernels win, although an expert with
+// more than 8 positions streams its weights once per segment of 8 (measured:
+// at 4 positions per expert the GEMM takes 0.95 of the rows kernels' time on
+// the DeepSeek-V3-shaped layer, H = 7168, and 1.28 times it on the
+// Qwen3-shaped one, H = 2048).
 bool moe_uses_gemm(int M, int E, int k, int H) {
   const long long n = static_cast<long long>(M) * k;
-  return n > 8LL * E;
+  return n > 8LL * E || (H >= 4096 && n >= 4LL * E);
 }
 
 bool moe_layout(int M, int E, int k, int H, int I, int has_shared, int sms, MoeLayout* L, bool g64 = false) {
