@@ -1245,6 +1245,13 @@ int launch_tcdec(const void* x, int M, int K, const void* w, int N, void* y, voi
   p.U = p.T * p.G;
   const int sms = flh::sm_count();
   p.P = p.U < sms ? p.U : sms;
+  // Few row tiles: P = T * s with s = SMs / T, so that the contiguous ranges
+  // are s equal parts of each tile (K=4096, N=4096, M=32: 10.8 against 9.0
+  // us); the partial slots (P + T of them) stay within the workspace.
+  if (p.T * 2 <= sms) {
+    const int sp = sms / p.T;
+    p.P = p.T * (sp < p.G ? sp : p.G);
+  }
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
