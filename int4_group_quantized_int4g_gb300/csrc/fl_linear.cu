@@ -58,6 +58,12 @@ struct RowsParams {
   unsigned long long red_wait_ns;  // bound of rank 0's wait for its peers' partial sums
   int withhold;      // test hook: the reduction barrier expects one arrival nobody makes
   const uint8_t* w_up;   // GLU: the up matrix (w is the gate); y receives h = silu(gate) * up
+  // > 0 (cluster mode, M <= 8): the x rows of the CTA's whole K slice sit at
+  // shared-memory offset xr_off, token m's at m * xr_stride, filled once by
+  // the consumer warps; the stages then hold weights only.  0: each stage
+  // carries its groups' x rows (kXRowStride apart), copied by the producer.
+  int xr_stride;
+  uint32_t xr_off;
 };
 
 // CTA c owns units [unit_begin(c), unit_begin(c+1)); cta_of_unit inverts it.
@@ -297,7 +303,9 @@ __device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem,
   constexpr int Mp = 8 * NT;
   constexpr int XS = G64 ? 2 : 1;          // token sums per group slot: one per 64-column group
   const uint32_t xoff = UPS * kSbBytes;
-  const uint32_t soff = xoff + UPS * p.M * kXRowStride;   // G64: the stage's side entries
+  const bool xr = CL && p.xr_stride > 0;   // x from the CTA's x region, not from the stage
+  const uint32_t soff = xoff + (xr ? 0 : UPS * p.M * kXRowStride);   // G64: the stage's side entries
+  const int xstride = xr ? p.xr_stride : kXRowStride;
   const int gid = lane >> 2, tig = lane & 3;
   const int r0 = warp * 16 + gid;
   const uint8_t* xzero = smem + p.zrow_off;
@@ -326,16 +334,20 @@ __device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem,
     // of the range holds stale shared memory and its result is dropped.
 #pragma unroll
     for (int i = 0; i < UPS; ++i) {
+      // cluster mode: group slot = unit index in the range (a slot past its
+      // end reads the last group's x: in bounds, and its result is dropped)
+      const uint8_t* sx = xr ? smem + p.xr_off + min(k * UPS + i, nslot - 1) * 256
+                             : sb + xoff + i * p.M * kXRowStride;
       if constexpr (G64) {
         float s0[2], s1[2];
         uint32_t z0[2], z1[2];
-        unit_dot64<NT, FOLD, true>(sb + i * kSbBytes, sb + soff + i * kSbSide, sb + xoff + i * p.M * kXRowStride, p.M,
-                                   r0, gid, tig, acc[i], s0, s1, z0, z1, NT, xzero);
+        unit_dot64<NT, FOLD, true>(sb + i * kSbBytes, sb + soff + i * kSbSide, sx, p.M, r0, gid, tig, acc[i], s0, s1,
+                                   z0, z1, NT, xzero, xstride);
 #pragma unroll
         for (int hh = 0; hh < XS; ++hh) sc[i][hh][0] = s0[hh], sc[i][hh][1] = s1[hh], zr[i][hh][0] = z0[hh], zr[i][hh][1] = z1[hh];
       } else {
-        unit_dot<NT, FOLD, true>(sb + i * kSbBytes, sb + xoff + i * p.M * kXRowStride, p.M, r0, gid, tig, acc[i][0],
-                                 sc[i][0][0], sc[i][0][1], zr[i][0][0], zr[i][0][1], NT, xzero);
+        unit_dot<NT, FOLD, true>(sb + i * kSbBytes, sx, p.M, r0, gid, tig, acc[i][0], sc[i][0][0], sc[i][0][1],
+                                 zr[i][0][0], zr[i][0][1], NT, xzero, xstride);
       }
     }
     __syncwarp();
@@ -423,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
   const uint32_t xoff = UPS * kSbBytes;           // x slices follow the super-blocks
   const int g0 = u0 % p.G;
   const int nslot = (u1 - u0) < p.G ? (u1 - u0) : p.G;   // distinct groups, from g0 on (mod G)
+  const bool xr = !GLU && p.csize > 1 && p.xr_stride > 0;   // x region (cluster mode): no x in the stages
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -456,15 +469,17 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
       const int ua = u0 + k * UPS, n = min(UPS, u1 - ua);
       if (lane == 0) {
         uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(n) * (kSbBytes + p.M * 256u + (G64 ? kSbSide : 0)));
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(n) * (kSbBytes + (xr ? 0u : p.M * 256u) +
+                                                                      (G64 ? kSbSide : 0)));
         bulk_g2s_hint(st, p.w + static_cast<size_t>(ua) * kSbBytes, static_cast<uint32_t>(n) * kSbBytes, &full[slot],
                       pol);
         if (G64)
-          bulk_g2s_hint(st + xoff + UPS * p.M * kXRowStride, p.side + static_cast<size_t>(ua) * kSbSide,
+          bulk_g2s_hint(st + xoff + (xr ? 0 : UPS * p.M * kXRowStride), p.side + static_cast<size_t>(ua) * kSbSide,
                         static_cast<uint32_t>(n) * kSbSide, &full[slot], pol);
       }
     };
     auto issue_x = [&](int k, int slot) {   // the M token rows' slices of stage k's groups
+      if (xr) return;   // the consumers fill the x region instead
       const int ua = GLU ? u0 + k : u0 + k * UPS, n = GLU ? 1 : min(UPS, u1 - ua);
       uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes + xoff;
       for (int idx = lane; idx < n * p.M; idx += 32) {
@@ -524,6 +539,12 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
         uint4 q[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) q[t] = __ldg(src + t);
+        if (xr) {   // these 64 bytes of x into the region: token m, group slot i
+          uint4* dst = reinterpret_cast<uint4*>(smem + p.xr_off + static_cast<size_t>(m) * p.xr_stride + i * 256) +
+                       part * 4;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) dst[t] = q[t];
+        }
         float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -565,8 +586,8 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
 
 // ------------------------------------------------------------------ plan
 struct RowsPlan {
-  int T, G, P, NT, ups, stages, U, csize, minb;
-  uint32_t stage_bytes, red_off, zrow_off;
+  int T, G, P, NT, ups, stages, U, csize, minb, xr_stride;
+  uint32_t stage_bytes, red_off, zrow_off, xr_off;
   size_t smem, cnt_off, part_off, ws_bytes;
 };
 
@@ -613,19 +634,43 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bo
       pl->csize > 1
           ? 16 + static_cast<size_t>(pl->csize - 1) * kConsumerWarps * 32 * 4 * pl->NT * (glu ? 2 : 1) * sizeof(float)
           : 0;
-  pl->stage_bytes = static_cast<uint32_t>(align_up(
-      glu ? 2 * static_cast<size_t>(kSbBytes) + static_cast<size_t>(M) * kXRowStride
-          : static_cast<size_t>(pl->ups) * (kSbBytes + static_cast<size_t>(M) * kXRowStride + (g64 ? kSbSide : 0)),
-      128));
-  const size_t budget = (pl->minb == 3 ? 66u * 1024u : pl->minb == 2 ? 100u * 1024u : 200u * 1024u) - red_bytes;
-  int stages = static_cast<int>(budget / pl->stage_bytes);
-  pl->stages = stages > 12 ? 12 : (stages < 2 ? 2 : stages);
   const int units_max = pl->csize > 1 ? (pl->G + pl->csize - 1) / pl->csize : (pl->U + pl->P - 1) / pl->P;
   const int nslot = units_max < pl->G ? units_max : pl->G;
-  pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes + 2 * pl->stages * sizeof(uint64_t) +
-             static_cast<size_t>(nslot) * (g64 ? 2 : 1) * 8 * pl->NT * sizeof(float);
+  const size_t xsum_bytes = static_cast<size_t>(nslot) * (g64 ? 2 : 1) * 8 * pl->NT * sizeof(float);
+  // Cluster mode with one token tile: the x rows of a rank's K slice (one
+  // contiguous run of groups) are loaded once, by the token-sum prologue,
+  // into an x region; the stages then carry weights only and the producer
+  // issues one weight copy per stage instead of one more 256-byte copy per
+  // token and group (QKV, M=8: 12.9 to ~10.5 us a launch).  Rows are an odd
+  // multiple of 64 bytes apart: conflict-free B-fragment loads.
+  for (int xr = (pl->csize > 1 && pl->NT == 1 && !glu) ? 1 : 0; xr >= 0; --xr) {
+    pl->xr_stride = xr ? nslot * 256 + 64 : 0;
+    const size_t xr_bytes = static_cast<size_t>(M) * pl->xr_stride;
+    pl->stage_bytes = static_cast<uint32_t>(align_up(
+        glu ? 2 * static_cast<size_t>(kSbBytes) + static_cast<size_t>(M) * kXRowStride
+            : static_cast<size_t>(pl->ups) *
+                  (kSbBytes + (xr ? 0 : static_cast<size_t>(M) * kXRowStride) + (g64 ? kSbSide : 0)),
+        128));
+    long long stages;
+    if (pl->minb == 2) {
+      // two CTAs per SM: 113 KB each, of which the ring takes the rest (256
+      // bytes of zero row, 256 of alignment slack)
+      const long long fixed = static_cast<long long>(xsum_bytes + 256 + 256 + xr_bytes + red_bytes);
+      stages = (113LL * 1024 - fixed) / static_cast<long long>(pl->stage_bytes + 2 * sizeof(uint64_t));
+    } else {
+      stages = (static_cast<long long>(pl->minb == 3 ? 66u * 1024u : 200u * 1024u) -
+                static_cast<long long>(red_bytes + xr_bytes)) /
+               static_cast<long long>(pl->stage_bytes);
+    }
+    if (xr && stages < 3) continue;   // too little room left for the ring: x in the stages
+    pl->stages = stages > 12 ? 12 : (stages < 2 ? 2 : static_cast<int>(stages));
+    break;
+  }
+  pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes + 2 * pl->stages * sizeof(uint64_t) + xsum_bytes;
   pl->zrow_off = static_cast<uint32_t>(align_up(pl->smem, 16));
   pl->smem = pl->zrow_off + 256;
+  pl->xr_off = static_cast<uint32_t>(align_up(pl->smem, 128));
+  if (pl->xr_stride) pl->smem = pl->xr_off + static_cast<size_t>(M) * pl->xr_stride;
   pl->red_off = static_cast<uint32_t>(align_up(pl->smem, 16));
   if (red_bytes) pl->smem = pl->red_off + red_bytes;
   pl->cnt_off = kTicketOff;
@@ -766,6 +811,8 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
   prm.csize = pl.csize;
   prm.red_off = pl.red_off;
   prm.zrow_off = pl.zrow_off;
+  prm.xr_stride = pl.xr_stride;
+  prm.xr_off = pl.xr_off;
   const long long hook = g_withhold_ns.load();
   prm.withhold = (hook >= 0 && pl.csize > 1) ? 1 : 0;
   prm.red_wait_ns = prm.withhold ? static_cast<unsigned long long>(hook) : kWaitLimitNs;
@@ -819,6 +866,8 @@ int fl_linear_glu(const void* x, int M, int H, const void* w_gate, const void* w
   prm.csize = pl.csize;
   prm.red_off = pl.red_off;
   prm.zrow_off = pl.zrow_off;
+  prm.xr_stride = pl.xr_stride;
+  prm.xr_off = pl.xr_off;
   const long long hook = g_withhold_ns.load();
   prm.withhold = hook >= 0 ? 1 : 0;
   prm.red_wait_ns = prm.withhold ? static_cast<unsigned long long>(hook) : kWaitLimitNs;

@@ -26,10 +26,12 @@ constexpr int kXRowStride = 320;  // 256 B of x per staged row + 64 B pad: confl
 // second chain would cost a merge and its own zeroing per super-block.
 // ZROW: lanes whose token m >= M read their B fragment from `xzero` (256
 // zero bytes in shared memory) instead of zero-filling registers per step.
+// xstride: bytes between the x rows of consecutive tokens in `sx` (a
+// multiple of 16, and an odd multiple of 64 for conflict-free loads).
 template <int NT, bool FOLD, bool ZROW = false>
 __device__ __forceinline__ void unit_dot(const uint8_t* sb, const uint8_t* sx, int M, int r0, int gid, int tig,
                                          float (&acc)[NT][4], float& s0, float& s1, uint32_t& z0, uint32_t& z1,
-                                         int ntiles = NT, const uint8_t* xzero = nullptr) {
+                                         int ntiles = NT, const uint8_t* xzero = nullptr, int xstride = kXRowStride) {
   // chunk tig of rows r0 and r0+8 (both rotated by (r0/2)%4 in the layout)
   const int pos = ((tig + (r0 >> 1)) & 3) * 16;
   const uint4 wa = *reinterpret_cast<const uint4*>(sb + r0 * 64 + pos);
@@ -49,7 +51,7 @@ __device__ __forceinline__ void unit_dot(const uint8_t* sb, const uint8_t* sx, i
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int m = nt * 8 + gid;
-    xrow[nt] = (!ZROW || m < M) ? sx + m * kXRowStride : xzero;
+    xrow[nt] = (!ZROW || m < M) ? sx + m * xstride : xzero;
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -91,7 +93,7 @@ template <int NT, bool FOLD, bool ZROW = false>
 __device__ __forceinline__ void unit_dot64(const uint8_t* sb, const uint8_t* side, const uint8_t* sx, int M, int r0,
                                            int gid, int tig, float (&acc)[2][NT][4], float (&s0)[2], float (&s1)[2],
                                            uint32_t (&z0)[2], uint32_t (&z1)[2], int ntiles = NT,
-                                           const uint8_t* xzero = nullptr) {
+                                           const uint8_t* xzero = nullptr, int xstride = kXRowStride) {
   const int pos = ((tig + (r0 >> 1)) & 3) * 16;
   const uint4 wa = *reinterpret_cast<const uint4*>(sb + r0 * 64 + pos);
   const uint4 wb = *reinterpret_cast<const uint4*>(sb + (r0 + 8) * 64 + pos);
@@ -116,7 +118,7 @@ __device__ __forceinline__ void unit_dot64(const uint8_t* sb, const uint8_t* sid
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int m = nt * 8 + gid;
-    xrow[nt] = (!ZROW || m < M) ? sx + m * kXRowStride : xzero;
+    xrow[nt] = (!ZROW || m < M) ? sx + m * xstride : xzero;
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
