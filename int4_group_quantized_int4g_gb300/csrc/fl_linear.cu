@@ -215,8 +215,9 @@ __device__ __forceinline__ void cluster_reduce(const RowsParams& p, int T, int r
 // = unit index in the range, no tile boundaries); otherwise a stream-K range
 // that may cross row tiles, finished through the ticket hand-off.
 // GLU (the gate/up half of a decode MLP block, M <= 8, cluster mode): each
-// stage holds the gate and the up super-block of one (row tile, group) and
-// that group's x rows; two folded sums per row; rank 0 of the cluster adds
+// stage holds the gate and the up super-block of one (row tile, group) (and
+// that group's x rows when there is no x region); two folded sums per row;
+// rank 0 of the cluster adds
 // the ranks' gate and up sums in rank order and stores h = silu(gate) * up.
 __device__ __forceinline__ void glu_reduce(const RowsParams& p, int T, int rank, int warp, int lane,
                                            const float (&tg)[4], const float (&tu)[4], uint64_t* red_bar,
@@ -274,11 +275,14 @@ __device__ __forceinline__ void rows_consume_glu(const RowsParams& p, uint8_t* s
       return;
     }
     const uint8_t* sb = smem + static_cast<size_t>(s) * p.stage_bytes;
+    // unit k's x rows: the x region (slot k) or the stage
+    const uint8_t* sx = p.xr_stride > 0 ? smem + p.xr_off + k * 256 : sb + xoff;
+    const int xstride = p.xr_stride > 0 ? p.xr_stride : kXRowStride;
     float ag[1][4], au[1][4];
     float sg0, sg1, su0, su1;
     uint32_t zg0, zg1, zu0, zu1;
-    unit_dot<1, true, true>(sb, sb + xoff, p.M, r0, gid, tig, ag, sg0, sg1, zg0, zg1, 1, xzero);
-    unit_dot<1, true, true>(sb + kSbBytes, sb + xoff, p.M, r0, gid, tig, au, su0, su1, zu0, zu1, 1, xzero);
+    unit_dot<1, true, true>(sb, sx, p.M, r0, gid, tig, ag, sg0, sg1, zg0, zg1, 1, xzero, xstride);
+    unit_dot<1, true, true>(sb + kSbBytes, sx, p.M, r0, gid, tig, au, su0, su1, zu0, zu1, 1, xzero, xstride);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     const float2 xs = *reinterpret_cast<const float2*>(xsum + k * Mp + 2 * tig);
@@ -435,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
   const uint32_t xoff = UPS * kSbBytes;           // x slices follow the super-blocks
   const int g0 = u0 % p.G;
   const int nslot = (u1 - u0) < p.G ? (u1 - u0) : p.G;   // distinct groups, from g0 on (mod G)
-  const bool xr = !GLU && p.csize > 1 && p.xr_stride > 0;   // x region (cluster mode): no x in the stages
+  const bool xr = p.csize > 1 && p.xr_stride > 0;   // x region (cluster mode): no x in the stages
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
         if (lane == 0) {
           uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
           const size_t off = static_cast<size_t>(u0 + k) * kSbBytes;
-          mbar_arrive_expect_tx(&full[slot], 2u * kSbBytes + p.M * 256u);
+          mbar_arrive_expect_tx(&full[slot], 2u * kSbBytes + (xr ? 0u : p.M * 256u));
           bulk_g2s_hint(st, p.w + off, kSbBytes, &full[slot], pol);
           bulk_g2s_hint(st + kSbBytes, p.w_up + off, kSbBytes, &full[slot], pol);
         }
@@ -641,13 +645,14 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bo
   // contiguous run of groups) are loaded once, by the token-sum prologue,
   // into an x region; the stages then carry weights only and the producer
   // issues one weight copy per stage instead of one more 256-byte copy per
-  // token and group (QKV, M=8: 12.9 to ~10.5 us a launch).  Rows are an odd
-  // multiple of 64 bytes apart: conflict-free B-fragment loads.
-  for (int xr = (pl->csize > 1 && pl->NT == 1 && !glu) ? 1 : 0; xr >= 0; --xr) {
+  // token and group (chained launches at M=8: fused QKV 12.9 to 11.5 us; the
+  // decode MLP block's gate/up half, M=8: its block 26.7 to 24.3 us).  Rows
+  // are an odd multiple of 64 bytes apart: conflict-free B-fragment loads.
+  for (int xr = (pl->csize > 1 && pl->NT == 1) ? 1 : 0; xr >= 0; --xr) {
     pl->xr_stride = xr ? nslot * 256 + 64 : 0;
     const size_t xr_bytes = static_cast<size_t>(M) * pl->xr_stride;
     pl->stage_bytes = static_cast<uint32_t>(align_up(
-        glu ? 2 * static_cast<size_t>(kSbBytes) + static_cast<size_t>(M) * kXRowStride
+        glu ? 2 * static_cast<size_t>(kSbBytes) + (xr ? 0 : static_cast<size_t>(M) * kXRowStride)
             : static_cast<size_t>(pl->ups) *
                   (kSbBytes + (xr ? 0 : static_cast<size_t>(M) * kXRowStride) + (g64 ? kSbSide : 0)),
         128));
