@@ -331,6 +331,28 @@ def test_linear_stream_k_many_row_tiles(M):
     assert fl.fl_int4g_status(ws) == 0
 
 
+@pytest.mark.parametrize("M", [1, 8])
+def test_linear_cluster_long_k(M):
+    """A long-K decode linear (K=32768, N=1024: 8 row tiles, each split over
+    a cluster of 8 ranks of 32 groups).  At M=1 each rank keeps the x rows of
+    its K slice in an x region of shared memory; at M=8 that region (8 x 8 KB)
+    would leave fewer than three weight stages, so x travels in the stages.
+    66 sampled columns, the first and the last among them, against the
+    oracle."""
+    K, N = 32768, 1024
+    W = inputs.dense_weight(N, K, layer=K + M)
+    q, s, z = quantize_dev(W)
+    w = fl.fl_int4g_repack(q, s, z, N, K)
+    cols = np.unique(np.concatenate([np.sort(inputs.rng(9, K, N).choice(N, 64, replace=False)), [0, N - 1]]))
+    Qc, Sc, Zc = O.quantize(W[cols])
+    xb = inputs.activations(M, K, stream=K + M)
+    y = fl.fl_int4g_linear(bf16_dev(xb), w, N)
+    xf = O.bf16_value(xb)
+    ref, tol = O.linear_columns(xf, Qc, Sc, Zc, np.arange(len(cols)))
+    got = y.float().cpu().numpy().astype(np.float64)[:, cols]
+    assert np.all(np.abs(got - ref) <= tol), (M, np.max(np.abs(got - ref) / tol))
+
+
 def test_cluster_reduction_timeout_is_reported():
     """The failure path of the decode kernel's bounded inter-CTA wait, made
     to run out by the test hook (a barrier arrival nobody makes, 1 ms

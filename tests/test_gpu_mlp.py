@@ -93,6 +93,24 @@ def test_mlp_llama_full(M, one_launch):
     check(y1, ref, tol)
 
 
+@pytest.mark.parametrize("M", [1, 8])
+def test_mlp_long_hidden(M):
+    """H=16384, I=256: the gate/up half runs in clusters of 8 ranks of 16
+    groups.  At M=1 each rank keeps the x rows of its slice in an x region of
+    shared memory; at M=8 that region would leave fewer than three stages,
+    so x travels in the stages.  Every output against the oracle."""
+    H, I = 16384, 256
+    G, U, D, (g, u, d) = mlp_case(H, I, layer=1600)
+    xb = inputs.activations(M, H, stream=1600 + M)
+    ws = torch.zeros(fl.fl_int4g_mlp_workspace(M, H, I), dtype=torch.uint8, device=DEV)
+    x = to_dev(xb.view(np.int16)).view(torch.bfloat16)
+    y = fl.fl_int4g_mlp(x, g, u, d, I, ws=ws)
+    torch.cuda.synchronize()
+    assert fl.fl_int4g_status(ws) == 0
+    ref, tol = oracle_mlp(xb, G, U, D)
+    check(y, ref, tol)
+
+
 @pytest.mark.parametrize("one_launch", [False, True])
 def test_mlp_in_a_cuda_graph(one_launch):
     """Both forms (the cooperative launch among them) captured in a CUDA
