@@ -10,10 +10,13 @@
 //    tiles: equal contiguous ranges of super-blocks, one per CTA (stream-K),
 //    a tile shared by several CTAs finished by the last one to take its
 //    ticket (no waiting; partials summed in CTA order, deterministic);
-//  * one producer warp moves super-blocks and the matching 256-byte slices of
-//    every token row of x into a ring of shared-memory stages with 1-D bulk
-//    copies completing on mbarriers; the weights of the first stages are
-//    requested before the wait on the previous kernel (programmatic launch);
+//  * one producer warp moves super-blocks into a ring of shared-memory stages
+//    with 1-D bulk copies completing on mbarriers; the weights of the first
+//    stages are requested before the wait on the previous kernel
+//    (programmatic launch).  x: in cluster mode (M <= 8) the consumer warps
+//    load the x rows of their CTA's K slice once, into an x region, while
+//    they form the per-group token sums; otherwise the producer also copies
+//    the matching 256-byte slices of every token row of x into each stage;
 //  * 8 consumer warps each own 16 rows: 16 bytes of codes per lane and row
 //    become 8 bf16 pairs (128 + q) with one LOP3 each, the A operand of
 //    mma.sync m16n8k16 (the K order inside a group is permuted consistently
@@ -217,8 +220,8 @@ __device__ __forceinline__ void cluster_reduce(const RowsParams& p, int T, int r
 // GLU (the gate/up half of a decode MLP block, M <= 8, cluster mode): each
 // stage holds the gate and the up super-block of one (row tile, group) (and
 // that group's x rows when there is no x region); two folded sums per row;
-// rank 0 of the cluster adds
-// the ranks' gate and up sums in rank order and stores h = silu(gate) * up.
+// rank 0 of the cluster adds the ranks' gate and up sums in rank order and
+// stores h = silu(gate) * up.
 __device__ __forceinline__ void glu_reduce(const RowsParams& p, int T, int rank, int warp, int lane,
                                            const float (&tg)[4], const float (&tu)[4], uint64_t* red_bar,
                                            float* red_buf) {
