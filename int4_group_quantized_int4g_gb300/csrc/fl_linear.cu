@@ -541,16 +541,20 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
         const int i = it / p.M, m = it - i * p.M;
         int g = g0 + i;
         if (g >= p.G) g -= p.G;
-        const uint4* src =
-            reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K + g * kGroup) + part * 4;
+        // the thread's four 16-byte chunks of the group's 256 bytes: part + 4t
+        // (the four threads of a token read 64 contiguous bytes per load, and
+        // the eight threads of a store phase hit distinct bank groups); with
+        // groups of 64, 4 part + t (parts 0, 1: columns 0..63)
+        constexpr int kCs = G64 ? 1 : 4;   // chunk stride
+        const int c0 = G64 ? part * 4 : part;
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.K + g * kGroup) + c0;
         uint4 q[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) q[t] = __ldg(src + t);
+        for (int t = 0; t < 4; ++t) q[t] = __ldg(src + kCs * t);
         if (xr) {   // these 64 bytes of x into the region: token m, group slot i
-          uint4* dst = reinterpret_cast<uint4*>(smem + p.xr_off + static_cast<size_t>(m) * p.xr_stride + i * 256) +
-                       part * 4;
+          uint4* dst = reinterpret_cast<uint4*>(smem + p.xr_off + static_cast<size_t>(m) * p.xr_stride + i * 256) + c0;
 #pragma unroll
-          for (int t = 0; t < 4; ++t) dst[t] = q[t];
+          for (int t = 0; t < 4; ++t) dst[kCs * t] = q[t];
         }
         float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -564,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams
         }
         v = (a[0] + a[1]) + (a[2] + a[3]);
       }
-      // part 0, 1: columns 0..63 of the group, 2, 3: columns 64..127
+      // G64: part 0, 1 summed columns 0..63 of the group, 2, 3 columns 64..127
       v += __shfl_xor_sync(0xffffffffu, v, 1);
       if (G64) {
         if ((part & 1) == 0 && it < items) xsum[((it / p.M) * XS + (part >> 1)) * Mp + it % p.M] = v;
