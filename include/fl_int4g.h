@@ -168,7 +168,11 @@ int fl_int4g_linear(const void* x, int M, int K, const void* w, int N,
  * the layout as well (fl_int4g_repack with group 64), each 64-column group
  * with its own scale and zero point.  The workspace is the one
  * fl_int4g_linear_workspace returns.  Group 64 runs the mma.sync decode
- * kernel for every M <= 32 and the tcgen05 prefill GEMM above.
+ * kernel for every M <= 32 and the tcgen05 prefill GEMM above.  Its ring
+ * of stages sheds stages to fit 227 KB of shared memory; a shape that does
+ * not fit even with two (many tokens, very long K and many row tiles, as
+ * M = 32, K = 131072, N = 18432) returns FL_ERR_UNSUPPORTED before
+ * launching anything.
  * FL_ERR_UNSUPPORTED for other group sizes. */
 int fl_int4g_linear_g(const void* x, int M, int K, const void* w, int N, int group,
                       void* y, void* ws, size_t ws_bytes, fl_stream_t stream);
@@ -248,6 +252,20 @@ int fl_int4g_mlp_fused(const void* x, int M, int H, int I, const void* w_gate, c
  * default) turns the hook off.  Process-wide; for tests only.  Always
  * FL_OK. */
 int fl_int4g_test_withhold_cluster_arrival(long long ns);
+
+/* Test hook: the plan of the decode kernel (M <= 8 mma.sync stream, and the
+ * gate/up half of the decode MLP block when glu != 0) for one shape, computed
+ * on the host without touching a GPU.  sms: the SM count to plan for; group:
+ * 128 or 64; minb: CTAs per SM the kernel build holds (0: the default for M,
+ * 3: the three-per-SM build); max_cs: the largest cluster to consider (the
+ * launcher lowers it while clusters would crowd the GPU's capacity).
+ * out[0..10] receives T (row tiles), G (groups), P (CTAs), csize (cluster
+ * size, 1: stream-K), stages, stage bytes, dynamic shared memory bytes,
+ * x-region stride (0: x travels in the stages), x-region offset, reduction
+ * offset and zero-row offset.  FL_ERR_ARG for a shape the decode kernel
+ * does not take or a bad argument; for tests only. */
+int fl_int4g_test_decode_plan(int M, int N, int K, int sms, int group, int glu, int minb, int max_cs,
+                              long long* out);
 
 /* ------------------------------------------------------- a5-a7: MoE layer */
 

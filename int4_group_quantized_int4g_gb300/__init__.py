@@ -19,7 +19,7 @@ __all__ = [
     "fl_int4g_quantize", "fl_int4g_repacked_bytes", "fl_int4g_repack", "fl_int4g_unrepack",
     "fl_int4g_linear_workspace", "fl_int4g_linear", "fl_int4g_linear_noalloc", "fl_int4g_linear_noalloc_status",
     "fl_int4g_linear_g", "fl_moe_int4g_g",
-    "fl_int4g_test_withhold_cluster_arrival",
+    "fl_int4g_test_withhold_cluster_arrival", "fl_int4g_test_decode_plan",
     "fl_moe_int4g_workspace", "fl_moe_int4g", "fl_moe_int4g_ptrs", "FlMoeRouting", "fl_int4g_mlp_workspace",
     "fl_moe_router_logits_workspace", "fl_moe_router_logits",
     "fl_int4g_mlp", "fl_int4g_mlp_fused",
@@ -57,6 +57,7 @@ SIGNATURES = {
     "fl_int4g_linear_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp]),
     "fl_int4g_linear_noalloc_status": (_i, [_vp, ctypes.POINTER(_i)]),
     "fl_int4g_test_withhold_cluster_arrival": (_i, [ctypes.c_longlong]),
+    "fl_int4g_test_decode_plan": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_longlong)]),
     "fl_moe_int4g_workspace": (_i, [_i, _i, _i, _i, _i, _i, _c_size_p]),
     "fl_int4g_mlp_workspace": (_i, [_i, _i, _i, _c_size_p]),
     "fl_moe_router_logits_workspace": (_i, [_i, _i, _i, _c_size_p]),
@@ -249,6 +250,19 @@ def fl_int4g_test_withhold_cluster_arrival(ns):
     launches withhold one arrival, so their bounded wait runs out after ns
     nanoseconds and FL_ERR_TIMEOUT is recorded; ns < 0 turns it off."""
     lib().fl_int4g_test_withhold_cluster_arrival(int(ns))
+
+
+def fl_int4g_test_decode_plan(M, N, K, sms, group=GROUP, glu=False, minb=0, max_cs=8):
+    """Test hook: the decode kernel's plan for one shape, computed on the
+    host without a GPU.  A dict of T, G, P, csize, stages, stage_bytes, smem,
+    xr_stride, xr_off, red_off and zrow_off, or None when the kernel does not
+    take the shape."""
+    out = (ctypes.c_longlong * 11)()
+    rc = lib().fl_int4g_test_decode_plan(M, N, K, sms, group, int(bool(glu)), minb, max_cs, out)
+    if rc != 0:
+        return None
+    keys = ("T", "G", "P", "csize", "stages", "stage_bytes", "smem", "xr_stride", "xr_off", "red_off", "zrow_off")
+    return dict(zip(keys, list(out)))
 
 
 def fl_int4g_mlp_workspace(M, H, I):

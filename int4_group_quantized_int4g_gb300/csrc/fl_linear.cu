@@ -36,6 +36,7 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxTokens = 32;
+constexpr size_t kMaxDynSmem = 227u * 1024u;   // the kernel's dynamic shared-memory limit
 // Ticket counters live at a fixed offset with room for kMaxRowTiles row tiles,
 // so that a workspace reused across shapes never finds another shape's
 // scratch partial sums where its counters are (they must be zero on entry).
@@ -678,13 +679,21 @@ bool make_rows_plan(int M, int N, int K, int sms, RowsPlan* pl, int minb = 0, bo
     pl->stages = stages > 12 ? 12 : (stages < 2 ? 2 : static_cast<int>(stages));
     break;
   }
-  pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes + 2 * pl->stages * sizeof(uint64_t) + xsum_bytes;
-  pl->zrow_off = static_cast<uint32_t>(align_up(pl->smem, 16));
-  pl->smem = pl->zrow_off + 256;
-  pl->xr_off = static_cast<uint32_t>(align_up(pl->smem, 128));
-  if (pl->xr_stride) pl->smem = pl->xr_off + static_cast<size_t>(M) * pl->xr_stride;
-  pl->red_off = static_cast<uint32_t>(align_up(pl->smem, 16));
-  if (red_bytes) pl->smem = pl->red_off + red_bytes;
+  // The layout; a launch takes at most 227 KB of dynamic shared memory, so a
+  // plan above that (long K with many tokens, whose group sums take room)
+  // sheds stages, down to two.  A plan still above it is kept (its workspace
+  // offsets serve the tcgen05 decode too); the launchers refuse it.
+  for (;;) {
+    pl->smem = static_cast<size_t>(pl->stages) * pl->stage_bytes + 2 * pl->stages * sizeof(uint64_t) + xsum_bytes;
+    pl->zrow_off = static_cast<uint32_t>(align_up(pl->smem, 16));
+    pl->smem = pl->zrow_off + 256;
+    pl->xr_off = static_cast<uint32_t>(align_up(pl->smem, 128));
+    if (pl->xr_stride) pl->smem = pl->xr_off + static_cast<size_t>(M) * pl->xr_stride;
+    pl->red_off = static_cast<uint32_t>(align_up(pl->smem, 16));
+    if (red_bytes) pl->smem = pl->red_off + red_bytes;
+    if (pl->smem <= kMaxDynSmem || pl->stages <= 2) break;
+    --pl->stages;
+  }
   pl->cnt_off = kTicketOff;
   pl->part_off = kScratchOff;
   pl->ws_bytes = pl->part_off + static_cast<size_t>(pl->P + pl->T) * kRowTile * (8 * pl->NT) * 4;
@@ -697,7 +706,7 @@ bool rows_attr(int dev) {
   if (dev < 0 || dev >= 64) return false;
   if (!attr_done[dev]) {
     if (cudaFuncSetAttribute(k_linear_rows<NT, UPS, MINB, G64, GLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             227 * 1024) != cudaSuccess)
+                             static_cast<int>(kMaxDynSmem)) != cudaSuccess)
       return false;
     attr_done[dev] = true;
   }
@@ -773,6 +782,21 @@ extern "C" int fl_int4g_test_withhold_cluster_arrival(long long ns) {
   return FL_OK;
 }
 
+// Test hook: the decode kernel's plan for a shape, without a GPU.
+// out[0..10] = T, G, P, csize, stages, stage_bytes, dynamic shared memory,
+// x-region stride (0: x in the stages), x-region offset, reduction offset,
+// zero-row offset.
+extern "C" int fl_int4g_test_decode_plan(int M, int N, int K, int sms, int group, int glu, int minb, int max_cs,
+                                         long long* out) {
+  if (!out || (group != kGroup && group != kGroup / 2) || max_cs < 1) return FL_ERR_ARG;
+  RowsPlan pl;
+  if (!make_rows_plan(M, N, K, sms, &pl, minb, group == kGroup / 2, glu != 0, max_cs)) return FL_ERR_ARG;
+  const long long v[11] = {pl.T, pl.G, pl.P, pl.csize, pl.stages, pl.stage_bytes, static_cast<long long>(pl.smem),
+                           pl.xr_stride, pl.xr_off, pl.red_off, pl.zrow_off};
+  for (int i = 0; i < 11; ++i) out[i] = v[i];
+  return FL_OK;
+}
+
 // Shared with the MoE and prefill launchers.
 int fl_linear_rows_workspace(int M, int N, int K, size_t* out) {
   RowsPlan pl;
@@ -802,6 +826,7 @@ int fl_linear_rows(const void* x, int M, int K, const void* w, int N, void* y, v
     }
     if (cap > 0 && pl.T > cap - 2 && !make_rows_plan(M, N, K, flh::sm_count(), &pl, 3, g64)) return FL_ERR_ARG;
   }
+  if (pl.smem > kMaxDynSmem) return FL_ERR_UNSUPPORTED;   // even two stages do not fit
   RowsParams prm;
   prm.w = static_cast<const uint8_t*>(w);
   prm.side = g64 ? static_cast<const uint8_t*>(w) + static_cast<size_t>(pl.U) * kSbBytes : nullptr;
@@ -855,6 +880,7 @@ int fl_linear_glu(const void* x, int M, int H, const void* w_gate, const void* w
   RowsPlan pl;
   if (!make_rows_plan(M, I, H, flh::sm_count(), &pl, 0, false, true)) return FL_ERR_UNSUPPORTED;
   if (ws_bytes < pl.ws_bytes) return FL_ERR_WORKSPACE;
+  if (pl.smem > kMaxDynSmem) return FL_ERR_UNSUPPORTED;
   const int cap = rows_cluster_capacity(pl);
   if (cap > 0 && pl.T > cap - 2) return FL_ERR_UNSUPPORTED;   // a second wave of clusters: not worth it
   RowsParams prm;

@@ -91,3 +91,66 @@ def test_argument_errors_are_caught_on_the_host(L):
     assert moe_ex(8, 2, fl.FL_SIGMOID, 0x20004, 1, 1, 1.0) == 1      # misaligned bias
     assert moe_ex(8, 2, fl.FL_SIGMOID, None, 1, 1, 0.0) == 1         # routed_scale must be positive
     assert moe_ex(8, 2, fl.FL_SIGMOID, None, 1, 1, float("inf")) == 1
+
+
+def test_decode_plan_fits_shared_memory(L):
+    """The decode kernel's plans (host arithmetic, no GPU) over a sweep of
+    shapes.  Every plan fits the 227 KB launch limit, or has shed its ring to
+    two stages (the launchers then refuse it); the two-per-SM build (M <= 8)
+    fits two CTAs per SM; an x region appears only in cluster mode with one
+    token tile and at least three stages, its token rows an odd multiple of
+    64 bytes apart (conflict-free B-fragment loads), long enough for a rank's
+    groups and placed between the zero row and the reduction buffer."""
+    KB = 1024
+    n = 0
+    for M in (1, 2, 5, 8, 9, 16, 17, 32):
+        for K in (128, 384, 1024, 4096, 7168, 11008, 16384, 28672, 65536):
+            for N in (1, 200, 1024, 3072, 4096, 7168, 11008, 12288, 14336, 32000, 152064):
+                for group in (128, 64):
+                    for glu in ((0, 1) if M <= 8 else (0,)):
+                        for minb in ((0, 3) if M <= 8 else (0,)):
+                            for max_cs in (8, 2, 1):
+                                p = fl.fl_int4g_test_decode_plan(M, N, K, 152, group, glu, minb, max_cs)
+                                if p is None:
+                                    assert glu, (M, N, K, group, minb, max_cs)   # only the GLU half declines
+                                    continue
+                                n += 1
+                                where = (M, N, K, group, glu, minb, max_cs, p)
+                                assert p["stage_bytes"] % 128 == 0 and p["stages"] >= 2, where
+                                assert p["smem"] <= 227 * KB or p["stages"] == 2, where
+                                if M <= 8 and minb == 0:
+                                    assert p["smem"] <= 113 * KB, where
+                                assert p["stages"] * (p["stage_bytes"] + 16) <= p["zrow_off"], where
+                                assert p["red_off"] <= p["smem"], where
+                                if p["xr_stride"] > 0:
+                                    assert M <= 8 and p["csize"] > 1 and p["stages"] >= 3, where
+                                    assert p["xr_stride"] % 128 == 64, where
+                                    assert p["xr_stride"] >= -(-p["G"] // p["csize"]) * 256, where
+                                    assert p["xr_off"] % 128 == 0 and p["xr_off"] >= p["zrow_off"] + 256, where
+                                    assert p["xr_off"] + M * p["xr_stride"] <= p["red_off"], where
+    assert n > 3000
+
+
+def test_decode_plan_x_region_choice(L):
+    """The Llama- and Qwen-shaped decode linears and the Llama MLP block's
+    gate/up half take the x region at every M <= 8; the long-K shapes of the
+    GPU parity tests take it at M=1 and fall back to x in the stages at M=8."""
+    for M in range(1, 9):
+        for K, N, max_cs in ((4096, 12288, 2), (4096, 11008, 8), (11008, 4096, 8), (4096, 4096, 8), (1024, 3072, 8)):
+            assert fl.fl_int4g_test_decode_plan(M, N, K, 152, max_cs=max_cs)["xr_stride"] > 0, (M, K, N)
+        assert fl.fl_int4g_test_decode_plan(M, 11008, 4096, 152, glu=True)["xr_stride"] > 0, M
+    for glu, K, N in ((False, 32768, 1024), (True, 16384, 256)):
+        assert fl.fl_int4g_test_decode_plan(1, N, K, 152, glu=glu)["xr_stride"] > 0
+        assert fl.fl_int4g_test_decode_plan(8, N, K, 152, glu=glu)["xr_stride"] == 0
+    # stream-K (many row tiles) keeps x in the stages
+    assert fl.fl_int4g_test_decode_plan(1, 32000, 4096, 152)["csize"] == 1
+    assert fl.fl_int4g_test_decode_plan(1, 32000, 4096, 152)["xr_stride"] == 0
+    assert fl.fl_int4g_test_decode_plan(1, 0, 4096, 152) is None
+
+
+def test_decode_plan_sheds_stages_to_fit(L):
+    """Groups of 64 at M=32, K=28672, N=7168 (the GPU parity case): the ring
+    is cut to fit the 227 KB launch limit, one stage short of overflowing."""
+    p = fl.fl_int4g_test_decode_plan(32, 7168, 28672, 152, group=64)
+    assert p["smem"] <= 227 * 1024 < p["smem"] + p["stage_bytes"] + 16
+    assert p["stages"] > 2

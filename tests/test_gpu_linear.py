@@ -198,6 +198,26 @@ def test_linear_group64_llama_sampled():
         assert np.all(np.abs(got - ref) <= tol), (M, np.max(np.abs(got - ref) / tol))
 
 
+def test_linear_group64_long_k_many_tokens():
+    """Groups of 64 at M=32 with K=28672 (N=7168): the decode kernel's plan
+    would take ten 19 KB stages and overflow the 227 KB shared-memory limit;
+    it runs with nine.  64 sampled columns, the first and the last among
+    them, against the oracle's group-64 linear."""
+    M, K, N = 32, 28672, 7168
+    W = inputs.dense_weight(N, K, layer=64065)
+    q, s_, z = fl.fl_int4g_quantize(to_dev(W), group=64)
+    w = fl.fl_int4g_repack(q, s_, z, N, K, group=64)
+    cols = np.unique(np.concatenate([np.sort(inputs.rng(10, K, N).choice(N, 64, replace=False)), [0, N - 1]]))
+    Qc, Sc, Zc = O.quantize(W[cols], 64)
+    del W
+    xb = inputs.activations(M, K, stream=M + 65)
+    y = fl.fl_int4g_linear(bf16_dev(xb), w, N, group=64)
+    xf = O.bf16_value(xb)
+    ref, tol = O.linear(xf, Qc, Sc, Zc, 64), O.linear_tolerance(xf, Qc, Sc, Zc, 64)
+    got = y.float().cpu().numpy().astype(np.float64)[:, cols]
+    assert np.all(np.abs(got - ref) <= tol), np.max(np.abs(got - ref) / tol)
+
+
 @pytest.mark.parametrize("M", [1, 8, 9, 32, 64, 300])
 def test_linear_group256_parity(M):
     """Decode (rows and tcgen05 kernels) and prefill on group-256 weights,
