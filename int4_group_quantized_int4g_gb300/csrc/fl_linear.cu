@@ -411,9 +411,10 @@ __device__ __forceinline__ void rows_consume(const RowsParams& p, uint8_t* smem,
 
 // NT token tiles of 8; UPS super-blocks per pipeline stage (2 gives each
 // warp two independent MMA chains and 17 KB bulk copies).  MINB CTAs per SM:
-// 2 (M <= 8, ~100 KB of stages each), 3 (M <= 8 when the row tiles' clusters
-// would fill the GPU's cluster capacity at 2: smaller stages, fewer
-// registers, so that every cluster is resident in one wave) or 1 (M > 8).
+// 2 (M <= 8, up to 113 KB of shared memory each), 3 (M <= 8 when the row
+// tiles' clusters would fill the GPU's cluster capacity at 2: smaller
+// stages, fewer registers, so that every cluster is resident in one wave)
+// or 1 (M > 8).
 template <int NT, int UPS, int MINB, bool G64, bool GLU = false>
 __global__ void __launch_bounds__(kThreads, MINB) k_linear_rows(const RowsParams p) {
   static_assert(!GLU || (NT == 1 && UPS == 2 && !G64), "GLU: one token tile, the gate and up super-blocks per stage");
